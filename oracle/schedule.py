@@ -1,0 +1,206 @@
+"""Oracle: per-stage F/B/W orders and a unit-time simulator of all p stages.
+
+TEST INFRASTRUCTURE (see the package docstring).  Pure Python, small inputs.
+
+Model ("Zero-Bubble Pipeline Parallelism Guide for LLMs", section
+"Mathematical Modeling: Bubble Fractions, Memory Bounds, and Speedups"):
+every op takes one time unit (t_F = t_B = t_W), communication is free.
+Dependencies, for stage s and microbatch i:
+  F(s, i) after F(s-1, i)                       (activations flow down)
+  B(s, i) after F(s, i) and after the backward of stage s+1 for i
+  W(s, i) after B(s, i)                         (section "Core Innovation 1")
+plus each stage's own program order.  When the backward is not split
+(GPipe, 1F1B), stage s+1 sends its input gradient only once its whole
+backward, B and W, is done, so B(s, i) then waits for W(s+1, i).
+
+Orders:
+* GPipe (section "1. The GPipe Bubble"): all m forwards, then all backwards.
+* 1F1B (section "2. The 1F1B (One-Forward-One-Backward) Schedule" and the
+  first diagram of "The Mechanics of Pipeline Bubbles"): stage s runs p-s
+  forwards before its first backward, then alternates B and F, then drains
+  the remaining B.  W is written right after its B.
+* ZB-H1, the guide's ZB-1F1B (section "Core Innovation 2": same memory as
+  1F1B, F and B prioritised, a W fills every slot that would otherwise be
+  idle, steady F -> B -> W rhythm, the W left over are drained at the end;
+  section "Memory Management & Activation Rollback": a hard ceiling on
+  in-flight microbatches, and at the ceiling a W must run before the next F).
+  Reading: the stage keeps the 1F1B order of its F and B; whenever it is free
+  it runs that next F/B if its inputs are there, except that an F that would
+  pass the ceiling (F issued minus W issued = ``limit``, default p) yields to
+  the oldest pending W; when the next F/B is not ready it runs the oldest
+  pending W; otherwise it idles.  The listing's fourth rule (an F past the
+  ceiling) contradicts that hard ceiling and is not used.  The listing's
+  first three rules alone do not give the section's own (p-1)/(3m) bubble
+  (at p=4, m=8 they take 29 units where this reading takes 3m+p-1 = 27).
+"""
+from __future__ import annotations
+
+F, B, W = "F", "B", "W"
+
+
+def order_gpipe(s, p, m):
+    """All forwards, then each backward as B followed by its W."""
+    out = [(F, i) for i in range(m)]
+    for i in range(m):
+        out += [(B, i), (W, i)]
+    return out
+
+
+def order_1f1b(s, p, m):
+    """1F1B for stage s: p-s forwards before the first B, then B/F alternate."""
+    warm = min(p - s - 1, m)
+    out = [(F, i) for i in range(warm)]
+    for j in range(m - warm):
+        out += [(F, warm + j), (B, j), (W, j)]
+    for i in range(m - warm, m):
+        out += [(B, i), (W, i)]
+    return out
+
+
+def _deps(kind, s, i, p, split):
+    """Ops (kind, stage, mb) that must finish before (kind, s, i) may start."""
+    if kind == F:
+        return [(F, s - 1, i)] if s > 0 else []
+    if kind == B:
+        d = [(F, s, i)]
+        if s < p - 1:
+            d.append((B if split else W, s + 1, i))
+        return d
+    return [(B, s, i)]
+
+
+def simulate_orders(orders, p, split):
+    """Run fixed per-stage orders as early as the dependencies allow.
+
+    Returns a dict (kind, stage, mb) -> start time.  Raises if the orders
+    deadlock.
+    """
+    start = {}
+    finish = {}
+    ptr = [0] * p
+    free_at = [0] * p
+    total = sum(len(o) for o in orders)
+    while len(start) < total:
+        progressed = False
+        for s in range(p):
+            while ptr[s] < len(orders[s]):
+                kind, i = orders[s][ptr[s]]
+                deps = _deps(kind, s, i, p, split)
+                if any(d not in finish for d in deps):
+                    break
+                t0 = max([free_at[s]] + [finish[d] for d in deps])
+                start[(kind, s, i)] = t0
+                finish[(kind, s, i)] = t0 + 1
+                free_at[s] = t0 + 1
+                ptr[s] += 1
+                progressed = True
+        if not progressed:
+            raise RuntimeError("orders deadlock")
+    return start
+
+
+def simulate_zbh1(p, m, limit=None):
+    """Time-stepped run of the ZB-H1 policy on all p stages.
+
+    Returns (orders, start): per-stage lists of (kind, mb) and the start time
+    of every op.
+    """
+    if limit is None:
+        limit = p
+    fb = [[op for op in order_1f1b(s, p, m) if op[0] != W] for s in range(p)]
+    ptr = [0] * p
+    orders = [[] for _ in range(p)]
+    start = {}
+    finish = {}
+    f_issued = [0] * p
+    w_issued = [0] * p
+    pending_w = [[] for _ in range(p)]  # oldest first
+    busy_until = [0] * p
+    t = 0
+    total = 3 * m * p
+    while len(start) < total:
+        if t > 100 * (m + p) + 100:
+            raise RuntimeError("zbh1 simulation did not finish")
+        decided = []
+        for s in range(p):
+            if busy_until[s] > t:
+                continue
+            op = None
+            if ptr[s] < len(fb[s]):
+                kind, i = fb[s][ptr[s]]
+                ready = all(d in finish and finish[d] <= t for d in _deps(kind, s, i, p, True))
+                if ready:
+                    if kind == F and f_issued[s] - w_issued[s] >= limit:
+                        if pending_w[s]:
+                            op = (W, pending_w[s][0])
+                    else:
+                        op = (kind, i)
+                elif pending_w[s]:
+                    op = (W, pending_w[s][0])
+            elif pending_w[s]:
+                op = (W, pending_w[s][0])
+            if op is not None:
+                decided.append((s, op))
+        # all stages decide on the state at time t, then the ops are applied
+        for s, (kind, i) in decided:
+            start[(kind, s, i)] = t
+            finish[(kind, s, i)] = t + 1
+            busy_until[s] = t + 1
+            orders[s].append((kind, i))
+            if kind == W:
+                pending_w[s].pop(0)
+                w_issued[s] += 1
+            else:
+                ptr[s] += 1
+                if kind == F:
+                    f_issued[s] += 1
+                else:
+                    pending_w[s].append(i)
+        t += 1
+    return orders, start
+
+
+def orders_for(kind, p, m):
+    """Per-stage orders for "gpipe", "1f1b" or "zbh1"."""
+    if kind == "gpipe":
+        return [order_gpipe(s, p, m) for s in range(p)]
+    if kind == "1f1b":
+        return [order_1f1b(s, p, m) for s in range(p)]
+    if kind == "zbh1":
+        return simulate_zbh1(p, m)[0]
+    raise ValueError(kind)
+
+
+def timeline(kind, p, m):
+    """(orders, start times) of a schedule under the unit-time model."""
+    orders = orders_for(kind, p, m)
+    split = kind == "zbh1"
+    return orders, simulate_orders(orders, p, split)
+
+
+def makespan(start):
+    return max(start.values()) + 1
+
+
+def bubble(kind, p, m):
+    """Idle time of the pipeline under the unit-time model.
+
+    Returns (idle / compute, idle / wall): compute is the 3m units each stage
+    works, wall is the makespan, both summed over the p stages.
+    """
+    _, start = timeline(kind, p, m)
+    span = makespan(start)
+    idle = p * span - 3 * m * p
+    return idle / (3 * m * p), idle / (p * span)
+
+
+def peak_in_flight(order):
+    """Largest number of microbatches whose F has run and whose W has not."""
+    cur = peak = 0
+    for kind, _ in order:
+        if kind == F:
+            cur += 1
+            peak = max(peak, cur)
+        elif kind == W:
+            cur -= 1
+    return peak
