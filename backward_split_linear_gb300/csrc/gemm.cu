@@ -1,0 +1,414 @@
+// Persistent tcgen05 GEMM for sm_103a with fused epilogues.
+//
+// One CTA per SM walks output tiles of BM x BN = 128 x 256.  Warp roles:
+//   warp 0   one thread issues TMA tile loads into a 4-stage shared-memory ring
+//   warp 1   allocates tensor memory; one thread issues tcgen05.mma (bf16 in,
+//            f32 accumulate) into one of two 128 x 256 f32 accumulators
+//   warps 2-5 epilogue: tcgen05.ld the accumulator (one row per thread), apply
+//            the fused op, store to global memory
+// Two accumulators (512 tensor-memory columns) let the epilogue of one tile run
+// while the MMAs of the next tile fill the other.
+//
+// Operand layouts (the three GEMMs of a split backward, "Zero-Bubble Pipeline
+// Parallelism Guide for LLMs", "Core Innovation 1"; weights [out, in] as in
+// its "Step-by-Step Implementation"):
+//   Forward        y  = x w^T    A = x  [M=T, K=in]  K-major, B = w [N=out, K=in] K-major
+//   BackwardInput  dx = dy w     A = dy [M=T, K=out] K-major, B = w [K=out, N=in] MN-major
+//   BackwardWeight dw += dy^T x  A = dy [K=T, M=out] MN-major, B = x [K=T, N=in] MN-major
+// All tiles use 128-byte swizzling.  A K-major tile is rows of 64 bf16 (128 B);
+// an MN-major tile is BK rows of 64 MN-elements per 64-wide block, one TMA box
+// per block.  Out-of-range rows and columns of a box read as zero, so ragged
+// M, N and K need no special mainloop; the epilogue masks rows >= M, cols >= N.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace zbk {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kAStageBytes = BM * BK * 2;   // 16 KiB
+constexpr uint32_t kBStageBytes = BN * BK * 2;   // 32 KiB
+constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
+constexpr uint32_t kMnBlockBytes = 64 * BK * 2;  // one 64-wide MN block of an MN-major tile
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kNumBars = 2 * STAGES + 5;
+constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + kNumBars * 8 + 16;
+
+struct KParams {
+    int m, n, k;
+    int tiles_m, num_tiles, k_blocks;
+    void* out;
+    int64_t ldo;
+    const void* aux;
+    int64_t ld_aux;
+    int ffn;
+    int* status;
+    // MN-major 128B-swizzled operands: the leading-dimension offset steps between
+    // 64-element MN blocks, the stride-dimension offset between 8-row K groups.
+    uint32_t mn_lbo;
+    uint32_t mn_sbo;
+};
+
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const KParams& p, int m, int n, const uint32_t (&r)[32],
+                                               const uint4 (&x0)[4], const uint4 (&x1)[4]) {
+    if constexpr (EPI == static_cast<int>(Epilogue::AccumF32)) {
+        float* dst = static_cast<float*>(p.out) + static_cast<int64_t>(m) * p.ldo + n;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * j),
+                         "f"(__uint_as_float(r[4 * j])), "f"(__uint_as_float(r[4 * j + 1])),
+                         "f"(__uint_as_float(r[4 * j + 2])), "f"(__uint_as_float(r[4 * j + 3]))
+                         : "memory");
+        }
+    } else if constexpr (EPI == static_cast<int>(Epilogue::SwigluBwd)) {
+        uint16_t* base = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(m) * p.ldo;
+        uint4* dg_dst = reinterpret_cast<uint4*>(base + n);
+        uint4* du_dst = reinterpret_cast<uint4*>(base + p.ffn + n);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t gw[4] = {x0[j].x, x0[j].y, x0[j].z, x0[j].w};
+            const uint32_t uw[4] = {x1[j].x, x1[j].y, x1[j].z, x1[j].w};
+            uint32_t dgw[4], duw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float dg2[2], du2[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float ds = __uint_as_float(r[8 * j + 2 * e + h]);
+                    const float g = h ? bf16_hi(gw[e]) : bf16_lo(gw[e]);
+                    const float u = h ? bf16_hi(uw[e]) : bf16_lo(uw[e]);
+                    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+                    dg2[h] = ds * u * sg * (1.0f + g * (1.0f - sg));
+                    du2[h] = ds * g * sg;
+                }
+                dgw[e] = pack_bf16x2(dg2[0], dg2[1]);
+                duw[e] = pack_bf16x2(du2[0], du2[1]);
+            }
+            dg_dst[j] = make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
+            du_dst[j] = make_uint4(duw[0], duw[1], duw[2], duw[3]);
+        }
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                              static_cast<int64_t>(m) * p.ldo + n);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[8 * j + e]);
+            if constexpr (EPI == static_cast<int>(Epilogue::AddResidual)) {
+                const uint32_t rw[4] = {x0[j].x, x0[j].y, x0[j].z, x0[j].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[2 * e] += bf16_lo(rw[e]);
+                    v[2 * e + 1] += bf16_hi(rw[e]);
+                }
+            }
+            dst[j] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        }
+    }
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t s_a = base;
+    const uint32_t s_b = base + STAGES * kAStageBytes;
+    const uint32_t bars = s_b + STAGES * kBStageBytes;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bars + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bars + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+    const uint32_t tmem_slot = bars + 8u * kNumBars;
+    volatile uint32_t* tmem_slot_ptr =
+        reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 128);
+        }
+        mbar_init(drain_bar, 1);
+        mbar_fence_init();
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            uint32_t issued[STAGES];
+            for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                const int m0 = (tile % p.tiles_m) * BM;
+                const int n0 = (tile / p.tiles_m) * BN;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    const int k0 = kb * BK;
+                    const uint32_t a_dst = s_a + stage * kAStageBytes;
+                    const uint32_t b_dst = s_b + stage * kBStageBytes;
+                    if constexpr (A_MN) {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j)
+                            tma_load_2d(a_dst + j * kMnBlockBytes, &map_a, fb, m0 + 64 * j, k0);
+                    } else {
+                        tma_load_2d(a_dst, &map_a, fb, k0, m0);
+                    }
+                    if constexpr (B_MN) {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(b_dst + j * kMnBlockBytes, &map_b, fb, n0 + 64 * j, k0);
+                    } else {
+                        tma_load_2d(b_dst, &map_b, fb, k0, n0);
+                    }
+                    ++issued[stage];
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every load issued must land before the CTA's shared memory goes away.
+            for (int s = 0; s < STAGES; ++s)
+                if (issued[s] > 0)
+                    mbar_wait(full_bar(s), (issued[s] - 1u) & 1u, p.status, kSiteDrain,
+                              kWaitLimitNs);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = mma_idesc_bf16(BM, BN, A_MN, B_MN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t aph = (static_cast<uint32_t>(it) >> 1) & 1u;
+                if (!mbar_wait(tempty_bar(acc), aph ^ 1u, p.status, kSiteMmaTmemEmpty)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, p.status, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = s_a + stage * kAStageBytes;
+                    const uint32_t b0 = s_b + stage * kBStageBytes;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        // K-major: the 16-element K step is 32 bytes inside the
+                        // 128-byte swizzled row; MN-major: it is 16 rows of 128 B.
+                        const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, p.mn_lbo, p.mn_sbo)
+                                                 : smem_desc_sw128(a0 + k * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, p.mn_lbo, p.mn_sbo)
+                                                 : smem_desc_sw128(b0 + k * 32, 16, 1024);
+                        umma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(acc));
+            }
+            // No MMA may still run when tensor memory is freed.
+            umma_commit(drain_bar);
+            mbar_wait(drain_bar, 0, p.status, kSiteDrain, kWaitLimitNs);
+        }
+    } else {
+        // ---------------- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t aph = (static_cast<uint32_t>(it) >> 1) & 1u;
+            if (!mbar_wait(tfull_bar(acc), aph, p.status, kSiteEpiTmemFull)) break;
+            tc_fence_after();
+            const int m = (tile % p.tiles_m) * BM + row;
+            const int n_base = (tile / p.tiles_m) * BN;
+            const bool row_ok = m < p.m;
+            const uint32_t tbase =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int n = n_base + c * 32;
+                const bool ok = row_ok && n < p.n;
+                uint4 x0[4], x1[4];
+                if constexpr (EPI == static_cast<int>(Epilogue::AddResidual) ||
+                              EPI == static_cast<int>(Epilogue::SwigluBwd)) {
+                    if (ok) {
+                        const uint16_t* rowp =
+                            static_cast<const uint16_t*>(p.aux) + static_cast<int64_t>(m) * p.ld_aux;
+                        const uint4* s0 = reinterpret_cast<const uint4*>(rowp + n);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) x0[j] = s0[j];
+                        if constexpr (EPI == static_cast<int>(Epilogue::SwigluBwd)) {
+                            const uint4* s1 = reinterpret_cast<const uint4*>(rowp + p.ffn + n);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) x1[j] = s1[j];
+                        }
+                    }
+                }
+                uint32_t r[32];
+                tmem_load_32(tbase + static_cast<uint32_t>(c * 32), r);
+                tmem_wait_load();
+                if (c == BN / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(tempty_bar(acc));
+                }
+                if (ok) epilogue_chunk<EPI>(p, m, n, r, x0, x1);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix of `rows` x `cols` with row stride `ld` elements,
+// boxes of box_cols x box_rows, 128-byte swizzle, zero fill out of range.
+bool encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& p,
+                           cudaStream_t stream) {
+    auto kern = gemm_kernel<A_MN, B_MN, EPI>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kSmemBytes));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
+    if (g.m <= 0 || g.n <= 0 || g.k <= 0) return cudaSuccess;
+    CUtensorMap ma, mb;
+    bool ok = true;
+    switch (g.kind) {
+        case GemmKind::Forward:
+            ok = encode_map(&ma, g.a, g.m, g.k, g.lda, 64, BM) &&
+                 encode_map(&mb, g.b, g.n, g.k, g.ldb, 64, BN);
+            break;
+        case GemmKind::BackwardInput:
+            ok = encode_map(&ma, g.a, g.m, g.k, g.lda, 64, BM) &&
+                 encode_map(&mb, g.b, g.k, g.n, g.ldb, 64, BK);
+            break;
+        case GemmKind::BackwardWeight:
+            ok = encode_map(&ma, g.a, g.k, g.m, g.lda, 64, BK) &&
+                 encode_map(&mb, g.b, g.k, g.n, g.ldb, 64, BK);
+            break;
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    KParams p;
+    p.m = g.m;
+    p.n = g.n;
+    p.k = g.k;
+    p.tiles_m = (g.m + BM - 1) / BM;
+    p.num_tiles = p.tiles_m * ((g.n + BN - 1) / BN);
+    p.k_blocks = (g.k + BK - 1) / BK;
+    p.out = g.out;
+    p.ldo = g.ldo;
+    p.aux = g.aux;
+    p.ld_aux = g.ld_aux;
+    p.ffn = g.ffn;
+    p.status = status_word();
+    p.mn_lbo = kMnBlockBytes;
+    p.mn_sbo = 1024;
+    if (!p.status) return cudaErrorInvalidDevice;
+    constexpr int kStore = static_cast<int>(Epilogue::StoreBf16);
+    constexpr int kResid = static_cast<int>(Epilogue::AddResidual);
+    constexpr int kSwiglu = static_cast<int>(Epilogue::SwigluBwd);
+    constexpr int kAccum = static_cast<int>(Epilogue::AccumF32);
+    switch (g.kind) {
+        case GemmKind::Forward:
+            if (g.epi == Epilogue::StoreBf16) return launch_variant<false, false, kStore>(ma, mb, p, stream);
+            if (g.epi == Epilogue::AddResidual) return launch_variant<false, false, kResid>(ma, mb, p, stream);
+            break;
+        case GemmKind::BackwardInput:
+            if (g.epi == Epilogue::StoreBf16) return launch_variant<false, true, kStore>(ma, mb, p, stream);
+            if (g.epi == Epilogue::SwigluBwd) return launch_variant<false, true, kSwiglu>(ma, mb, p, stream);
+            break;
+        case GemmKind::BackwardWeight:
+            if (g.epi == Epilogue::AccumF32) return launch_variant<true, true, kAccum>(ma, mb, p, stream);
+            break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace zbk

@@ -1,0 +1,379 @@
+// Memory-bound kernels of the stage: RMSNorm forward / input backward, the
+// RMSNorm gamma-gradient reduction, SwiGLU forward and the attention stand-in.
+// All of them stream bf16 rows with 16-byte vector accesses (8 elements per
+// access); per-row reductions use warp shuffles and one shared-memory step.
+#include <mutex>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace zbk {
+
+namespace {
+
+__device__ int g_status_word;  // see zb_device_status
+
+constexpr int kRowThreads = 256;
+
+struct V8 {
+    float v[8];
+};
+
+__device__ __forceinline__ V8 load8(const uint16_t* p) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    V8 r;
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        r.v[2 * e] = bf16_lo(w[e]);
+        r.v[2 * e + 1] = bf16_hi(w[e]);
+    }
+    return r;
+}
+
+__device__ __forceinline__ void store8(uint16_t* p, const float (&v)[8]) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                              pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = 0.f;
+    if (threadIdx.x < 32) {
+        s = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) red[0] = s;
+    }
+    __syncthreads();
+    s = red[0];
+    __syncthreads();
+    return s;
+}
+
+// ---------------------------------------------------------------- RMSNorm forward
+// One block per row; thread t owns 8-element chunks t, t + 256, ... (VPT of them).
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_fwd_kernel(const uint16_t* __restrict__ x,
+                                                                  const float* __restrict__ gamma,
+                                                                  float eps, uint16_t* __restrict__ n,
+                                                                  float* __restrict__ rstd, int hidden) {
+    __shared__ float red[32];
+    const int64_t row = blockIdx.x;
+    const int chunks = hidden >> 3;
+    const uint16_t* xr = x + row * hidden;
+    V8 xv[VPT];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int c = threadIdx.x + i * kRowThreads;
+        if (c < chunks) {
+            xv[i] = load8(xr + 8 * c);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss += xv[i].v[e] * xv[i].v[e];
+        }
+    }
+    const float r = rsqrtf(block_sum(ss, red) / static_cast<float>(hidden) + eps);
+    if (threadIdx.x == 0) rstd[row] = r;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int c = threadIdx.x + i * kRowThreads;
+        if (c < chunks) {
+            const float4 g0 = *reinterpret_cast<const float4*>(gamma + 8 * c);
+            const float4 g1 = *reinterpret_cast<const float4*>(gamma + 8 * c + 4);
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = g[e] * (xv[i].v[e] * r);
+            store8(n + row * hidden + 8 * c, o);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- RMSNorm input backward
+// dx = dres + r (gamma dn - xh * mean(gamma dn xh)), xh = x r.
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_kernel(
+    const uint16_t* __restrict__ dn, const uint16_t* __restrict__ x, const float* __restrict__ rstd,
+    const float* __restrict__ gamma, const uint16_t* dres, uint16_t* dx, int hidden) {
+    __shared__ float red[32];
+    const int64_t row = blockIdx.x;
+    const int chunks = hidden >> 3;
+    const float r = rstd[row];
+    V8 gd[VPT], xh[VPT];
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int c = threadIdx.x + i * kRowThreads;
+        if (c < chunks) {
+            const V8 dv = load8(dn + row * hidden + 8 * c);
+            const V8 xv = load8(x + row * hidden + 8 * c);
+            const float4 g0 = *reinterpret_cast<const float4*>(gamma + 8 * c);
+            const float4 g1 = *reinterpret_cast<const float4*>(gamma + 8 * c + 4);
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                gd[i].v[e] = g[e] * dv.v[e];
+                xh[i].v[e] = xv.v[e] * r;
+                dot += gd[i].v[e] * xh[i].v[e];
+            }
+        }
+    }
+    const float mean = block_sum(dot, red) / static_cast<float>(hidden);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int c = threadIdx.x + i * kRowThreads;
+        if (c < chunks) {
+            const V8 rv = load8(dres + row * hidden + 8 * c);
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = rv.v[e] + r * (gd[i].v[e] - xh[i].v[e] * mean);
+            store8(dx + row * hidden + 8 * c, o);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- RMSNorm gamma gradient
+// Pass 1: block (cx, cy) sums rows [cy * R, cy * R + R) for 8-column chunk
+// cx * 256 + t into part[cy][...].  Pass 2: dgamma[j] += sum over cy in order.
+constexpr int kGammaRows = 32;
+
+__global__ void __launch_bounds__(kRowThreads) dgamma_partial_kernel(
+    const uint16_t* __restrict__ dn, const uint16_t* __restrict__ x, const float* __restrict__ rstd,
+    float* __restrict__ part, int tokens, int hidden) {
+    const int c = blockIdx.x * kRowThreads + threadIdx.x;
+    if (c >= (hidden >> 3)) return;
+    const int t0 = blockIdx.y * kGammaRows;
+    const int t1 = min(tokens, t0 + kGammaRows);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int t = t0; t < t1; ++t) {
+        const float r = rstd[t];
+        const V8 dv = load8(dn + static_cast<int64_t>(t) * hidden + 8 * c);
+        const V8 xv = load8(x + static_cast<int64_t>(t) * hidden + 8 * c);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += dv.v[e] * (xv.v[e] * r);
+    }
+    float4* dst = reinterpret_cast<float4*>(part + static_cast<int64_t>(blockIdx.y) * hidden + 8 * c);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+__global__ void dgamma_final_kernel(const float* __restrict__ part, int parts, float* dgamma,
+                                    int hidden) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= hidden) return;
+    float s = 0.f;
+    for (int q = 0; q < parts; ++q) s += part[static_cast<int64_t>(q) * hidden + j];
+    dgamma[j] += s;
+}
+
+// ---------------------------------------------------------------- SwiGLU forward
+__global__ void swiglu_fwd_kernel(const uint16_t* __restrict__ gu, uint16_t* __restrict__ s,
+                                  int tokens, int ffn) {
+    const int cpr = ffn >> 3;
+    const int64_t total = static_cast<int64_t>(tokens) * cpr;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / cpr;
+        const int c = static_cast<int>(i - t * cpr);
+        const uint16_t* row = gu + t * 2 * ffn;
+        const V8 g = load8(row + 8 * c);
+        const V8 u = load8(row + ffn + 8 * c);
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = g.v[e] * __fdividef(1.0f, 1.0f + __expf(-g.v[e])) * u.v[e];
+        store8(s + t * ffn + 8 * c, o);
+    }
+}
+
+// ---------------------------------------------------------------- attention stand-in
+// a[:, h] = q_h + k_j + v_j with j = h / (nh / nkv); qkv row = [q heads | k heads | v heads].
+__global__ void attn_fwd_kernel(const uint16_t* __restrict__ qkv, uint16_t* __restrict__ a,
+                                int tokens, int nh, int nkv, int hd) {
+    const int width = nh * hd;
+    const int qkv_w = (nh + 2 * nkv) * hd;
+    const int group = nh / nkv;
+    const int cpr = width >> 3;
+    const int64_t total = static_cast<int64_t>(tokens) * cpr;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / cpr;
+        const int col = 8 * static_cast<int>(i - t * cpr);
+        const int h = col / hd, off = col - h * hd;
+        const int j = h / group;
+        const uint16_t* row = qkv + t * qkv_w;
+        const V8 q = load8(row + col);
+        const V8 k = load8(row + width + j * hd + off);
+        const V8 v = load8(row + width + nkv * hd + j * hd + off);
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = q.v[e] + k.v[e] + v.v[e];
+        store8(a + t * width + col, o);
+    }
+}
+
+// dqkv holds da in its q columns; writes dk_j = dv_j = sum over the heads of group j.
+__global__ void attn_bwd_kv_kernel(uint16_t* dqkv, int tokens, int nh, int nkv, int hd) {
+    const int width = nh * hd;
+    const int qkv_w = (nh + 2 * nkv) * hd;
+    const int group = nh / nkv;
+    const int cpr = (nkv * hd) >> 3;
+    const int64_t total = static_cast<int64_t>(tokens) * cpr;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / cpr;
+        const int col = 8 * static_cast<int>(i - t * cpr);  // inside the k block
+        const int j = col / hd, off = col - j * hd;
+        uint16_t* row = dqkv + t * qkv_w;
+        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int h = j * group; h < (j + 1) * group; ++h) {
+            const V8 d = load8(row + h * hd + off);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s[e] += d.v[e];
+        }
+        store8(row + width + col, s);
+        store8(row + width + nkv * hd + col, s);
+    }
+}
+
+// ---------------------------------------------------------------- self test
+__global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    mbar_fence_init();
+    // Nothing ever arrives: the bounded wait must give up and record the site.
+    mbar_wait(b, 0, status, kSiteSelftest, limit_ns);
+}
+
+int grid_for(int64_t items, int threads) {
+    const int64_t blocks = (items + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+    return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+
+int* status_word() {
+    static int* ptrs[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+int sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (!counts[dev]) {
+        int c = 0;
+        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+        counts[dev] = c > 0 ? c : 1;
+    }
+    return counts[dev];
+}
+
+int device_arch() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return -1;
+    return major * 10 + minor;
+}
+
+#define ZB_ROW_DISPATCH(KERNEL, VPT_NEEDED, ...)                                          \
+    do {                                                                                  \
+        if ((VPT_NEEDED) <= 1) KERNEL<1><<<grid, kRowThreads, 0, stream>>>(__VA_ARGS__);  \
+        else if ((VPT_NEEDED) <= 2) KERNEL<2><<<grid, kRowThreads, 0, stream>>>(__VA_ARGS__); \
+        else if ((VPT_NEEDED) <= 4) KERNEL<4><<<grid, kRowThreads, 0, stream>>>(__VA_ARGS__); \
+        else KERNEL<8><<<grid, kRowThreads, 0, stream>>>(__VA_ARGS__);                    \
+    } while (0)
+
+cudaError_t launch_rmsnorm_forward(const void* x, const float* gamma, float eps, void* n,
+                                   float* rstd, int tokens, int hidden, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const int vpt = (hidden / 8 + kRowThreads - 1) / kRowThreads;
+    const int grid = tokens;
+    ZB_ROW_DISPATCH(rmsnorm_fwd_kernel, vpt, static_cast<const uint16_t*>(x), gamma, eps,
+                    static_cast<uint16_t*>(n), rstd, hidden);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_backward_input(const void* dn, const void* x, const float* rstd,
+                                          const float* gamma, const void* dres, void* dx,
+                                          int tokens, int hidden, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const int vpt = (hidden / 8 + kRowThreads - 1) / kRowThreads;
+    const int grid = tokens;
+    ZB_ROW_DISPATCH(rmsnorm_bwd_kernel, vpt, static_cast<const uint16_t*>(dn),
+                    static_cast<const uint16_t*>(x), rstd, gamma, static_cast<const uint16_t*>(dres),
+                    static_cast<uint16_t*>(dx), hidden);
+    return cudaGetLastError();
+}
+
+size_t rmsnorm_gamma_scratch_bytes(int tokens, int hidden) {
+    if (tokens <= 0 || hidden <= 0) return 0;
+    const size_t parts = (static_cast<size_t>(tokens) + kGammaRows - 1) / kGammaRows;
+    return parts * static_cast<size_t>(hidden) * sizeof(float);
+}
+
+cudaError_t launch_rmsnorm_backward_gamma(const void* dn, const void* x, const float* rstd,
+                                          float* dgamma, int tokens, int hidden, float* scratch,
+                                          cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const int parts = (tokens + kGammaRows - 1) / kGammaRows;
+    const dim3 grid1((hidden / 8 + kRowThreads - 1) / kRowThreads, parts);
+    dgamma_partial_kernel<<<grid1, kRowThreads, 0, stream>>>(static_cast<const uint16_t*>(dn),
+                                                            static_cast<const uint16_t*>(x), rstd,
+                                                            scratch, tokens, hidden);
+    dgamma_final_kernel<<<(hidden + 255) / 256, 256, 0, stream>>>(scratch, parts, dgamma, hidden);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_forward(const void* gu, void* s, int tokens, int ffn, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const int64_t items = static_cast<int64_t>(tokens) * (ffn / 8);
+    swiglu_fwd_kernel<<<grid_for(items, 256), 256, 0, stream>>>(static_cast<const uint16_t*>(gu),
+                                                                static_cast<uint16_t*>(s), tokens, ffn);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention_forward(const void* qkv, void* a, int tokens, int n_heads,
+                                     int n_kv_heads, int head_dim, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const int64_t items = static_cast<int64_t>(tokens) * (n_heads * head_dim / 8);
+    attn_fwd_kernel<<<grid_for(items, 256), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(qkv), static_cast<uint16_t*>(a), tokens, n_heads, n_kv_heads,
+        head_dim);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention_backward_kv(void* dqkv, int tokens, int n_heads, int n_kv_heads,
+                                         int head_dim, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const int64_t items = static_cast<int64_t>(tokens) * (n_kv_heads * head_dim / 8);
+    attn_bwd_kv_kernel<<<grid_for(items, 256), 256, 0, stream>>>(static_cast<uint16_t*>(dqkv), tokens,
+                                                                 n_heads, n_kv_heads, head_dim);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(int limit_us, cudaStream_t stream) {
+    int* st = status_word();
+    if (!st) return cudaErrorInvalidDevice;
+    selftest_wait_kernel<<<1, 1, 0, stream>>>(st, static_cast<uint64_t>(limit_us) * 1000ull);
+    return cudaGetLastError();
+}
+
+}  // namespace zbk

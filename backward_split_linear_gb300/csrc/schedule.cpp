@@ -1,0 +1,237 @@
+// F/B/W order of one pipeline stage (CPU only) and the unit-time pipeline model.
+//
+// "Zero-Bubble Pipeline Parallelism Guide for LLMs":
+//  - section "2. The 1F1B (One-Forward-One-Backward) Schedule" and the first
+//    diagram of "The Mechanics of Pipeline Bubbles": stage s runs p - s
+//    forwards before its first backward, then alternates B and F;
+//  - section "Core Innovation 2" (ZB-1F1B, here ZB-H1): same activation memory
+//    as 1F1B, F and B keep priority, a W fills each slot that would idle, the
+//    steady state runs F -> B -> W, leftover W drain at the end;
+//  - section "Memory Management & Activation Rollback": at the in-flight
+//    ceiling a W must run before the next F;
+//  - section "Mathematical Modeling": unit op times, bubble formulas.
+//
+// ZB-H1, m >= p, in closed form for stage s:
+//   F_0 .. F_{p-s-1}
+//   B_j, F_{p-s+j}            for j = 0 .. s-1
+//   B_{s+k}, W_k, F_{p+k}     for k = 0 .. m-p-1     (steady F -> B -> W)
+//   B_{s+k}, W_k              for k = m-p .. m-s-1
+//   W_k                       for k = m-s .. m-1     (drain)
+// It keeps the 1F1B F/B order, never holds more than p microbatches and ends
+// every stage at 3m + p - 1 units.  For m < p the same policy is run step by
+// step over all stages instead.
+#include <algorithm>
+#include <vector>
+
+#include "../../include/zb.h"
+
+namespace {
+
+struct Op {
+    char kind;
+    int mb;
+};
+
+void order_gpipe(int, int, int m, std::vector<Op>& o) {
+    for (int i = 0; i < m; ++i) o.push_back({'F', i});
+    for (int i = 0; i < m; ++i) {
+        o.push_back({'B', i});
+        o.push_back({'W', i});
+    }
+}
+
+void order_1f1b(int s, int p, int m, std::vector<Op>& o) {
+    const int warm = std::min(p - s - 1, m);
+    for (int i = 0; i < warm; ++i) o.push_back({'F', i});
+    for (int j = 0; j < m - warm; ++j) {
+        o.push_back({'F', warm + j});
+        o.push_back({'B', j});
+        o.push_back({'W', j});
+    }
+    for (int i = m - warm; i < m; ++i) {
+        o.push_back({'B', i});
+        o.push_back({'W', i});
+    }
+}
+
+void order_zbh1_closed(int s, int p, int m, std::vector<Op>& o) {
+    for (int i = 0; i < p - s; ++i) o.push_back({'F', i});
+    for (int j = 0; j < s; ++j) {
+        o.push_back({'B', j});
+        o.push_back({'F', p - s + j});
+    }
+    for (int k = 0; k < m - p; ++k) {
+        o.push_back({'B', s + k});
+        o.push_back({'W', k});
+        o.push_back({'F', p + k});
+    }
+    for (int k = m - p; k < m - s; ++k) {
+        o.push_back({'B', s + k});
+        o.push_back({'W', k});
+    }
+    for (int k = m - s; k < m; ++k) o.push_back({'W', k});
+}
+
+// Step-by-step run of the ZB-H1 policy on all p stages (used when m < p).
+// At every unit of time each free stage, looking at the state at that time:
+// runs its next F/B (1F1B order) if that op's inputs exist, unless it is an
+// F that would pass the ceiling of p held microbatches, in which case it runs
+// its oldest pending W; if the next F/B is not ready it runs the oldest
+// pending W; else it idles.
+std::vector<std::vector<Op>> zbh1_policy_all(int p, int m) {
+    std::vector<std::vector<Op>> fb(p), out(p);
+    for (int s = 0; s < p; ++s) {
+        std::vector<Op> o;
+        order_1f1b(s, p, m, o);
+        for (const Op& op : o)
+            if (op.kind != 'W') fb[s].push_back(op);
+    }
+    // finish time of F/B per (stage, mb); -1 = not run
+    std::vector<int> fin_f(p * m, -1), fin_b(p * m, -1);
+    std::vector<size_t> ptr(p, 0);
+    std::vector<int> held(p, 0), busy(p, 0);
+    std::vector<std::vector<int>> pending(p);
+    int done = 0;
+    const int total = 3 * m * p;
+    for (int t = 0; done < total && t < 64 * (m + p) + 64; ++t) {
+        std::vector<Op> choice(p, Op{0, -1});
+        for (int s = 0; s < p; ++s) {
+            if (busy[s] > t) continue;
+            if (ptr[s] < fb[s].size()) {
+                const Op nx = fb[s][ptr[s]];
+                bool ready;
+                if (nx.kind == 'F')
+                    ready = s == 0 || (fin_f[(s - 1) * m + nx.mb] >= 0 && fin_f[(s - 1) * m + nx.mb] <= t);
+                else
+                    ready = fin_f[s * m + nx.mb] >= 0 && fin_f[s * m + nx.mb] <= t &&
+                            (s == p - 1 || (fin_b[(s + 1) * m + nx.mb] >= 0 && fin_b[(s + 1) * m + nx.mb] <= t));
+                if (ready) {
+                    if (nx.kind == 'F' && held[s] >= p) {
+                        if (!pending[s].empty()) choice[s] = {'W', pending[s].front()};
+                    } else {
+                        choice[s] = nx;
+                    }
+                } else if (!pending[s].empty()) {
+                    choice[s] = {'W', pending[s].front()};
+                }
+            } else if (!pending[s].empty()) {
+                choice[s] = {'W', pending[s].front()};
+            }
+        }
+        for (int s = 0; s < p; ++s) {
+            const Op op = choice[s];
+            if (op.mb < 0) continue;
+            busy[s] = t + 1;
+            out[s].push_back(op);
+            ++done;
+            if (op.kind == 'W') {
+                pending[s].erase(pending[s].begin());
+                --held[s];
+            } else {
+                ++ptr[s];
+                if (op.kind == 'F') {
+                    fin_f[s * m + op.mb] = t + 1;
+                    ++held[s];
+                } else {
+                    fin_b[s * m + op.mb] = t + 1;
+                    pending[s].push_back(op.mb);
+                }
+            }
+        }
+    }
+    return out;
+}
+
+void stage_order(zb_sched_kind kind, int s, int p, int m, std::vector<Op>& o) {
+    if (kind == ZB_SCHED_GPIPE) {
+        order_gpipe(s, p, m, o);
+    } else if (kind == ZB_SCHED_1F1B) {
+        order_1f1b(s, p, m, o);
+    } else if (m >= p) {
+        order_zbh1_closed(s, p, m, o);
+    } else {
+        o = zbh1_policy_all(p, m)[s];
+    }
+}
+
+bool valid_kind(int k) { return k == ZB_SCHED_1F1B || k == ZB_SCHED_ZBH1 || k == ZB_SCHED_GPIPE; }
+
+}  // namespace
+
+extern "C" zb_status zb_schedule(zb_sched_kind kind, int32_t stage, int32_t p, int32_t m, zb_op* out,
+                                 int32_t cap, int32_t* n_out) {
+    if (!valid_kind(kind) || p < 1 || m < 1 || stage < 0 || stage >= p || !n_out ||
+        (cap > 0 && !out) || cap < 0 || m > (1 << 24))
+        return ZB_ERR_ARG;
+    *n_out = 3 * m;
+    if (cap < 3 * m) return ZB_ERR_CAPACITY;
+    std::vector<Op> o;
+    o.reserve(3 * m);
+    stage_order(kind, stage, p, m, o);
+    for (int i = 0; i < 3 * m; ++i) {
+        out[i].kind = static_cast<uint8_t>(o[i].kind);
+        out[i].pad[0] = out[i].pad[1] = out[i].pad[2] = 0;
+        out[i].mb = o[i].mb;
+    }
+    return ZB_OK;
+}
+
+extern "C" zb_status zb_schedule_bubble(zb_sched_kind kind, int32_t p, int32_t m, int32_t* makespan,
+                                        double* idle_over_compute, double* idle_over_wall) {
+    if (!valid_kind(kind) || p < 1 || m < 1 || p > 4096 || m > (1 << 20)) return ZB_ERR_ARG;
+    const bool split = kind == ZB_SCHED_ZBH1;
+    std::vector<std::vector<Op>> orders(p);
+    for (int s = 0; s < p; ++s) stage_order(kind, s, p, m, orders[s]);
+    // finish times per (kind, stage, mb)
+    auto idx = [m](int s, int i) { return s * m + i; };
+    std::vector<int> ff(p * m, -1), fb(p * m, -1), fw(p * m, -1);
+    std::vector<size_t> ptr(p, 0);
+    std::vector<int> free_at(p, 0);
+    size_t placed = 0, total = static_cast<size_t>(3) * m * p;
+    int span = 0;
+    while (placed < total) {
+        bool progressed = false;
+        for (int s = 0; s < p; ++s) {
+            while (ptr[s] < orders[s].size()) {
+                const Op op = orders[s][ptr[s]];
+                int ready = free_at[s];
+                bool ok = true;
+                if (op.kind == 'F') {
+                    if (s > 0) {
+                        const int d = ff[idx(s - 1, op.mb)];
+                        ok = d >= 0;
+                        ready = std::max(ready, d);
+                    }
+                } else if (op.kind == 'B') {
+                    const int d0 = ff[idx(s, op.mb)];
+                    ok = d0 >= 0;
+                    ready = std::max(ready, d0);
+                    if (s < p - 1) {
+                        const int d1 = split ? fb[idx(s + 1, op.mb)] : fw[idx(s + 1, op.mb)];
+                        ok = ok && d1 >= 0;
+                        ready = std::max(ready, d1);
+                    }
+                } else {
+                    const int d = fb[idx(s, op.mb)];
+                    ok = d >= 0;
+                    ready = std::max(ready, d);
+                }
+                if (!ok) break;
+                const int fin = ready + 1;
+                (op.kind == 'F' ? ff : op.kind == 'B' ? fb : fw)[idx(s, op.mb)] = fin;
+                free_at[s] = fin;
+                span = std::max(span, fin);
+                ++ptr[s];
+                ++placed;
+                progressed = true;
+            }
+        }
+        if (!progressed) return ZB_ERR_ORDER;  // orders deadlock (cannot happen for valid kinds)
+    }
+    const double compute = 3.0 * m * p;
+    const double idle = static_cast<double>(p) * span - compute;
+    if (makespan) *makespan = span;
+    if (idle_over_compute) *idle_over_compute = idle / compute;
+    if (idle_over_wall) *idle_over_wall = idle / (static_cast<double>(p) * span);
+    return ZB_OK;
+}

@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""B and W backward TFLOP/s of one pipeline stage on GB300 (bf16, float32 accumulation).
+
+A step is one iteration of the stage over m microbatches in the ZB-H1 order
+the library generates (stage 0 of a p = m pipeline: F of every microbatch,
+then B and W alternating): F, B and W of every microbatch, all through the C
+ABI on one CUDA stream.  CUDA events around every B call and every W call
+(on that stream) give the B and W device time; F runs inside the step but is
+not part of the metric.  ``value`` = (B GEMM FLOPs + W GEMM FLOPs) / (B time +
+W time) over the K timed steps.  ``e2e`` is the same metric with host buffers:
+each step copies x and dy of every microbatch from pinned host memory,
+runs F / B / W and copies dx back, all inside the timed region.
+
+Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+     python bench.py --impl reference   (the float64 oracle on the host cores)
+Under torchrun each rank runs its own replica (weak scaling, no collective on
+the data path); the barrier and the max over ranks only frame the timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "llama8b_stage": dict(kind="transformer", n_layers=4, hidden=4096, ffn=14336, n_heads=32, n_kv_heads=8,
+                          head_dim=128, tokens=4096, m=8),
+    "llama70b_stage": dict(kind="transformer", n_layers=2, hidden=8192, ffn=28672, n_heads=64, n_kv_heads=8,
+                           head_dim=128, tokens=4096, m=8),
+    "tiny_stage": dict(kind="mlp", n_layers=2, hidden=256, ffn=1024, n_heads=0, n_kv_heads=0, head_dim=0,
+                       tokens=128, m=4),
+}
+for _t in (512, 1024, 2048, 4096, 8192):
+    WORKLOADS[f"wgrad_sweep_t{_t}"] = dict(kind="linear", n_layers=1, hidden=4096, ffn=14336, n_heads=0,
+                                           n_kv_heads=0, head_dim=0, tokens=_t, m=4)
+
+METRIC = "B and W backward TFLOP/s per stage (bf16, 1xGB300) and % of dense tensor peak"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def gemm_flops_per_mb(w):
+    """Algorithmic GEMM FLOPs of one microbatch for one pass (B or W): 2 T in out per linear."""
+    t, h, f = w["tokens"], w["hidden"], w["ffn"]
+    if w["kind"] == "linear":
+        return 2.0 * t * h * f
+    per_layer = 2.0 * t * (2 * f * h + h * f)
+    if w["kind"] == "transformer":
+        q = (w["n_heads"] + 2 * w["n_kv_heads"]) * w["head_dim"]
+        per_layer += 2.0 * t * (q * h + h * h)
+    return per_layer * w["n_layers"]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            if self.path:
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if s > 0.5 * max(sm)]
+        return {"sm_mhz": statistics.median(loaded or sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+# ---------------------------------------------------------------- oracle (host) leg
+
+
+def oracle_sample(w, sample_tokens, seed=0, params_f64=None):
+    """Times the float64 oracle's B and W for one microbatch of `sample_tokens` tokens."""
+    import numpy as np
+
+    from backward_split_linear_gb300 import synth
+    from oracle import stage as S
+
+    shp = dict(kind=w["kind"], n_layers=w["n_layers"], hidden=w["hidden"], ffn=w["ffn"], n_heads=w["n_heads"],
+               n_kv_heads=w["n_kv_heads"], head_dim=w["head_dim"], eps=1e-5)
+    if params_f64 is None:
+        inp = synth.stage_inputs(w["kind"], w["n_layers"], w["hidden"], w["ffn"], w["n_heads"], w["n_kv_heads"],
+                                 w["head_dim"], tokens=sample_tokens, n_mb=1, seed=seed, gamma="ones")
+        params_f64 = synth.params_f64(inp["params"])
+        x, dy = synth.bf16_to_f64(inp["x"][0]), synth.bf16_to_f64(inp["dy"][0])
+    else:
+        rng = np.random.default_rng(seed + 1)
+        out = w["ffn"] if w["kind"] == "linear" else w["hidden"]
+        x = synth.bf16_to_f64(synth.bf16_bits(rng.standard_normal((sample_tokens, w["hidden"]), dtype=np.float32)))
+        dy = synth.bf16_to_f64(synth.bf16_bits(rng.standard_normal((sample_tokens, out), dtype=np.float32)))
+    _, saved = S.stage_forward(x, params_f64, shp)
+    t0 = time.perf_counter()
+    _, kept = S.stage_backward_input(dy, params_f64, saved, shp)
+    t1 = time.perf_counter()
+    acc = S.zero_grads(params_f64)
+    S.stage_backward_weight(acc, saved, kept, shp)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1, params_f64
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return None
+
+
+def cpu_baseline(w, sample_tokens):
+    tb, tw, _ = oracle_sample(w, sample_tokens)
+    flops = 2 * gemm_flops_per_mb(dict(w, tokens=sample_tokens))
+    cores = len(os.sched_getaffinity(0))
+    return {"value": flops / (tb + tw) / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "blas_threads": blas_threads(),
+            "sample": f"B and W of one {sample_tokens}-token microbatch of the {w['n_layers']}-layer stage "
+                      f"(float64 numpy, F untimed); B {tb:.2f} s, W {tw:.2f} s"}
+
+
+def run_reference(args, w):
+    """--impl reference: the float64 oracle timed on the host cores, same metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    sample = args.sample_tokens
+    _, _, params = oracle_sample(w, sample)  # builds the parameters once (untimed)
+    for _ in range(args.warmup):
+        oracle_sample(w, sample, params_f64=params)
+    tb = tw = 0.0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        b, wt, _ = oracle_sample(w, sample, seed=k, params_f64=params)
+        tb += b
+        tw += wt
+    wall = time.perf_counter() - t0
+    flops = 2 * gemm_flops_per_mb(dict(w, tokens=sample)) * args.steps
+    value = flops / (tb + tw) / 1e12
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * (tb + tw) / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "tokens_per_step": sample, "wall_s": wall},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "blas_threads": blas_threads(),
+                             "sample": f"each step: B and W of one {sample}-token microbatch of the stage"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU leg
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    from backward_split_linear_gb300 import binding as zb
+    from backward_split_linear_gb300 import synth
+    from backward_split_linear_gb300.runtime import Stage, bf16_from_bits
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    __graft_entry__.build()
+
+    t, m = w["tokens"], w["m"]
+    inp = synth.stage_inputs(w["kind"], w["n_layers"], w["hidden"], w["ffn"], w["n_heads"], w["n_kv_heads"],
+                             w["head_dim"], tokens=t, n_mb=m, seed=rank, gamma="ones")
+    st = Stage.from_synth(w["kind"], w["n_layers"], w["hidden"], w["ffn"], w["n_heads"], w["n_kv_heads"],
+                          w["head_dim"], 1e-5, t, m, inp["params"])
+    xs = [bf16_from_bits(b) for b in inp["x"]]
+    dys = [bf16_from_bits(b) for b in inp["dy"]]
+    out_dim = st.out_dim
+    ys = [torch.empty(t, out_dim, dtype=torch.bfloat16, device="cuda") for _ in range(m)]
+    dxs = [torch.empty(t, w["hidden"], dtype=torch.bfloat16, device="cuda") for _ in range(m)]
+    order = zb.zb_schedule("zbh1", 0, m, m)
+    stream = torch.cuda.current_stream()
+    n_b = sum(1 for k, _ in order if k == "B")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * n_b)]
+
+    def step(record):
+        i_ev = 0
+        spans = []
+        for kind, mb in order:
+            if kind == "F":
+                st.forward(mb, xs[mb], ys[mb], stream)
+                continue
+            a, b = ev[i_ev]
+            i_ev += 1
+            if record:
+                a.record(stream)
+            if kind == "B":
+                st.backward_input(mb, dys[mb], dxs[mb], stream)
+            else:
+                st.backward_weight(mb, stream)
+            if record:
+                b.record(stream)
+                spans.append((kind, a, b))
+        return spans
+
+    st.set_tracing(True)
+    for _ in range(args.warmup):
+        step(False)
+    st.sync()
+    st.read_tracing(reset=True)
+    st.zero_grads()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    b_ms = w_ms = 0.0
+    with ClockSampler(local) as clocks:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        all_spans = []
+        for _ in range(args.steps):
+            all_spans.append(step(True))
+        t_end.record(stream)
+        barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    for spans in all_spans:
+        for kind, a, b in spans:
+            if kind == "B":
+                b_ms += a.elapsed_time(b)
+            else:
+                w_ms += a.elapsed_time(b)
+    trace = st.read_tracing(reset=True)
+    st.sync()
+    launches = sum(c["launches"] for c in trace.values())
+
+    flops_mb = gemm_flops_per_mb(w)
+    b_flops = flops_mb * m * args.steps
+    w_flops = flops_mb * m * args.steps
+    bw_ms = b_ms + w_ms
+    if dist is not None:
+        tt = torch.tensor([bw_ms, b_ms, w_ms, total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        bw_ms, b_ms, w_ms, total_ms = tt.tolist()
+    value = world * (b_flops + w_flops) / (bw_ms * 1e-3) / 1e12
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hx = [torch.empty(t, w["hidden"], dtype=torch.bfloat16, pin_memory=True) for _ in range(m)]
+        hdy = [torch.empty(t, out_dim, dtype=torch.bfloat16, pin_memory=True) for _ in range(m)]
+        hdx = [torch.empty(t, w["hidden"], dtype=torch.bfloat16, pin_memory=True) for _ in range(m)]
+        for i in range(m):
+            hx[i].copy_(xs[i])
+            hdy[i].copy_(dys[i])
+        st.set_tracing(False)
+
+        def e2e_step():
+            for i in range(m):
+                xs[i].copy_(hx[i], non_blocking=True)
+                dys[i].copy_(hdy[i], non_blocking=True)
+            step(False)
+            for i in range(m):
+                hdx[i].copy_(dxs[i], non_blocking=True)
+
+        e2e_step()
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 3))
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        barrier()
+        e_ms = a.elapsed_time(b) / n_e2e
+        h2d = sum(x.numel() * 2 for x in hx) + sum(x.numel() * 2 for x in hdy)
+        d2h = sum(x.numel() * 2 for x in hdx)
+        e2e = {"value": world * 2 * flops_mb * m / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "note": "B+W GEMM FLOPs over the whole step: H2D of x and dy, F, B, W, D2H of dx"}
+
+    peaks = measured_peaks()
+    gemm = {k: trace[k] for k in ("gemm_backward_input", "gemm_backward_weight")}
+    g_ms = sum(c["ms"] for c in gemm.values())
+    g_launch = sum(c["launches"] for c in gemm.values())
+    g_flops = sum(c["flops"] for c in gemm.values())
+    g_ach = g_flops / (g_ms * 1e-3) / 1e12
+    rows = {k: trace[k] for k in ("row_backward_input", "row_backward_weight")}
+    r_ms = sum(c["ms"] for c in rows.values())
+    r_bytes = sum(c["bytes"] for c in rows.values())
+    r_ach = r_bytes / (r_ms * 1e-3) / 1e9 if r_ms > 0 else None
+    roofline = {"bound": "tensor", "kernel": "gemm_kernel (B and W GEMMs, tcgen05)",
+                "achieved": g_ach, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": g_ach / peaks["bf16_tflops_sustained"], "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
+                "launches": g_launch, "flops_per_launch": g_flops / max(1, g_launch),
+                "ms_per_launch": g_ms / max(1, g_launch)}
+    roofline_rows = None
+    if r_ach is not None:
+        roofline_rows = {"bound": "hbm", "kernel": "B/W row kernels (RMSNorm backward, stand-in backward, "
+                                                   "gamma reduction, dy stash copy)",
+                         "achieved": r_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": r_ach / peaks["hbm_gbs"],
+                         "traffic": None, "launches": sum(c["launches"] for c in rows.values()),
+                         "share_of_bw_time": r_ms / bw_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.sample_tokens if w["kind"] != "mlp" else w["tokens"])
+
+    if rank == 0:
+        cs = clocks.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": bw_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "b_tflops": world * b_flops / (b_ms * 1e-3) / 1e12,
+            "w_tflops": world * w_flops / (w_ms * 1e-3) / 1e12,
+            "pct_of_dense_bf16_peak": {
+                "b": 100 * b_flops / (b_ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
+                "w": 100 * w_flops / (w_ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
+                "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peaks["source"] + " sustained"},
+            "step_ms_with_forward": total_ms / args.steps,
+            "config": {"workload": args.workload, **{k: v for k, v in w.items()},
+                       "order": "ZB-H1 order of stage 0, p = m (library generator)",
+                       "timed": "CUDA events around each B and W call; F runs in the step, untimed",
+                       "l2": "inputs larger than L2 (stash per microbatch far above 129 MB)",
+                       "gamma": "ones", "seed": rank},
+            "roofline": roofline, "roofline_rows": roofline_rows,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"], "reasons": cs["reasons"],
+                       "samples": cs["samples"]},
+            "trace": {k: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k, v in trace.items()},
+        }
+        print(json.dumps(line), flush=True)
+    st.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b_stage")
+    ap.add_argument("--sample-tokens", type=int, default=256,
+                    help="tokens of the microbatch the host oracle runs (cpu_baseline / reference arm)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

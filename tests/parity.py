@@ -1,0 +1,50 @@
+"""Tolerances and comparison helpers for the GPU-vs-oracle tests.
+
+Per step (one kernel or one fused op on seeded bf16 inputs, float32
+accumulation) the bar is the stated one: relative Frobenius error <= 5e-3 and
+max-abs error <= 2e-2 * max|ref|.
+
+A whole stage chains many such steps, and each one rounds its tensor-core
+operand to bf16 (RMS relative error about 1.6e-3 per rounding, independent
+from step to step).  A layer puts four rounded GEMM operands on the forward
+path and four on the backward path, so errors grow like the square root of
+the number of chained steps.  Whole-stage comparisons against the exact
+float64 oracle therefore use Frobenius <= 5e-3 * sqrt(4 L) for L layers
+(1e-2 for one layer, 2e-2 for four), and keep max-abs <= 2e-2 * max|ref|.
+"""
+import numpy as np
+
+FRO_TOL = 5e-3
+MAX_TOL = 2e-2
+
+
+def stage_fro_tol(n_layers):
+    return FRO_TOL * float(np.sqrt(4 * n_layers))
+
+
+def errors(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    nref = np.linalg.norm(ref)
+    mref = np.max(np.abs(ref)) if ref.size else 0.0
+    diff = got - ref
+    fro = np.linalg.norm(diff) / nref if nref > 0 else np.linalg.norm(diff)
+    mx = np.max(np.abs(diff)) / mref if mref > 0 else (np.max(np.abs(diff)) if diff.size else 0.0)
+    return float(fro), float(mx)
+
+
+def assert_close(got, ref, what="", fro_tol=FRO_TOL, max_tol=MAX_TOL):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    fro, mx = errors(got, ref)
+    assert fro <= fro_tol and mx <= max_tol, f"{what}: frobenius {fro:.3e} (tol {fro_tol:.1e}), max {mx:.3e} (tol {max_tol:.1e})"
+    return fro, mx
+
+
+def draw_bf16(rng, shape, std=1.0):
+    """Seeded N(0, std^2) values rounded to bf16: (bits, float64 values)."""
+    from backward_split_linear_gb300 import synth
+
+    bits = synth.bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(std))
+    return bits, synth.bf16_to_f64(bits)

@@ -1,0 +1,133 @@
+"""libzb checks that need no GPU: exports, the schedule generator, host-side argument checks."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from backward_split_linear_gb300 import binding as zb
+from oracle import schedule as S
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "zb.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zb_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(zblib):
+    names = header_functions()
+    assert len(names) >= 25
+    for name in names:
+        assert hasattr(zblib, name), name
+    assert sorted(zb.declared_symbols()) == names
+
+
+def test_version_and_status_strings(zblib):
+    assert zb.zb_version() == 100
+    for code in zb.STATUS_NAMES:
+        assert zb.zb_status_string(code) != "unknown status"
+
+
+@pytest.mark.parametrize("kind", ["1f1b", "zbh1", "gpipe"])
+def test_generator_equals_oracle(zblib, kind):
+    """The library's orders equal the oracle's simulator, op for op."""
+    for p in range(1, 13):
+        for m in list(range(1, 3 * p + 2)) + [40]:
+            ref = S.orders_for(kind, p, m)
+            for s in range(p):
+                assert zb.zb_schedule(kind, s, p, m) == ref[s], (kind, s, p, m)
+
+
+def test_config4_zbh1_order(zblib):
+    """ZB-H1 for stage 3 of p = 8, m = 16: W deferred behind B, steady B W F rhythm, drain at the end."""
+    got = " ".join(f"{k}{i}" for k, i in zb.zb_schedule("zbh1", 3, 8, 16))
+    want = ("F0 F1 F2 F3 F4 B0 F5 B1 F6 B2 F7 B3 W0 F8 B4 W1 F9 B5 W2 F10 B6 W3 F11 B7 W4 F12 "
+            "B8 W5 F13 B9 W6 F14 B10 W7 F15 B11 W8 B12 W9 B13 W10 B14 W11 B15 W12 W13 W14 W15")
+    assert got == want
+
+
+@pytest.mark.parametrize("kind", ["1f1b", "zbh1", "gpipe"])
+@pytest.mark.parametrize("p,m", [(1, 1), (2, 5), (4, 3), (8, 16), (8, 12), (8, 24), (8, 32), (6, 40)])
+def test_bubble_model_equals_oracle(zblib, kind, p, m):
+    span, over_c, over_w = zb.zb_schedule_bubble(kind, p, m)
+    c, w = S.bubble(kind, p, m)
+    _, start = S.timeline(kind, p, m)
+    assert span == S.makespan(start)
+    assert abs(over_c - c) < 1e-12 and abs(over_w - w) < 1e-12
+
+
+def test_bubble_printed_values(zblib):
+    # "Zero-Bubble Pipeline Parallelism Guide for LLMs": 7/16 (section "2. The 1F1B ..."),
+    # 30.4 % of wall time (first diagram), (p-1)/(3m) for ZB-1F1B (section "Mathematical Modeling")
+    assert abs(zb.zb_schedule_bubble("1f1b", 8, 16)[1] - 7 / 16) < 1e-12
+    assert round(100 * zb.zb_schedule_bubble("1f1b", 8, 16)[2], 1) == 30.4
+    assert abs(zb.zb_schedule_bubble("zbh1", 8, 16)[1] - 7 / 48) < 1e-12
+
+
+def test_schedule_errors(zblib):
+    st, n, _ = zb.zb_schedule_raw(1, 0, 4, 8, 10)
+    assert st == -8 and n == 24  # ZB_ERR_CAPACITY reports the size needed
+    assert zb.zb_schedule_raw(1, 4, 4, 8, 24)[0] == -1  # stage out of range
+    assert zb.zb_schedule_raw(1, 0, 0, 8, 24)[0] == -1
+    assert zb.zb_schedule_raw(1, 0, 4, 0, 24)[0] == -1
+    assert zb.zb_schedule_raw(7, 0, 4, 8, 24)[0] == -1  # unknown kind
+    assert zb.zb_schedule_raw(1, 0, 4, 8, 24)[0] == 0
+
+
+def test_stage_config_checks(zblib):
+    ok = zb.make_config("transformer", 2, 256, 512, 4, 2, 64, max_tokens=128, max_inflight=2)
+    assert zb.zb_stage_workspace_bytes(ok) > 0
+    bad_shape = zb.make_config("transformer", 2, 256, 500, 4, 2, 64)   # ffn not a multiple of 64
+    assert zb.zb_stage_workspace_bytes(bad_shape) == 0
+    bad_heads = zb.make_config("transformer", 2, 256, 512, 4, 3, 64)   # 4 heads, 3 kv heads
+    assert zb.zb_stage_workspace_bytes(bad_heads) == 0
+    bad_linear = zb.make_config("linear", 2, 256, 512)                 # a linear stage has one layer
+    assert zb.zb_stage_workspace_bytes(bad_linear) == 0
+    # workspace grows linearly with the number of stash slots
+    one = zb.zb_stage_workspace_bytes(zb.make_config("mlp", 2, 256, 1024, max_tokens=128, max_inflight=1))
+    four = zb.zb_stage_workspace_bytes(zb.make_config("mlp", 2, 256, 1024, max_tokens=128, max_inflight=4))
+    scratch = zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(128, 256)
+    assert scratch == 4 * 256 * 4
+    assert four - one == 3 * (one - scratch)
+
+
+def test_stage_host_errors_without_device(zblib):
+    """Creation and order errors are decided on the host, before any device call."""
+    cfg = zb.make_config("linear", 1, 256, 512, max_tokens=64, max_inflight=1)
+    nbytes = zb.zb_stage_workspace_bytes(cfg)
+    fake = 1 << 20  # never dereferenced by these calls
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_stage_create(cfg, [{"w": fake, "dw": fake}], fake + 8, nbytes)
+    assert e.value.name == "ZB_ERR_WORKSPACE"  # misaligned workspace
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_stage_create(cfg, [{"w": fake}], fake, nbytes)
+    assert e.value.name == "ZB_ERR_ARG"  # missing accumulator
+    st = zb.zb_stage_create(cfg, [{"w": fake, "dw": fake}], fake, nbytes)
+    try:
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_backward_input(st, 0, fake, fake, 0)
+        assert e.value.name == "ZB_ERR_NO_MB"
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_backward_weight(st, 3, 0)
+        assert e.value.name == "ZB_ERR_NO_MB"
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_stage_forward(st, 0, fake, 65, fake, 0)
+        assert e.value.name == "ZB_ERR_SHAPE"  # tokens > max_tokens
+        assert zb.zb_stage_stats(st) == (0, 0, 0)
+        zb.zb_wgrad_flush(st, 0)  # nothing pending: no device call
+    finally:
+        zb.zb_stage_destroy(st)
+
+
+def test_op_argument_errors(zblib):
+    fake = 1 << 20
+    lib = zblib
+    assert lib.zb_op_backward_weight(None, fake, fake, 8, 64, 64, None) == -1
+    assert lib.zb_op_backward_weight(fake + 2, fake, fake, 8, 64, 64, None) == -1  # misaligned
+    assert lib.zb_op_backward_weight(fake, fake, fake, 8, 65, 64, None) == -2
+    assert lib.zb_op_backward_weight(fake, fake, fake, -1, 64, 64, None) == -2
+    assert lib.zb_op_backward_input_attention(fake, fake, fake, 8, 6, 4, 64, None) == -2  # 4 does not divide 6
+    assert lib.zb_op_rmsnorm_backward_gamma(fake, fake, fake, fake, 64, 256, fake, 10, None) == -10
