@@ -77,6 +77,9 @@ _SIGS = {
     "zb_op_rmsnorm_backward_gamma_scratch_bytes": (c_size_t, [c_int32, c_int32]),
     "zb_op_rmsnorm_backward_gamma": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
                                                c_void_p, c_size_t, c_void_p]),
+    "zb_op_rmsnorm_backward_gamma_noalloc_max_floats": (c_size_t, []),
+    "zb_op_rmsnorm_backward_gamma_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
+                                                       c_void_p]),
     "zb_op_rmsnorm_forward": (c_int32, [c_void_p, c_void_p, c_float, c_void_p, c_void_p, c_int32, c_int32,
                                         c_void_p]),
     "zb_op_swiglu_forward": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p]),
@@ -222,6 +225,16 @@ def zb_op_rmsnorm_backward_gamma(dn, x, rstd, dgamma, tokens, hidden, scratch, s
     _check(lib().zb_op_rmsnorm_backward_gamma(_ptr(dn), _ptr(x), _ptr(rstd), _ptr(dgamma), tokens, hidden,
                                               _ptr(scratch), scratch_bytes, _stream(stream)),
            "zb_op_rmsnorm_backward_gamma")
+
+
+def zb_op_rmsnorm_backward_gamma_noalloc_max_floats():
+    return lib().zb_op_rmsnorm_backward_gamma_noalloc_max_floats()
+
+
+def zb_op_rmsnorm_backward_gamma_noalloc(dn, x, rstd, dgamma, tokens, hidden, stream=None):
+    """Gamma-gradient reduction without caller scratch (see include/zb.h for its limits)."""
+    _check(lib().zb_op_rmsnorm_backward_gamma_noalloc(_ptr(dn), _ptr(x), _ptr(rstd), _ptr(dgamma), tokens, hidden,
+                                                      _stream(stream)), "zb_op_rmsnorm_backward_gamma_noalloc")
 
 
 def zb_op_rmsnorm_forward(x, gamma, eps, n, rstd, tokens, hidden, stream=None):

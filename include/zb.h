@@ -175,6 +175,34 @@ zb_status zb_op_rmsnorm_backward_gamma(const void* dn, const void* x, const floa
                                        float* dgamma, int32_t tokens, int32_t hidden,
                                        void* scratch, size_t scratch_bytes, void* stream);
 
+/* The same gamma-gradient reduction for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a convenience of this
+ * library.  Some callers get only their input and output tensors from a host
+ * framework, for example a plugin or custom-op interface that offers no
+ * workspace.  Others run where all device memory belongs to another allocator,
+ * so a cudaMalloc of their own would fail or synchronise the device.  These
+ * callers cannot provide `scratch`, so this variant keeps the partial sums in
+ * a fixed 4 MiB float32 array inside the library.
+ *  - Every GPU that loads the library holds that array until the process exits.
+ *  - Size limit: ceil(tokens / 32) * hidden must not exceed
+ *    zb_op_rmsnorm_backward_gamma_noalloc_max_floats() (1,048,576): for
+ *    example T <= 4096 at H = 8192, or T <= 8192 at H = 4096.  Larger sizes
+ *    return ZB_ERR_SHAPE and enqueue nothing.
+ *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *    routine.
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current).  Make that first call before any stream capture.
+ *  - All calls share the one array, and it keeps the last call's contents.
+ *    Every partial sum a call reads is first written by that same call, so
+ *    nothing needs clearing.
+ *  - Calls that overlap on the GPU (other streams, other host threads) race on
+ *    the array and give wrong results: order them.
+ * Arguments, layout and result are as for zb_op_rmsnorm_backward_gamma. */
+size_t zb_op_rmsnorm_backward_gamma_noalloc_max_floats(void);
+zb_status zb_op_rmsnorm_backward_gamma_noalloc(const void* dn, const void* x, const float* rstd,
+                                               float* dgamma, int32_t tokens, int32_t hidden,
+                                               void* stream);
+
 /* F pieces.  RMSNorm: rstd[t] = (mean_j x[t,j]^2 + eps)^(-1/2) (float32),
  * n = gamma * x * rstd (bf16).  SwiGLU: s[T,F] = silu(gu[:, :F]) * gu[:, F:].
  * Attention stand-in: a[T, nh hd] from qkv[T, (nh + 2 nkv) hd] as above. */

@@ -1,0 +1,56 @@
+"""The gamma-gradient reduction that allocates nothing.
+
+Some callers cannot give the library scratch memory.  They get only their
+input and output tensors from a host framework, or all device memory belongs
+to another allocator.  For them,
+zb_op_rmsnorm_backward_gamma_noalloc keeps its partial sums in a fixed array
+inside the library.  This file checks it against the caller-scratch entry
+point, through the C ABI, on two calls in a row.  The file is named so that
+pytest collects it last.
+"""
+import numpy as np
+import pytest
+import torch
+
+from backward_split_linear_gb300 import binding as zb
+from backward_split_linear_gb300.runtime import bf16_from_bits
+from oracle import stage as S
+from parity import assert_close, draw_bf16
+
+
+def _case(rng, t, hidden):
+    dnb, _ = draw_bf16(rng, (t, hidden))
+    xb, x = draw_bf16(rng, (t, hidden), 2.0)
+    _, r = S.rmsnorm(x, np.ones(hidden), 1e-5)
+    rstd = torch.from_numpy(r.astype(np.float32)).cuda()
+    return bf16_from_bits(dnb), bf16_from_bits(xb), rstd
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_scratch_entry_point_twice(cuda_device):
+    rng = np.random.default_rng(123)
+    # Two calls in a row with different sizes: the second must not see the first's partial sums.
+    for t, hidden in ((4096, 4096), (1000, 8192)):
+        dn, x, rstd = _case(rng, t, hidden)
+        init = torch.from_numpy(rng.standard_normal(hidden).astype(np.float32)).cuda()
+        ref = init.clone()
+        nbytes = zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(t, hidden)
+        scratch = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+        zb.zb_op_rmsnorm_backward_gamma(dn, x, rstd, ref, t, hidden, scratch, nbytes)
+        got = init.clone()
+        zb.zb_op_rmsnorm_backward_gamma_noalloc(dn, x, rstd, got, t, hidden)
+        torch.cuda.synchronize()
+        assert_close(got.cpu().numpy(), ref.cpu().numpy(), f"noalloc dgamma, T={t}, H={hidden}")
+    assert zb.zb_device_status()[0] == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_sizes_beyond_its_array(cuda_device):
+    cap = zb.zb_op_rmsnorm_backward_gamma_noalloc_max_floats()
+    assert cap == 1 << 20
+    t, hidden = 8192, 8192  # needs 256 * 8192 = 2M floats
+    dummy = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    dg = torch.zeros(hidden, dtype=torch.float32, device="cuda")
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_op_rmsnorm_backward_gamma_noalloc(dummy, dummy, dg, dg, t, hidden)
+    assert e.value.name == "ZB_ERR_SHAPE"
