@@ -1,9 +1,9 @@
 // Persistent tcgen05 GEMM for sm_103a with fused epilogues.
 //
 // One CTA per SM walks output tiles of BM x BN = 128 x 256.  Warp roles:
-//   warp 0   one thread issues TMA tile loads into a 4-stage shared-memory ring
+//   warp 0   one thread issues TMA tile loads into a 4-stage ring of 48 KiB
 //   warp 1   allocates tensor memory; one thread issues tcgen05.mma (bf16 in,
-//            f32 accumulate) into one of two 128 x 256 f32 accumulators
+//            f32 accumulate) into one of two 128 x BN f32 accumulators
 //   warps 2-5 epilogue: tcgen05.ld the accumulator (one row per thread), apply
 //            the fused op, store to global memory
 // Two accumulators (512 tensor-memory columns) let the epilogue of one tile run
@@ -19,9 +19,17 @@
 // an MN-major tile is BK rows of 64 MN-elements per 64-wide block, one TMA box
 // per block.  Out-of-range rows and columns of a box read as zero, so ragged
 // M, N and K need no special mainloop; the epilogue masks rows >= M, cols >= N.
+//
+// Tile order: tiles are walked in groups of G rows (or columns) of tiles so that
+// the tiles in flight at once share operand panels in L2.  The host picks G
+// per launch with a small model of the DRAM bytes each wave of tiles fetches.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <map>
 #include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -31,21 +39,33 @@ namespace zbk {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int kThreads = 192;
 constexpr uint32_t kAStageBytes = BM * BK * 2;   // 16 KiB
-constexpr uint32_t kBStageBytes = BN * BK * 2;   // 32 KiB
-constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
 constexpr uint32_t kMnBlockBytes = 64 * BK * 2;  // one 64-wide MN block of an MN-major tile
-constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kNumBars = 2 * STAGES + 5;
-constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + kNumBars * 8 + 16;
+
+// A 128 x 128 tile was tried for launches whose 128 x 256 tiling leaves a
+// poor last wave: on GB300 it ran at about two thirds of the wide tile's rate
+// per FLOP (twice the A-operand shared-memory traffic per MMA FLOP), so every
+// launch uses the wide tile.
+constexpr int kBN = 256;
+
+template <int BN>
+struct Cfg {
+    static constexpr int STAGES = 4;
+    static constexpr uint32_t kBStageBytes = BN * BK * 2;
+    static constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
+    static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + kNumBars * 8 + 16;
+};
+static_assert(Cfg<kBN>::kSmemBytes <= 232448, "shared memory");
 
 struct KParams {
     int m, n, k;
-    int tiles_m, num_tiles, k_blocks;
+    int tiles_m, tiles_n, num_tiles, k_blocks;
+    int group;      // tiles per group along the grouped dimension
+    int group_m;    // 1: groups of `group` tile rows (m fastest inside); 0: groups of tile columns
     void* out;
     int64_t ldo;
     const void* aux;
@@ -57,6 +77,25 @@ struct KParams {
     uint32_t mn_lbo;
     uint32_t mn_sbo;
 };
+
+// Tile index -> (tile row, tile column) under the grouped raster.
+__device__ __forceinline__ void tile_coords(const KParams& p, int tile, int& tm, int& tn) {
+    if (p.group_m) {
+        const int per = p.group * p.tiles_n;
+        const int g = tile / per;
+        const int in = tile - g * per;
+        const int rows = min(p.group, p.tiles_m - g * p.group);
+        tm = g * p.group + in % rows;
+        tn = in / rows;
+    } else {
+        const int per = p.group * p.tiles_m;
+        const int g = tile / per;
+        const int in = tile - g * per;
+        const int cols = min(p.group, p.tiles_n - g * p.group);
+        tn = g * p.group + in % cols;
+        tm = in / cols;
+    }
+}
 
 template <int EPI>
 __device__ __forceinline__ void epilogue_chunk(const KParams& p, int m, int n, const uint32_t (&r)[32],
@@ -119,10 +158,15 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int m, int n, c
     }
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const KParams p) {
+    constexpr int STAGES = Cfg<BN>::STAGES;
+    constexpr uint32_t kBStageBytes = Cfg<BN>::kBStageBytes;
+    constexpr uint32_t kStageBytes = Cfg<BN>::kStageBytes;
+    constexpr uint32_t kTmemCols = Cfg<BN>::kTmemCols;
+    constexpr int kNumBars = Cfg<BN>::kNumBars;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -170,8 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                const int m0 = (tile % p.tiles_m) * BM;
-                const int n0 = (tile / p.tiles_m) * BN;
+                int tm, tn;
+                tile_coords(p, tile, tm, tn);
+                const int m0 = tm * BM;
+                const int n0 = tn * BN;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty)) {
                         ok = false;
@@ -264,8 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t aph = (static_cast<uint32_t>(it) >> 1) & 1u;
             if (!mbar_wait(tfull_bar(acc), aph, p.status, kSiteEpiTmemFull)) break;
             tc_fence_after();
-            const int m = (tile % p.tiles_m) * BM + row;
-            const int n_base = (tile / p.tiles_m) * BN;
+            int tm, tn;
+            tile_coords(p, tile, tm, tn);
+            const int m = tm * BM + row;
+            const int n_base = tn * BN;
             const bool row_ok = m < p.m;
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
@@ -338,32 +386,139 @@ bool encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, i
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <int BN, bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& p,
                            cudaStream_t stream) {
-    auto kern = gemm_kernel<A_MN, B_MN, EPI>;
+    auto kern = gemm_kernel<BN, A_MN, B_MN, EPI>;
+    constexpr size_t smem = Cfg<BN>::kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kSmemBytes));
+                                        static_cast<int>(smem));
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
+    kern<<<grid, kThreads, smem, stream>>>(ma, mb, p);
     return cudaGetLastError();
+}
+
+// DRAM bytes a raster fetches, modelled wave by wave: a wave reads the A
+// panels (one tile row over all of K) and B panels (one tile column) of its
+// tiles; panels of the previous wave are still in L2 if that wave's panels fit.
+double raster_cost(int tiles_m, int tiles_n, double panel_a, double panel_b, int grid, int group, bool group_m,
+                   double l2_bytes) {
+    KParams q{};
+    q.tiles_m = tiles_m;
+    q.tiles_n = tiles_n;
+    q.group = group;
+    q.group_m = group_m ? 1 : 0;
+    const int total = tiles_m * tiles_n;
+    std::vector<char> pm(tiles_m, 0), pn(tiles_n, 0), cm(tiles_m), cn(tiles_n);
+    double prev_bytes = 0.0, cost = 0.0;
+    for (int w0 = 0; w0 < total; w0 += grid) {
+        std::fill(cm.begin(), cm.end(), 0);
+        std::fill(cn.begin(), cn.end(), 0);
+        for (int t = w0; t < std::min(total, w0 + grid); ++t) {
+            int tm, tn;
+            if (q.group_m) {
+                const int per = group * tiles_n, g = t / per, in = t - g * per;
+                const int rows = std::min(group, tiles_m - g * group);
+                tm = g * group + in % rows;
+                tn = in / rows;
+            } else {
+                const int per = group * tiles_m, g = t / per, in = t - g * per;
+                const int cols = std::min(group, tiles_n - g * group);
+                tn = g * group + in % cols;
+                tm = in / cols;
+            }
+            cm[tm] = 1;
+            cn[tn] = 1;
+        }
+        const bool kept = prev_bytes <= l2_bytes;
+        double bytes = 0.0;
+        for (int i = 0; i < tiles_m; ++i)
+            if (cm[i]) {
+                bytes += panel_a;
+                if (!kept || !pm[i]) cost += panel_a;
+            }
+        for (int j = 0; j < tiles_n; ++j)
+            if (cn[j]) {
+                bytes += panel_b;
+                if (!kept || !pn[j]) cost += panel_b;
+            }
+        pm.swap(cm);
+        pn.swap(cn);
+        prev_bytes = bytes;
+    }
+    return cost;
+}
+
+struct Raster {
+    int group;
+    bool group_m;
+};
+
+Raster choose_raster(int tiles_m, int tiles_n, int bn, int k, int grid) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, int>, Raster> cache;
+    const auto key = std::make_tuple(tiles_m, tiles_n, bn, k, grid);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const double pa = 2.0 * BM * k, pb = 2.0 * bn * k;
+    const double l2 = 64.0 * 1024 * 1024;  // about half of the 129 MB L2
+    Raster best{tiles_m, true};             // plain m-fastest order
+    double best_cost = raster_cost(tiles_m, tiles_n, pa, pb, grid, tiles_m, true, l2);
+    for (int g = 1; g < 256; g *= 2) {
+        if (g < tiles_m) {
+            const double c = raster_cost(tiles_m, tiles_n, pa, pb, grid, g, true, l2);
+            if (c < best_cost * 0.98) best = {g, true}, best_cost = c;
+        }
+        if (g < tiles_n) {
+            const double c = raster_cost(tiles_m, tiles_n, pa, pb, grid, g, false, l2);
+            if (c < best_cost * 0.98) best = {g, false}, best_cost = c;
+        }
+    }
+    cache.emplace(key, best);
+    return best;
+}
+
+template <int BN>
+cudaError_t dispatch(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMap& mb, KParams& p,
+                     cudaStream_t stream) {
+    constexpr int kStore = static_cast<int>(Epilogue::StoreBf16);
+    constexpr int kResid = static_cast<int>(Epilogue::AddResidual);
+    constexpr int kSwiglu = static_cast<int>(Epilogue::SwigluBwd);
+    constexpr int kAccum = static_cast<int>(Epilogue::AccumF32);
+    switch (g.kind) {
+        case GemmKind::Forward:
+            if (g.epi == Epilogue::StoreBf16) return launch_variant<BN, false, false, kStore>(ma, mb, p, stream);
+            if (g.epi == Epilogue::AddResidual) return launch_variant<BN, false, false, kResid>(ma, mb, p, stream);
+            break;
+        case GemmKind::BackwardInput:
+            if (g.epi == Epilogue::StoreBf16) return launch_variant<BN, false, true, kStore>(ma, mb, p, stream);
+            if (g.epi == Epilogue::SwigluBwd) return launch_variant<BN, false, true, kSwiglu>(ma, mb, p, stream);
+            break;
+        case GemmKind::BackwardWeight:
+            if (g.epi == Epilogue::AccumF32) return launch_variant<BN, true, true, kAccum>(ma, mb, p, stream);
+            break;
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     if (g.m <= 0 || g.n <= 0 || g.k <= 0) return cudaSuccess;
+    const int sms = sm_count();
+    constexpr int bn = kBN;
     CUtensorMap ma, mb;
     bool ok = true;
     switch (g.kind) {
         case GemmKind::Forward:
             ok = encode_map(&ma, g.a, g.m, g.k, g.lda, 64, BM) &&
-                 encode_map(&mb, g.b, g.n, g.k, g.ldb, 64, BN);
+                 encode_map(&mb, g.b, g.n, g.k, g.ldb, 64, static_cast<uint32_t>(bn));
             break;
         case GemmKind::BackwardInput:
             ok = encode_map(&ma, g.a, g.m, g.k, g.lda, 64, BM) &&
@@ -375,13 +530,17 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
             break;
     }
     if (!ok) return cudaErrorInvalidValue;
-    KParams p;
+    KParams p{};
     p.m = g.m;
     p.n = g.n;
     p.k = g.k;
     p.tiles_m = (g.m + BM - 1) / BM;
-    p.num_tiles = p.tiles_m * ((g.n + BN - 1) / BN);
+    p.tiles_n = (g.n + bn - 1) / bn;
+    p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_blocks = (g.k + BK - 1) / BK;
+    const Raster r = choose_raster(p.tiles_m, p.tiles_n, bn, g.k, std::min(p.num_tiles, sms));
+    p.group = r.group;
+    p.group_m = r.group_m ? 1 : 0;
     p.out = g.out;
     p.ldo = g.ldo;
     p.aux = g.aux;
@@ -391,24 +550,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     p.mn_lbo = kMnBlockBytes;
     p.mn_sbo = 1024;
     if (!p.status) return cudaErrorInvalidDevice;
-    constexpr int kStore = static_cast<int>(Epilogue::StoreBf16);
-    constexpr int kResid = static_cast<int>(Epilogue::AddResidual);
-    constexpr int kSwiglu = static_cast<int>(Epilogue::SwigluBwd);
-    constexpr int kAccum = static_cast<int>(Epilogue::AccumF32);
-    switch (g.kind) {
-        case GemmKind::Forward:
-            if (g.epi == Epilogue::StoreBf16) return launch_variant<false, false, kStore>(ma, mb, p, stream);
-            if (g.epi == Epilogue::AddResidual) return launch_variant<false, false, kResid>(ma, mb, p, stream);
-            break;
-        case GemmKind::BackwardInput:
-            if (g.epi == Epilogue::StoreBf16) return launch_variant<false, true, kStore>(ma, mb, p, stream);
-            if (g.epi == Epilogue::SwigluBwd) return launch_variant<false, true, kSwiglu>(ma, mb, p, stream);
-            break;
-        case GemmKind::BackwardWeight:
-            if (g.epi == Epilogue::AccumF32) return launch_variant<true, true, kAccum>(ma, mb, p, stream);
-            break;
-    }
-    return cudaErrorInvalidValue;
+    return dispatch<kBN>(g, ma, mb, p, stream);
 }
 
 }  // namespace zbk

@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_fwd_kernel(const uint16_t
 
 // ---------------------------------------------------------------- RMSNorm input backward
 // dx = dres + r (gamma dn - xh * mean(gamma dn xh)), xh = x r.
+// Every load of the row (dn, x, dres) is issued before the row reduction, so
+// a block keeps all of its row's bytes in flight at once.
 template <int VPT>
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_kernel(
     const uint16_t* __restrict__ dn, const uint16_t* __restrict__ x, const float* __restrict__ rstd,
@@ -104,22 +106,31 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_kernel(
     const int64_t row = blockIdx.x;
     const int chunks = hidden >> 3;
     const float r = rstd[row];
-    V8 gd[VPT], xh[VPT];
+    uint4 dv[VPT], xv[VPT], rv[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int c = threadIdx.x + i * kRowThreads;
+        if (c < chunks) {
+            dv[i] = *reinterpret_cast<const uint4*>(dn + row * hidden + 8 * c);
+            xv[i] = *reinterpret_cast<const uint4*>(x + row * hidden + 8 * c);
+            rv[i] = *reinterpret_cast<const uint4*>(dres + row * hidden + 8 * c);
+        }
+    }
     float dot = 0.f;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int c = threadIdx.x + i * kRowThreads;
         if (c < chunks) {
-            const V8 dv = load8(dn + row * hidden + 8 * c);
-            const V8 xv = load8(x + row * hidden + 8 * c);
             const float4 g0 = *reinterpret_cast<const float4*>(gamma + 8 * c);
             const float4 g1 = *reinterpret_cast<const float4*>(gamma + 8 * c + 4);
             const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const uint32_t dw[4] = {dv[i].x, dv[i].y, dv[i].z, dv[i].w};
+            const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                gd[i].v[e] = g[e] * dv.v[e];
-                xh[i].v[e] = xv.v[e] * r;
-                dot += gd[i].v[e] * xh[i].v[e];
+                const float d = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
+                const float xx = (e & 1) ? bf16_hi(xw[e >> 1]) : bf16_lo(xw[e >> 1]);
+                dot += g[e] * d * (xx * r);
             }
         }
     }
@@ -128,48 +139,112 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_kernel(
     for (int i = 0; i < VPT; ++i) {
         const int c = threadIdx.x + i * kRowThreads;
         if (c < chunks) {
-            const V8 rv = load8(dres + row * hidden + 8 * c);
+            const float4 g0 = *reinterpret_cast<const float4*>(gamma + 8 * c);
+            const float4 g1 = *reinterpret_cast<const float4*>(gamma + 8 * c + 4);
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const uint32_t dw[4] = {dv[i].x, dv[i].y, dv[i].z, dv[i].w};
+            const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+            const uint32_t rw[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
             float o[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = rv.v[e] + r * (gd[i].v[e] - xh[i].v[e] * mean);
+            for (int e = 0; e < 8; ++e) {
+                const float d = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
+                const float xx = (e & 1) ? bf16_hi(xw[e >> 1]) : bf16_lo(xw[e >> 1]);
+                const float res = (e & 1) ? bf16_hi(rw[e >> 1]) : bf16_lo(rw[e >> 1]);
+                o[e] = res + r * (g[e] * d - (xx * r) * mean);
+            }
             store8(dx + row * hidden + 8 * c, o);
         }
     }
 }
 
 // ---------------------------------------------------------------- RMSNorm gamma gradient
-// Pass 1: block (cx, cy) sums rows [cy * R, cy * R + R) for 8-column chunk
-// cx * 256 + t into part[cy][...].  Pass 2: dgamma[j] += sum over cy in order.
-constexpr int kGammaRows = 32;
+// Pass 1: block (cx, cy) covers columns [256 cx, 256 cx + 256) and tokens
+// [64 cy, 64 cy + 64).  Thread (g, c) sums 8 tokens (g = 0..7) of the 8
+// columns of chunk c; the 8 row groups are then added in order g = 0..7 in
+// shared memory and the block writes part[cy][256 columns].
+// Pass 2: dgamma[j] += part[0][j] + part[1][j] + ... in order.
+// Fixed assignment and fixed order make the result bitwise reproducible.
+constexpr int kGammaCols = 256;                 // columns per block
+constexpr int kGammaChunks = kGammaCols / 8;    // 32 threads across the columns
+constexpr int kGammaGroups = kRowThreads / kGammaChunks;  // 8 row groups
+constexpr int kGammaGroupRows = 8;
+constexpr int kGammaRows = kGammaGroups * kGammaGroupRows;  // 64 tokens per block
 
 __global__ void __launch_bounds__(kRowThreads) dgamma_partial_kernel(
     const uint16_t* __restrict__ dn, const uint16_t* __restrict__ x, const float* __restrict__ rstd,
     float* __restrict__ part, int tokens, int hidden) {
-    const int c = blockIdx.x * kRowThreads + threadIdx.x;
-    if (c >= (hidden >> 3)) return;
-    const int t0 = blockIdx.y * kGammaRows;
-    const int t1 = min(tokens, t0 + kGammaRows);
+    __shared__ float acc_s[kGammaGroups][kGammaCols];
+    const int cl = threadIdx.x % kGammaChunks;
+    const int grp = threadIdx.x / kGammaChunks;
+    const int col = blockIdx.x * kGammaCols + 8 * cl;
+    const bool col_ok = col < hidden;
+    const int t0 = blockIdx.y * kGammaRows + grp * kGammaGroupRows;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int t = t0; t < t1; ++t) {
-        const float r = rstd[t];
-        const V8 dv = load8(dn + static_cast<int64_t>(t) * hidden + 8 * c);
-        const V8 xv = load8(x + static_cast<int64_t>(t) * hidden + 8 * c);
+    if (col_ok) {
+        uint4 dv[kGammaGroupRows], xv[kGammaGroupRows];
+        float rr[kGammaGroupRows];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += dv.v[e] * (xv.v[e] * r);
+        for (int i = 0; i < kGammaGroupRows; ++i) {
+            const int t = t0 + i;
+            if (t < tokens) {
+                dv[i] = *reinterpret_cast<const uint4*>(dn + static_cast<int64_t>(t) * hidden + col);
+                xv[i] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * hidden + col);
+                rr[i] = rstd[t];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kGammaGroupRows; ++i) {
+            if (t0 + i < tokens) {
+                const uint32_t dw[4] = {dv[i].x, dv[i].y, dv[i].z, dv[i].w};
+                const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
+                    const float xx = (e & 1) ? bf16_hi(xw[e >> 1]) : bf16_lo(xw[e >> 1]);
+                    acc[e] += d * (xx * rr[i]);
+                }
+            }
+        }
     }
-    float4* dst = reinterpret_cast<float4*>(part + static_cast<int64_t>(blockIdx.y) * hidden + 8 * c);
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc_s[grp][8 * cl + e] = acc[e];
+    __syncthreads();
+    // thread j of the block finishes column j of the block's 256
+    const int j = threadIdx.x;
+    if (blockIdx.x * kGammaCols + j < hidden) {
+        float s = 0.f;
+#pragma unroll
+        for (int g = 0; g < kGammaGroups; ++g) s += acc_s[g][j];
+        part[static_cast<int64_t>(blockIdx.y) * hidden + blockIdx.x * kGammaCols + j] = s;
+    }
 }
 
-__global__ void dgamma_final_kernel(const float* __restrict__ part, int parts, float* dgamma,
-                                    int hidden) {
-    const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= hidden) return;
+// Pass 2: block covers 32 columns; thread (c, g) adds the partials q = g,
+// g + 8, g + 16, ... of column c in order, then thread (c, 0) adds the 8
+// sums in order g = 0..7 and accumulates into dgamma.
+constexpr int kFinalCols = 32;
+constexpr int kFinalGroups = 8;
+
+__global__ void __launch_bounds__(kFinalCols * kFinalGroups) dgamma_final_kernel(
+    const float* __restrict__ part, int parts, float* dgamma, int hidden) {
+    __shared__ float sums[kFinalGroups][kFinalCols];
+    const int c = threadIdx.x % kFinalCols;
+    const int g = threadIdx.x / kFinalCols;
+    const int j = blockIdx.x * kFinalCols + c;
     float s = 0.f;
-    for (int q = 0; q < parts; ++q) s += part[static_cast<int64_t>(q) * hidden + j];
-    dgamma[j] += s;
+    if (j < hidden) {
+#pragma unroll 4
+        for (int q = g; q < parts; q += kFinalGroups) s += part[static_cast<int64_t>(q) * hidden + j];
+    }
+    sums[g][c] = s;
+    __syncthreads();
+    if (g == 0 && j < hidden) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < kFinalGroups; ++k) t += sums[k][c];
+        dgamma[j] += t;
+    }
 }
 
 // ---------------------------------------------------------------- SwiGLU forward
@@ -334,11 +409,12 @@ cudaError_t launch_rmsnorm_backward_gamma(const void* dn, const void* x, const f
                                           cudaStream_t stream) {
     if (tokens <= 0) return cudaSuccess;
     const int parts = (tokens + kGammaRows - 1) / kGammaRows;
-    const dim3 grid1((hidden / 8 + kRowThreads - 1) / kRowThreads, parts);
+    const dim3 grid1((hidden + kGammaCols - 1) / kGammaCols, parts);
     dgamma_partial_kernel<<<grid1, kRowThreads, 0, stream>>>(static_cast<const uint16_t*>(dn),
                                                             static_cast<const uint16_t*>(x), rstd,
                                                             scratch, tokens, hidden);
-    dgamma_final_kernel<<<(hidden + 255) / 256, 256, 0, stream>>>(scratch, parts, dgamma, hidden);
+    dgamma_final_kernel<<<(hidden + kFinalCols - 1) / kFinalCols, kFinalCols * kFinalGroups, 0, stream>>>(
+        scratch, parts, dgamma, hidden);
     return cudaGetLastError();
 }
 

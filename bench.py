@@ -401,6 +401,67 @@ def run_ours(args, w):
     return 0
 
 
+def run_op(args):
+    """--op: times repeated launches of one per-step op at one shape (profiling and the wgrad sweep)."""
+    import torch
+
+    import __graft_entry__
+    from backward_split_linear_gb300 import binding as zb
+
+    __graft_entry__.build()
+    t, n_in, n_out = (int(v) for v in args.shape.split(","))
+    g = torch.Generator(device="cuda").manual_seed(0)
+
+    def rnd(*shape, std=1.0):
+        return (torch.randn(*shape, generator=g, device="cuda") * std).to(torch.bfloat16)
+
+    peaks = measured_peaks()
+    flops = 2.0 * t * n_in * n_out
+    if args.op == "backward_weight":
+        dy, x = rnd(t, n_out), rnd(t, n_in)
+        dw = torch.zeros(n_out, n_in, dtype=torch.float32, device="cuda")
+        launch = lambda: zb.zb_op_backward_weight(dy, x, dw, t, n_in, n_out)
+        nbytes = 2.0 * t * (n_in + n_out) + 8.0 * n_in * n_out
+    elif args.op == "backward_input":
+        dy, w = rnd(t, n_out), rnd(n_out, n_in, std=0.02)
+        dx = torch.empty(t, n_in, dtype=torch.bfloat16, device="cuda")
+        launch = lambda: zb.zb_op_backward_input(dy, w, dx, t, n_in, n_out)
+        nbytes = 2.0 * (t * n_out + n_out * n_in + t * n_in)
+    elif args.op == "backward_input_swiglu":  # n_in = ffn, n_out = hidden
+        dy, w, gu = rnd(t, n_out), rnd(n_out, n_in, std=0.02), rnd(t, 2 * n_in)
+        launch = lambda: zb.zb_op_backward_input_swiglu(dy, w, gu, gu, t, n_out, n_in)
+        nbytes = 2.0 * (t * n_out + n_out * n_in) + 8.0 * t * n_in
+    else:
+        x, w = rnd(t, n_in), rnd(n_out, n_in, std=0.02)
+        y = torch.empty(t, n_out, dtype=torch.bfloat16, device="cuda")
+        launch = lambda: zb.zb_op_linear_forward(x, w, None, y, t, n_in, n_out)
+        nbytes = 2.0 * (t * n_in + n_out * n_in + t * n_out)
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # 256 MiB, larger than L2
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        launch()
+        b.record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if flops / nbytes >= ridge else "hbm"
+    frac = tflops / peaks["bf16_tflops"] if bound == "tensor" else gbs / peaks["hbm_gbs"]
+    print(json.dumps({"op": args.op, "shape": {"tokens": t, "in": n_in, "out": n_out}, "ms": ms,
+                      "tflops": tflops, "pct_of_burst_bf16": 100 * tflops / peaks["bf16_tflops"],
+                      "gbs": gbs, "bound": bound, "frac_of_binding_roofline": frac,
+                      "peak_source": peaks["source"] + " burst (kernel timed alone)",
+                      "l2": "256 MiB buffer written before every launch"}), flush=True)
+    assert zb.zb_device_status()[0] == 0
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -412,7 +473,12 @@ def main():
                     help="tokens of the microbatch the host oracle runs (cpu_baseline / reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["backward_weight", "backward_input", "backward_input_swiglu", "forward"],
+                    help="time one per-step op instead of the stage (with --shape T,IN,OUT)")
+    ap.add_argument("--shape", default="4096,4096,14336")
     args = ap.parse_args()
+    if args.op:
+        return run_op(args)
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

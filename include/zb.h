@@ -184,9 +184,9 @@ zb_status zb_op_rmsnorm_backward_gamma(const void* dn, const void* x, const floa
  * callers cannot provide `scratch`, so this variant keeps the partial sums in
  * a fixed 4 MiB float32 array inside the library.
  *  - Every GPU that loads the library holds that array until the process exits.
- *  - Size limit: ceil(tokens / 32) * hidden must not exceed
- *    zb_op_rmsnorm_backward_gamma_noalloc_max_floats() (1,048,576): for
- *    example T <= 4096 at H = 8192, or T <= 8192 at H = 4096.  Larger sizes
+ *  - Size limit: zb_op_rmsnorm_backward_gamma_scratch_bytes(tokens, hidden)
+ *    must not exceed 4 * zb_op_rmsnorm_backward_gamma_noalloc_max_floats()
+ *    bytes (4 MiB), which admits at least T = 4096 at H = 8192.  Larger sizes
  *    return ZB_ERR_SHAPE and enqueue nothing.
  *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *    routine.

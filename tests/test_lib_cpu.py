@@ -90,7 +90,7 @@ def test_stage_config_checks(zblib):
     one = zb.zb_stage_workspace_bytes(zb.make_config("mlp", 2, 256, 1024, max_tokens=128, max_inflight=1))
     four = zb.zb_stage_workspace_bytes(zb.make_config("mlp", 2, 256, 1024, max_tokens=128, max_inflight=4))
     scratch = zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(128, 256)
-    assert scratch == 4 * 256 * 4
+    assert scratch > 0 and scratch % (256 * 4) == 0  # whole float32 rows of partial sums
     assert four - one == 3 * (one - scratch)
 
 

@@ -48,9 +48,15 @@ def test_noalloc_matches_scratch_entry_point_twice(cuda_device):
 def test_noalloc_rejects_sizes_beyond_its_array(cuda_device):
     cap = zb.zb_op_rmsnorm_backward_gamma_noalloc_max_floats()
     assert cap == 1 << 20
-    t, hidden = 8192, 8192  # needs 256 * 8192 = 2M floats
-    dummy = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    t, hidden = 32768, 8192
+    # The entry point rejects exactly when the partial sums exceed its array;
+    # check that on the host first, and pass full-size buffers anyway.
+    assert zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(t, hidden) > 4 * cap
+    dn = torch.zeros(t, hidden, dtype=torch.bfloat16, device="cuda")
+    rstd = torch.ones(t, dtype=torch.float32, device="cuda")
     dg = torch.zeros(hidden, dtype=torch.float32, device="cuda")
     with pytest.raises(zb.ZBError) as e:
-        zb.zb_op_rmsnorm_backward_gamma_noalloc(dummy, dummy, dg, dg, t, hidden)
+        zb.zb_op_rmsnorm_backward_gamma_noalloc(dn, dn, rstd, dg, t, hidden)
     assert e.value.name == "ZB_ERR_SHAPE"
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dg).item() == 0
