@@ -357,6 +357,240 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- CTA-pair kernel
+//
+// The two CTAs of a cluster compute one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2.  CTA r (cluster rank r) keeps rows 128 r .. +127
+// of the A tile and columns 128 r .. +127 of the B tile in its own shared
+// memory; the MMA, issued by one thread of rank 0, reads both halves, and
+// each CTA's tensor memory receives its 128 rows of D.  Per SM this moves a
+// third less operand data through shared memory than the one-CTA 128 x 256
+// tile, and a stage is 32 KiB, so the ring is 6 stages deep.
+//
+// Synchronisation across the pair:
+//   full[s]    lives in rank 0; rank 0 expects both CTAs' bytes, each CTA's
+//              TMA completes its share there (cta_group::2 loads);
+//   empty[s]   in each CTA; the MMA commit multicasts to both;
+//   tfull[a]   in each CTA; the MMA commit multicasts to both;
+//   tempty[a]  lives in rank 0; all 256 epilogue threads of the pair arrive.
+constexpr int kPairM = 256;
+constexpr int kPairN = 256;
+constexpr int kHalf = 128;
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairAStage = kHalf * BK * 2;  // 16 KiB
+constexpr uint32_t kPairBStage = kHalf * BK * 2;  // 16 KiB
+constexpr uint32_t kPairStage = kPairAStage + kPairBStage;
+constexpr int kPairNumBars = 2 * kPairStages + 5;
+constexpr size_t kPairSmemBytes = 1024 + kPairStages * kPairStage + kPairNumBars * 8 + 16;
+static_assert(kPairSmemBytes <= 232448, "shared memory");
+
+template <bool A_MN, bool B_MN, int EPI, int NACC>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                     const KParams p) {
+    constexpr uint32_t kTmemCols = NACC * kPairN;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t s_a = base;
+    const uint32_t s_b = base + kPairStages * kPairAStage;
+    const uint32_t bars = s_b + kPairStages * kPairBStage;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (kPairStages + s); };
+    auto tfull_bar = [&](int a) { return bars + 8u * (2 * kPairStages + a); };
+    auto tempty_bar = [&](int a) { return bars + 8u * (2 * kPairStages + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * kPairStages + 4);
+    const uint32_t tmem_slot = bars + 8u * kPairNumBars;
+    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * 128);
+        }
+        mbar_init(drain_bar, 1);
+        mbar_fence_init();
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b);
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
+    tc_fence_before();
+    cluster_sync_all();  // barriers of both CTAs initialised, tensor memory allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+    // Both CTAs must hold the accumulator at the same columns.
+    const uint32_t peer_base = ld_shared_cluster_u32(map_to_cta(tmem_slot, rank ^ 1u));
+    const bool usable = peer_base == tmem_base;
+    if (!usable && threadIdx.x == 0) atomicCAS(p.status, 0, kSitePairTmem);
+
+    if (usable && warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs)
+            uint32_t issued[kPairStages];
+            for (int s = 0; s < kPairStages; ++s) issued[s] = 0;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+                int tm, tn;
+                tile_coords(p, tile, tm, tn);
+                const int m0 = tm * kPairM + static_cast<int>(rank) * kHalf;
+                const int n0 = tn * kPairN + static_cast<int>(rank) * kHalf;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb_local = full_bar(stage);
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * kPairStage);
+                    const uint32_t fb = map_to_cta(fb_local, 0);
+                    const int k0 = kb * BK;
+                    const uint32_t a_dst = s_a + stage * kPairAStage;
+                    const uint32_t b_dst = s_b + stage * kPairBStage;
+                    if constexpr (A_MN) {
+#pragma unroll
+                        for (int j = 0; j < kHalf / 64; ++j)
+                            tma_load_2d_pair(a_dst + j * kMnBlockBytes, &map_a, fb, m0 + 64 * j, k0);
+                    } else {
+                        tma_load_2d_pair(a_dst, &map_a, fb, k0, m0);
+                    }
+                    if constexpr (B_MN) {
+#pragma unroll
+                        for (int j = 0; j < kHalf / 64; ++j)
+                            tma_load_2d_pair(b_dst + j * kMnBlockBytes, &map_b, fb, n0 + 64 * j, k0);
+                    } else {
+                        tma_load_2d_pair(b_dst, &map_b, fb, k0, n0);
+                    }
+                    ++issued[stage];
+                    if (++stage == kPairStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Loads must land before shared memory goes away: rank 0 sees its
+            // full barriers complete; rank 1 sees the MMA release each stage.
+            for (int s = 0; s < kPairStages; ++s)
+                if (issued[s] > 0) {
+                    if (leader)
+                        mbar_wait_cluster(full_bar(s), (issued[s] - 1u) & 1u, p.status, kSiteDrain, kWaitLimitNs);
+                    else
+                        mbar_wait_cluster(empty_bar(s), (issued[s] - 1u) & 1u, p.status, kSiteDrain, kWaitLimitNs);
+                }
+        }
+    } else if (usable && warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (rank 0 only)
+            constexpr uint32_t idesc = mma_idesc_bf16(kPairM, kPairN, A_MN, B_MN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < p.num_tiles; tile += npairs, ++it) {
+                const int acc = it % NACC;
+                const uint32_t aph = static_cast<uint32_t>(it / NACC) & 1u;
+                if (!mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, p.status, kSiteMmaTmemEmpty)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_cluster(full_bar(stage), phase, p.status, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = s_a + stage * kPairAStage;
+                    const uint32_t b0 = s_b + stage * kPairBStage;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, p.mn_lbo, p.mn_sbo)
+                                                 : smem_desc_sw128(a0 + k * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, p.mn_lbo, p.mn_sbo)
+                                                 : smem_desc_sw128(b0 + k * 32, 16, 1024);
+                        umma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    umma_commit_pair(empty_bar(stage), 0x3);
+                    if (++stage == kPairStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(tfull_bar(acc), 0x3);
+            }
+            umma_commit_pair(drain_bar, 0x1);
+            mbar_wait(drain_bar, 0, p.status, kSiteDrain, kWaitLimitNs);
+        }
+    } else if (usable && warp >= 2) {
+        // ---------------- epilogue (both CTAs): warp w reads lanes 32 (w % 4) .. +31
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int it = 0;
+        for (int tile = pair; tile < p.num_tiles; tile += npairs, ++it) {
+            const int acc = it % NACC;
+            const uint32_t aph = static_cast<uint32_t>(it / NACC) & 1u;
+            if (!mbar_wait_cluster(tfull_bar(acc), aph, p.status, kSiteEpiTmemFull)) break;
+            tc_fence_after();
+            int tm, tn;
+            tile_coords(p, tile, tm, tn);
+            const int m = tm * kPairM + static_cast<int>(rank) * kHalf + row;
+            const int n_base = tn * kPairN;
+            const bool row_ok = m < p.m;
+            const uint32_t tbase =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kPairN);
+#pragma unroll 1
+            for (int c = 0; c < kPairN / 32; ++c) {
+                const int n = n_base + c * 32;
+                const bool ok = row_ok && n < p.n;
+                uint4 x0[4], x1[4];
+                if constexpr (EPI == static_cast<int>(Epilogue::AddResidual) ||
+                              EPI == static_cast<int>(Epilogue::SwigluBwd)) {
+                    if (ok) {
+                        const uint16_t* rowp =
+                            static_cast<const uint16_t*>(p.aux) + static_cast<int64_t>(m) * p.ld_aux;
+                        const uint4* s0 = reinterpret_cast<const uint4*>(rowp + n);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) x0[j] = s0[j];
+                        if constexpr (EPI == static_cast<int>(Epilogue::SwigluBwd)) {
+                            const uint4* s1 = reinterpret_cast<const uint4*>(rowp + p.ffn + n);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) x1[j] = s1[j];
+                        }
+                    }
+                }
+                uint32_t r[32];
+                tmem_load_32(tbase + static_cast<uint32_t>(c * 32), r);
+                tmem_wait_load();
+                if (c == kPairN / 32 - 1) {
+                    tc_fence_before();
+                    if (leader)
+                        mbar_arrive(tempty_bar(acc));
+                    else
+                        mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+                }
+                if (ok) epilogue_chunk<EPI>(p, m, n, r, x0, x1);
+            }
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync_all();  // neither CTA leaves while the other may still signal it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -400,6 +634,36 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const K
     if (attr_err != cudaSuccess) return attr_err;
     const int grid = p.num_tiles < sm_count() ? p.num_tiles : sm_count();
     kern<<<grid, kThreads, smem, stream>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+// Accumulators per CTA pair: two 256-column f32 accumulators (all 512 tensor-
+// memory columns) let the epilogue of one tile overlap the MMAs of the next.
+// The pair allocation is collective: both CTAs receive the same columns (the
+// kernel checks this and reports kSitePairTmem otherwise).
+constexpr int kPairAccums = 2;
+
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_pair_variant(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& p,
+                                cudaStream_t stream) {
+    auto kern = gemm_pair_kernel<A_MN, B_MN, EPI, kPairAccums>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int max_clusters = 0;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kPairSmemBytes));
+        if (attr_err != cudaSuccess) return;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(sm_count()));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kPairSmemBytes;
+        attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    const int pairs = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+    kern<<<2 * pairs, kThreads, kPairSmemBytes, stream>>>(ma, mb, p);
     return cudaGetLastError();
 }
 
@@ -459,14 +723,14 @@ struct Raster {
     bool group_m;
 };
 
-Raster choose_raster(int tiles_m, int tiles_n, int bn, int k, int grid) {
+Raster choose_raster(int tiles_m, int tiles_n, int bm, int bn, int k, int grid) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, int, int>, Raster> cache;
-    const auto key = std::make_tuple(tiles_m, tiles_n, bn, k, grid);
+    static std::map<std::tuple<int, int, int, int, int, int>, Raster> cache;
+    const auto key = std::make_tuple(tiles_m, tiles_n, bm, bn, k, grid);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const double pa = 2.0 * BM * k, pb = 2.0 * bn * k;
+    const double pa = 2.0 * bm * k, pb = 2.0 * bn * k;
     const double l2 = 64.0 * 1024 * 1024;  // about half of the 129 MB L2
     Raster best{tiles_m, true};             // plain m-fastest order
     double best_cost = raster_cost(tiles_m, tiles_n, pa, pb, grid, tiles_m, true, l2);
@@ -507,26 +771,49 @@ cudaError_t dispatch(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMap
     return cudaErrorInvalidValue;
 }
 
+cudaError_t dispatch_pair(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMap& mb, KParams& p,
+                          cudaStream_t stream) {
+    constexpr int kStore = static_cast<int>(Epilogue::StoreBf16);
+    constexpr int kResid = static_cast<int>(Epilogue::AddResidual);
+    constexpr int kSwiglu = static_cast<int>(Epilogue::SwigluBwd);
+    constexpr int kAccum = static_cast<int>(Epilogue::AccumF32);
+    switch (g.kind) {
+        case GemmKind::Forward:
+            if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, false, kStore>(ma, mb, p, stream);
+            if (g.epi == Epilogue::AddResidual) return launch_pair_variant<false, false, kResid>(ma, mb, p, stream);
+            break;
+        case GemmKind::BackwardInput:
+            if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, true, kStore>(ma, mb, p, stream);
+            if (g.epi == Epilogue::SwigluBwd) return launch_pair_variant<false, true, kSwiglu>(ma, mb, p, stream);
+            break;
+        case GemmKind::BackwardWeight:
+            if (g.epi == Epilogue::AccumF32) return launch_pair_variant<true, true, kAccum>(ma, mb, p, stream);
+            break;
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     if (g.m <= 0 || g.n <= 0 || g.k <= 0) return cudaSuccess;
     const int sms = sm_count();
-    constexpr int bn = kBN;
+    // A CTA pair takes 256 x 256 tiles; small outputs keep the one-CTA kernel.
+    const bool pair = g.m >= kPairM && g.n >= kPairN;
+    const int tile_m = pair ? kPairM : BM;
+    const int tile_n = pair ? kPairN : kBN;
+    const uint32_t b_rows = pair ? kHalf : kBN;  // rows of a K-major B box
     CUtensorMap ma, mb;
     bool ok = true;
     switch (g.kind) {
         case GemmKind::Forward:
-            ok = encode_map(&ma, g.a, g.m, g.k, g.lda, 64, BM) &&
-                 encode_map(&mb, g.b, g.n, g.k, g.ldb, 64, static_cast<uint32_t>(bn));
+            ok = encode_map(&ma, g.a, g.m, g.k, g.lda, 64, BM) && encode_map(&mb, g.b, g.n, g.k, g.ldb, 64, b_rows);
             break;
         case GemmKind::BackwardInput:
-            ok = encode_map(&ma, g.a, g.m, g.k, g.lda, 64, BM) &&
-                 encode_map(&mb, g.b, g.k, g.n, g.ldb, 64, BK);
+            ok = encode_map(&ma, g.a, g.m, g.k, g.lda, 64, BM) && encode_map(&mb, g.b, g.k, g.n, g.ldb, 64, BK);
             break;
         case GemmKind::BackwardWeight:
-            ok = encode_map(&ma, g.a, g.k, g.m, g.lda, 64, BK) &&
-                 encode_map(&mb, g.b, g.k, g.n, g.ldb, 64, BK);
+            ok = encode_map(&ma, g.a, g.k, g.m, g.lda, 64, BK) && encode_map(&mb, g.b, g.k, g.n, g.ldb, 64, BK);
             break;
     }
     if (!ok) return cudaErrorInvalidValue;
@@ -534,11 +821,12 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     p.m = g.m;
     p.n = g.n;
     p.k = g.k;
-    p.tiles_m = (g.m + BM - 1) / BM;
-    p.tiles_n = (g.n + bn - 1) / bn;
+    p.tiles_m = (g.m + tile_m - 1) / tile_m;
+    p.tiles_n = (g.n + tile_n - 1) / tile_n;
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_blocks = (g.k + BK - 1) / BK;
-    const Raster r = choose_raster(p.tiles_m, p.tiles_n, bn, g.k, std::min(p.num_tiles, sms));
+    const int waves_of = pair ? sms / 2 : sms;
+    const Raster r = choose_raster(p.tiles_m, p.tiles_n, tile_m, tile_n, g.k, std::min(p.num_tiles, waves_of));
     p.group = r.group;
     p.group_m = r.group_m ? 1 : 0;
     p.out = g.out;
@@ -550,7 +838,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     p.mn_lbo = kMnBlockBytes;
     p.mn_sbo = 1024;
     if (!p.status) return cudaErrorInvalidDevice;
-    return dispatch<kBN>(g, ma, mb, p, stream);
+    return pair ? dispatch_pair(g, ma, mb, p, stream) : dispatch<kBN>(g, ma, mb, p, stream);
 }
 
 }  // namespace zbk

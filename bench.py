@@ -122,6 +122,25 @@ class ClockSampler:
                 "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
 
 
+# ---------------------------------------------------------------- multi-rank timing frame
+
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of `values` over all ranks (each rank times its own replica)."""
+    if dist is None:
+        return list(values)
+    import torch
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tflops(flops_per_rank, world, ms):
+    """Throughput of all ranks together: every rank does `flops_per_rank` in at most `ms`."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- oracle (host) leg
 
 
@@ -300,11 +319,8 @@ def run_ours(args, w):
     b_flops = flops_mb * m * args.steps
     w_flops = flops_mb * m * args.steps
     bw_ms = b_ms + w_ms
-    if dist is not None:
-        tt = torch.tensor([bw_ms, b_ms, w_ms, total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        bw_ms, b_ms, w_ms, total_ms = tt.tolist()
-    value = world * (b_flops + w_flops) / (bw_ms * 1e-3) / 1e12
+    bw_ms, b_ms, w_ms, total_ms = max_over_ranks([bw_ms, b_ms, w_ms, total_ms], dist, "cuda")
+    value = whole_job_tflops(b_flops + w_flops, world, bw_ms)
 
     # ---- end to end: host buffers, copies inside the timed region
     e2e = None
@@ -376,8 +392,8 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": bw_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "b_tflops": world * b_flops / (b_ms * 1e-3) / 1e12,
-            "w_tflops": world * w_flops / (w_ms * 1e-3) / 1e12,
+            "b_tflops": whole_job_tflops(b_flops, world, b_ms),
+            "w_tflops": whole_job_tflops(w_flops, world, w_ms),
             "pct_of_dense_bf16_peak": {
                 "b": 100 * b_flops / (b_ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
                 "w": 100 * w_flops / (w_ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
