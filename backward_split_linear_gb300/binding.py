@@ -23,7 +23,7 @@ STATUS_NAMES = {
     -5: "ZB_ERR_NO_MB", -6: "ZB_ERR_CUDA", -7: "ZB_ERR_DEVICE_TIMEOUT", -8: "ZB_ERR_CAPACITY",
     -9: "ZB_ERR_DEVICE", -10: "ZB_ERR_WORKSPACE",
 }
-SCHED = {"1f1b": 0, "zbh1": 1, "gpipe": 2}
+SCHED = {"1f1b": 0, "zbh1": 1, "gpipe": 2, "zb2p": 3}
 LAYER_KINDS = {"linear": 0, "mlp": 1, "transformer": 2}
 
 
@@ -65,6 +65,8 @@ _SIGS = {
                               ctypes.POINTER(c_int32)]),
     "zb_schedule_bubble": (c_int32, [c_int32, c_int32, c_int32, ctypes.POINTER(c_int32),
                                      ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
+    "zb_schedule_window_idle": (c_int32, [c_int32, c_int32, c_int32, ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_double)]),
     "zb_op_linear_forward": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                        c_void_p]),
     "zb_op_backward_input": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]),
@@ -181,6 +183,15 @@ def zb_schedule_bubble(kind, p, m):
     _check(lib().zb_schedule_bubble(SCHED[kind], p, m, ctypes.byref(span), ctypes.byref(a), ctypes.byref(b)),
            "zb_schedule_bubble")
     return span.value, a.value, b.value
+
+
+def zb_schedule_window_idle(kind, p, m):
+    """(idle units, idle / compute) inside each stage's own window, summed over stages."""
+    n = ctypes.c_int64(0)
+    f = ctypes.c_double(0)
+    _check(lib().zb_schedule_window_idle(SCHED[kind], p, m, ctypes.byref(n), ctypes.byref(f)),
+           "zb_schedule_window_idle")
+    return n.value, f.value
 
 
 # ---------------------------------------------------------------- per-step ops

@@ -310,10 +310,17 @@ constexpr size_t kAlign = 256;
 
 inline size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
-// Byte offsets, inside one stash slot, of what one layer keeps for B and W.
+// A stashed tensor: one region of the workspace holding it for every slot,
+// slot after slot with no padding ([slot][max_tokens][width]), so the stashes
+// of consecutive slots form one larger matrix.
+struct Region {
+    size_t off = kNone;  // byte offset of slot 0
+    size_t stride = 0;   // bytes per slot
+};
+
+// What one layer keeps for B and W.
 struct LayerSlot {
-    size_t x = kNone, r1 = kNone, n1 = kNone, a = kNone, h = kNone, r2 = kNone, n2 = kNone,
-           gu = kNone, s = kNone, dy = kNone, dn2 = kNone, dh = kNone, dqkv = kNone, dn1 = kNone;
+    Region x, r1, n1, a, h, r2, n2, gu, s, dy, dn2, dh, dqkv, dn1;
 };
 
 enum class MbState { Forwarded, BackwardInputDone };
@@ -326,7 +333,7 @@ struct MbEntry {
 
 struct Layout {
     std::vector<LayerSlot> layers;
-    size_t slot_bytes = 0;
+    size_t slot_bytes = 0;  // stash bytes of one microbatch
     size_t qkv_tmp = kNone;      // forward temporary, offset from the workspace start
     size_t gamma_scratch = kNone;
     size_t gamma_scratch_bytes = 0;
@@ -361,11 +368,15 @@ Layout make_layout(const zb_stage_config& c) {
     Layout L;
     const size_t T = static_cast<size_t>(c.max_tokens);
     const size_t H = static_cast<size_t>(c.hidden), F = static_cast<size_t>(c.ffn);
+    const size_t slots = static_cast<size_t>(c.max_inflight);
     size_t off = 0;
-    auto take = [&](size_t bytes) {
-        const size_t o = off;
-        off += round_up(bytes);
-        return o;
+    auto take = [&](size_t per_slot) {
+        Region r;
+        r.off = off;
+        r.stride = per_slot;
+        off += round_up(per_slot * slots);
+        L.slot_bytes += per_slot;
+        return r;
     };
     for (int l = 0; l < c.n_layers; ++l) {
         LayerSlot s;
@@ -394,14 +405,18 @@ Layout make_layout(const zb_stage_config& c) {
         }
         L.layers.push_back(s);
     }
-    L.slot_bytes = round_up(off);
-    size_t total = L.slot_bytes * static_cast<size_t>(c.max_inflight);
+    size_t total = off;
     if (c.kind == ZB_LAYER_TRANSFORMER) {
         L.qkv_tmp = total;
         total += round_up(T * static_cast<size_t>(qkv_width(c)) * 2);
     }
     if (c.kind != ZB_LAYER_LINEAR) {
-        L.gamma_scratch_bytes = zbk::rmsnorm_gamma_scratch_bytes(c.max_tokens, c.hidden);
+        // one launch reduces up to kMaxGammaProblems gammas of a W call; a flush
+        // covers up to max_inflight microbatches at once
+        const int per_layer = c.kind == ZB_LAYER_TRANSFORMER ? 2 : 1;
+        const size_t batch = static_cast<size_t>(std::min(zbk::kMaxGammaProblems, per_layer * c.n_layers));
+        L.gamma_scratch_bytes = batch * zbk::rmsnorm_gamma_scratch_bytes(
+            static_cast<int>(std::min<size_t>(T * slots, static_cast<size_t>(kMaxTokens))), c.hidden);
         L.gamma_scratch = total;
         total += round_up(L.gamma_scratch_bytes);
     }
@@ -448,10 +463,9 @@ struct zb_stage {
     int32_t inflight = 0;
     int32_t peak = 0;
 
-    uint8_t* slot_base(int slot) const { return ws + lay.slot_bytes * static_cast<size_t>(slot); }
     template <typename T = void>
-    T* at(int slot, size_t off) const {
-        return reinterpret_cast<T*>(slot_base(slot) + off);
+    T* at(int slot, const Region& r) const {
+        return reinterpret_cast<T*>(ws + r.off + r.stride * static_cast<size_t>(slot));
     }
 };
 
@@ -630,22 +644,25 @@ zb_status stage_backward_weight_body(zb_stage* st, int slot, int t, cudaStream_t
         return wgrad(st->at(slot, L.dy), st->at(slot, L.x), st->prm[0].dw, H, F);
     }
     float* scratch = reinterpret_cast<float*>(st->ws + st->lay.gamma_scratch);
-    auto dgamma = [&](const void* dn, const void* xv, const float* r, float* dg) {
-        return traced(st, ZB_KCLASS_ROW_BACKWARD_WEIGHT, 2, 0.0, dgamma_bytes(T, H), s, [&] {
-            return cuda_status(zbk::launch_rmsnorm_backward_gamma(dn, xv, r, dg, t, H, scratch, s));
-        });
-    };
+    // Every RMSNorm gamma reduction of the call runs in one launch pair.
+    std::vector<zbk::GammaProblem> gammas;
     for (int l = 0; l < c.n_layers; ++l) {
         const zb_layer_params& p = st->prm[l];
         const LayerSlot& L = st->lay.layers[l];
         ZB_TRY(wgrad(st->at(slot, L.dy), st->at(slot, L.s), p.dw_down, F, H));
         ZB_TRY(wgrad(st->at(slot, L.gu), st->at(slot, L.n2), p.dw_gu, H, 2 * F));
-        ZB_TRY(dgamma(st->at(slot, L.dn2), st->at(slot, L.h), st->at<float>(slot, L.r2), p.dgamma2));
+        gammas.push_back({st->at(slot, L.dn2), st->at(slot, L.h), st->at<float>(slot, L.r2), p.dgamma2});
         if (c.kind == ZB_LAYER_TRANSFORMER) {
             ZB_TRY(wgrad(st->at(slot, L.dh), st->at(slot, L.a), p.dw_o, H, H));
             ZB_TRY(wgrad(st->at(slot, L.dqkv), st->at(slot, L.n1), p.dw_qkv, H, Q));
-            ZB_TRY(dgamma(st->at(slot, L.dn1), st->at(slot, L.x), st->at<float>(slot, L.r1), p.dgamma1));
+            gammas.push_back({st->at(slot, L.dn1), st->at(slot, L.x), st->at<float>(slot, L.r1), p.dgamma1});
         }
+    }
+    for (size_t g0 = 0; g0 < gammas.size(); g0 += zbk::kMaxGammaProblems) {
+        const int n = static_cast<int>(std::min<size_t>(zbk::kMaxGammaProblems, gammas.size() - g0));
+        ZB_TRY(traced(st, ZB_KCLASS_ROW_BACKWARD_WEIGHT, 2, 0.0, n * dgamma_bytes(T, H), s, [&] {
+            return cuda_status(zbk::launch_rmsnorm_backward_gamma_batch(gammas.data() + g0, n, t, H, scratch, s));
+        }));
     }
     return ZB_OK;
 }
@@ -732,10 +749,37 @@ extern "C" zb_status zb_backward_weight(zb_stage_t st, int32_t mb, void* stream)
 
 extern "C" zb_status zb_wgrad_flush(zb_stage_t st, void* stream) {
     if (!st) return ZB_ERR_ARG;
-    std::vector<int32_t> pending;
-    for (const auto& kv : st->mbs)  // std::map iterates in ascending microbatch id
-        if (kv.second.state == MbState::BackwardInputDone) pending.push_back(kv.first);
-    for (int32_t mb : pending) ZB_TRY(zb_backward_weight(st, mb, stream));
+    // Pending microbatches (B done, W not), by stash slot.
+    std::vector<std::pair<int, int32_t>> pending;  // (slot, mb)
+    for (const auto& kv : st->mbs)
+        if (kv.second.state == MbState::BackwardInputDone) pending.emplace_back(kv.second.slot, kv.first);
+    if (pending.empty()) return ZB_OK;
+    ZB_TRY(device_ok());
+    std::sort(pending.begin(), pending.end());
+    const int full = st->cfg.max_tokens;
+    cudaStream_t s = as_stream(stream);
+    size_t i = 0;
+    while (i < pending.size()) {
+        // A run: consecutive slots whose microbatches all have max_tokens tokens.
+        // Their stashes are one [k * max_tokens, width] matrix per tensor, so one W
+        // over the concatenated tokens gives the sum of the k microbatches' W
+        // (every op but the weight contractions is per token).
+        size_t j = i + 1;
+        const bool first_full = st->mbs[pending[i].second].tokens == full;
+        while (first_full && j < pending.size() && pending[j].first == pending[j - 1].first + 1 &&
+               st->mbs[pending[j].second].tokens == full &&
+               static_cast<int64_t>(j + 1 - i) * full <= kMaxTokens)
+            ++j;
+        const int slot0 = pending[i].first;
+        const int tokens = first_full ? static_cast<int>(j - i) * full : st->mbs[pending[i].second].tokens;
+        ZB_TRY(stage_backward_weight_body(st, slot0, tokens, s));
+        for (size_t q = i; q < j; ++q) {
+            st->slot_used[pending[q].first] = 0;
+            st->mbs.erase(pending[q].second);
+            st->inflight -= 1;
+        }
+        i = j;
+    }
     return ZB_OK;
 }
 

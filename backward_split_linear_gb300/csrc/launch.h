@@ -44,7 +44,21 @@ cudaError_t launch_rmsnorm_forward(const void* x, const float* gamma, float eps,
 cudaError_t launch_rmsnorm_backward_input(const void* dn, const void* x, const float* rstd,
                                           const float* gamma, const void* dres, void* dx,
                                           int tokens, int hidden, cudaStream_t stream);
+// One gamma-gradient reduction: dgamma[j] += sum_t dn[t, j] x[t, j] rstd[t].
+struct GammaProblem {
+    const void* dn;
+    const void* x;
+    const float* rstd;
+    float* dgamma;
+};
+constexpr int kMaxGammaProblems = 16;
+
+// Scratch bytes of one reduction; a batch of n needs n times as much.
 size_t rmsnorm_gamma_scratch_bytes(int tokens, int hidden);
+// Up to kMaxGammaProblems reductions of the same [tokens, hidden] shape in one
+// launch pair; each problem's result is the same bits as when run alone.
+cudaError_t launch_rmsnorm_backward_gamma_batch(const GammaProblem* probs, int n, int tokens, int hidden,
+                                                float* scratch, cudaStream_t stream);
 cudaError_t launch_rmsnorm_backward_gamma(const void* dn, const void* x, const float* rstd,
                                           float* dgamma, int tokens, int hidden, float* scratch,
                                           cudaStream_t stream);

@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr size_t kStaticScratchFloats = size_t(1) << 20;  // 4 MiB of float32 partial sums
+constexpr size_t kStaticScratchFloats = size_t(1) << 17;  // 512 KiB of float32 partial sums
 
 __device__ __align__(256) float g_gamma_scratch[kStaticScratchFloats];
 

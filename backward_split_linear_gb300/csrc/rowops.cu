@@ -2,6 +2,7 @@
 // RMSNorm gamma-gradient reduction, SwiGLU forward and the attention stand-in.
 // All of them stream bf16 rows with 16-byte vector accesses (8 elements per
 // access); per-row reductions use warp shuffles and one shared-memory step.
+#include <algorithm>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -159,50 +160,72 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_kernel(
 }
 
 // ---------------------------------------------------------------- RMSNorm gamma gradient
-// Pass 1: block (cx, cy) covers columns [256 cx, 256 cx + 256) and tokens
-// [64 cy, 64 cy + 64).  Thread (g, c) sums 8 tokens (g = 0..7) of the 8
-// columns of chunk c; the 8 row groups are then added in order g = 0..7 in
-// shared memory and the block writes part[cy][256 columns].
+// Pass 1: block (cx, cy) covers columns [256 cx, 256 cx + 256) and the cy-th
+// of `parts` equal token ranges.  Thread (g, c) (g = 0..7 row group, c = 0..31
+// chunk of 8 columns) streams tokens t0 + g, t0 + g + 8, ... of that range,
+// four tokens of loads in flight; the 8 row groups are then added in order
+// g = 0..7 in shared memory and the block writes part[cy][256 columns].
+// `parts` depends only on T and H (about 320 blocks in all), never on the
+// device, so the partition and hence the float32 sums are reproducible.
 // Pass 2: dgamma[j] += part[0][j] + part[1][j] + ... in order.
-// Fixed assignment and fixed order make the result bitwise reproducible.
-constexpr int kGammaCols = 256;                 // columns per block
-constexpr int kGammaChunks = kGammaCols / 8;    // 32 threads across the columns
+constexpr int kGammaCols = 256;                           // columns per block
+constexpr int kGammaChunks = kGammaCols / 8;              // 32 threads across the columns
 constexpr int kGammaGroups = kRowThreads / kGammaChunks;  // 8 row groups
-constexpr int kGammaGroupRows = 8;
-constexpr int kGammaRows = kGammaGroups * kGammaGroupRows;  // 64 tokens per block
+constexpr int kGammaTargetBlocks = 320;
+constexpr int kGammaUnroll = 4;
 
-__global__ void __launch_bounds__(kRowThreads) dgamma_partial_kernel(
-    const uint16_t* __restrict__ dn, const uint16_t* __restrict__ x, const float* __restrict__ rstd,
-    float* __restrict__ part, int tokens, int hidden) {
+int gamma_parts(int tokens, int hidden) {
+    const int col_blocks = (hidden + kGammaCols - 1) / kGammaCols;
+    const int want = (kGammaTargetBlocks + col_blocks - 1) / col_blocks;
+    const int most = (tokens + kGammaGroups - 1) / kGammaGroups;  // at least 8 tokens per part
+    return std::max(1, std::min(want, most));
+}
+
+// Several reductions of the same shape in one launch: problem blockIdx.z.
+struct GammaBatch {
+    GammaProblem prob[kMaxGammaProblems];
+    int tokens, hidden, parts;
+};
+
+__global__ void __launch_bounds__(kRowThreads) dgamma_partial_kernel(const __grid_constant__ GammaBatch b,
+                                                                     float* __restrict__ part_all) {
     __shared__ float acc_s[kGammaGroups][kGammaCols];
+    const uint16_t* __restrict__ dn = static_cast<const uint16_t*>(b.prob[blockIdx.z].dn);
+    const uint16_t* __restrict__ x = static_cast<const uint16_t*>(b.prob[blockIdx.z].x);
+    const float* __restrict__ rstd = b.prob[blockIdx.z].rstd;
+    const int tokens = b.tokens, hidden = b.hidden, parts = b.parts;
+    float* __restrict__ part = part_all + static_cast<int64_t>(blockIdx.z) * parts * hidden;
     const int cl = threadIdx.x % kGammaChunks;
     const int grp = threadIdx.x / kGammaChunks;
     const int col = blockIdx.x * kGammaCols + 8 * cl;
-    const bool col_ok = col < hidden;
-    const int t0 = blockIdx.y * kGammaRows + grp * kGammaGroupRows;
+    const int per = (tokens + parts - 1) / parts;
+    const int t0 = blockIdx.y * per;
+    const int t1 = min(tokens, t0 + per);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (col_ok) {
-        uint4 dv[kGammaGroupRows], xv[kGammaGroupRows];
-        float rr[kGammaGroupRows];
+    if (col < hidden) {
+        for (int tb = t0 + grp; tb < t1; tb += kGammaGroups * kGammaUnroll) {
+            uint4 dv[kGammaUnroll], xv[kGammaUnroll];
+            float rr[kGammaUnroll];
 #pragma unroll
-        for (int i = 0; i < kGammaGroupRows; ++i) {
-            const int t = t0 + i;
-            if (t < tokens) {
-                dv[i] = *reinterpret_cast<const uint4*>(dn + static_cast<int64_t>(t) * hidden + col);
-                xv[i] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * hidden + col);
-                rr[i] = rstd[t];
+            for (int i = 0; i < kGammaUnroll; ++i) {
+                const int t = tb + i * kGammaGroups;
+                if (t < t1) {
+                    dv[i] = *reinterpret_cast<const uint4*>(dn + static_cast<int64_t>(t) * hidden + col);
+                    xv[i] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * hidden + col);
+                    rr[i] = rstd[t];
+                }
             }
-        }
 #pragma unroll
-        for (int i = 0; i < kGammaGroupRows; ++i) {
-            if (t0 + i < tokens) {
-                const uint32_t dw[4] = {dv[i].x, dv[i].y, dv[i].z, dv[i].w};
-                const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+            for (int i = 0; i < kGammaUnroll; ++i) {
+                if (tb + i * kGammaGroups < t1) {
+                    const uint32_t dw[4] = {dv[i].x, dv[i].y, dv[i].z, dv[i].w};
+                    const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float d = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
-                    const float xx = (e & 1) ? bf16_hi(xw[e >> 1]) : bf16_lo(xw[e >> 1]);
-                    acc[e] += d * (xx * rr[i]);
+                    for (int e = 0; e < 8; ++e) {
+                        const float d = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
+                        const float xx = (e & 1) ? bf16_hi(xw[e >> 1]) : bf16_lo(xw[e >> 1]);
+                        acc[e] += d * (xx * rr[i]);
+                    }
                 }
             }
         }
@@ -221,21 +244,33 @@ __global__ void __launch_bounds__(kRowThreads) dgamma_partial_kernel(
 }
 
 // Pass 2: block covers 32 columns; thread (c, g) adds the partials q = g,
-// g + 8, g + 16, ... of column c in order, then thread (c, 0) adds the 8
-// sums in order g = 0..7 and accumulates into dgamma.
+// g + 8, g + 16, ... of column c in order (loads issued first), then thread
+// (c, 0) adds the 8 sums in order g = 0..7 and accumulates into dgamma.
 constexpr int kFinalCols = 32;
 constexpr int kFinalGroups = 8;
+constexpr int kFinalMaxPerThread = 8;  // parts <= 64 loads issued together; more loop
 
-__global__ void __launch_bounds__(kFinalCols * kFinalGroups) dgamma_final_kernel(
-    const float* __restrict__ part, int parts, float* dgamma, int hidden) {
+__global__ void __launch_bounds__(kFinalCols * kFinalGroups) dgamma_final_kernel(const __grid_constant__ GammaBatch b,
+                                                                                 const float* __restrict__ part_all) {
     __shared__ float sums[kFinalGroups][kFinalCols];
+    const int parts = b.parts, hidden = b.hidden;
+    const float* __restrict__ part = part_all + static_cast<int64_t>(blockIdx.y) * parts * hidden;
+    float* dgamma = b.prob[blockIdx.y].dgamma;
     const int c = threadIdx.x % kFinalCols;
     const int g = threadIdx.x / kFinalCols;
     const int j = blockIdx.x * kFinalCols + c;
     float s = 0.f;
     if (j < hidden) {
-#pragma unroll 4
-        for (int q = g; q < parts; q += kFinalGroups) s += part[static_cast<int64_t>(q) * hidden + j];
+        for (int q0 = g; q0 < parts; q0 += kFinalGroups * kFinalMaxPerThread) {
+            float v[kFinalMaxPerThread];
+#pragma unroll
+            for (int i = 0; i < kFinalMaxPerThread; ++i) {
+                const int q = q0 + i * kFinalGroups;
+                v[i] = q < parts ? part[static_cast<int64_t>(q) * hidden + j] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < kFinalMaxPerThread; ++i) s += v[i];
+        }
     }
     sums[g][c] = s;
     __syncthreads();
@@ -400,22 +435,30 @@ cudaError_t launch_rmsnorm_backward_input(const void* dn, const void* x, const f
 
 size_t rmsnorm_gamma_scratch_bytes(int tokens, int hidden) {
     if (tokens <= 0 || hidden <= 0) return 0;
-    const size_t parts = (static_cast<size_t>(tokens) + kGammaRows - 1) / kGammaRows;
-    return parts * static_cast<size_t>(hidden) * sizeof(float);
+    return static_cast<size_t>(gamma_parts(tokens, hidden)) * static_cast<size_t>(hidden) * sizeof(float);
+}
+
+cudaError_t launch_rmsnorm_backward_gamma_batch(const GammaProblem* probs, int n, int tokens, int hidden,
+                                                float* scratch, cudaStream_t stream) {
+    if (tokens <= 0 || n <= 0) return cudaSuccess;
+    if (n > kMaxGammaProblems) return cudaErrorInvalidValue;
+    GammaBatch b{};
+    for (int i = 0; i < n; ++i) b.prob[i] = probs[i];
+    b.tokens = tokens;
+    b.hidden = hidden;
+    b.parts = gamma_parts(tokens, hidden);
+    const dim3 grid1((hidden + kGammaCols - 1) / kGammaCols, b.parts, n);
+    dgamma_partial_kernel<<<grid1, kRowThreads, 0, stream>>>(b, scratch);
+    const dim3 grid2((hidden + kFinalCols - 1) / kFinalCols, n);
+    dgamma_final_kernel<<<grid2, kFinalCols * kFinalGroups, 0, stream>>>(b, scratch);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_backward_gamma(const void* dn, const void* x, const float* rstd,
                                           float* dgamma, int tokens, int hidden, float* scratch,
                                           cudaStream_t stream) {
-    if (tokens <= 0) return cudaSuccess;
-    const int parts = (tokens + kGammaRows - 1) / kGammaRows;
-    const dim3 grid1((hidden + kGammaCols - 1) / kGammaCols, parts);
-    dgamma_partial_kernel<<<grid1, kRowThreads, 0, stream>>>(static_cast<const uint16_t*>(dn),
-                                                            static_cast<const uint16_t*>(x), rstd,
-                                                            scratch, tokens, hidden);
-    dgamma_final_kernel<<<(hidden + kFinalCols - 1) / kFinalCols, kFinalCols * kFinalGroups, 0, stream>>>(
-        scratch, parts, dgamma, hidden);
-    return cudaGetLastError();
+    const GammaProblem p{dn, x, rstd, dgamma};
+    return launch_rmsnorm_backward_gamma_batch(&p, 1, tokens, hidden, scratch, stream);
 }
 
 cudaError_t launch_swiglu_forward(const void* gu, void* s, int tokens, int ffn, cudaStream_t stream) {

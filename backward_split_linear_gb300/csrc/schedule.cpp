@@ -11,6 +11,11 @@
 //    ceiling a W must run before the next F;
 //  - section "Mathematical Modeling": unit op times, bubble formulas.
 //
+// ZB-2p (section "Core Innovation 2", item 2): the same policy with a ceiling
+// of 2p held microbatches and 2(p-s)-1 forwards before the first B of stage
+// s; every stage then works without idle from its first op to its last when
+// m >= 2p - 1.  Emitted by a step-by-step run of the policy.
+//
 // ZB-H1, m >= p, in closed form for stage s:
 //   F_0 .. F_{p-s-1}
 //   B_j, F_{p-s+j}            for j = 0 .. s-1
@@ -72,20 +77,27 @@ void order_zbh1_closed(int s, int p, int m, std::vector<Op>& o) {
     for (int k = m - s; k < m; ++k) o.push_back({'W', k});
 }
 
-// Step-by-step run of the ZB-H1 policy on all p stages (used when m < p).
-// At every unit of time each free stage, looking at the state at that time:
-// runs its next F/B (1F1B order) if that op's inputs exist, unless it is an
-// F that would pass the ceiling of p held microbatches, in which case it runs
-// its oldest pending W; if the next F/B is not ready it runs the oldest
-// pending W; else it idles.
-std::vector<std::vector<Op>> zbh1_policy_all(int p, int m) {
-    std::vector<std::vector<Op>> fb(p), out(p);
-    for (int s = 0; s < p; ++s) {
-        std::vector<Op> o;
-        order_1f1b(s, p, m, o);
-        for (const Op& op : o)
-            if (op.kind != 'W') fb[s].push_back(op);
+// F/B order of stage s: `warm` forwards, then B and F alternate, then the last B.
+void fb_order(int warm, int m, std::vector<Op>& o) {
+    warm = std::min(warm, m);
+    for (int i = 0; i < warm; ++i) o.push_back({'F', i});
+    for (int j = 0; j < m - warm; ++j) {
+        o.push_back({'B', j});
+        o.push_back({'F', warm + j});
     }
+    for (int i = m - warm; i < m; ++i) o.push_back({'B', i});
+}
+
+// Step-by-step run of the ZB-H1 policy on all p stages.  At every unit of
+// time each free stage, looking at the state at that time: runs its next F/B
+// if that op's inputs exist, unless it is an F that would pass the ceiling of
+// `limit` held microbatches, in which case it runs its oldest pending W; if
+// the next F/B is not ready it runs the oldest pending W; else it idles.
+// Stage s runs warm(s) forwards before its first B: p - s for ZB-H1 (the 1F1B
+// order), 2(p - s) - 1 for ZB-2p.
+std::vector<std::vector<Op>> zb_policy_all(int p, int m, int limit, bool two_p) {
+    std::vector<std::vector<Op>> fb(p), out(p);
+    for (int s = 0; s < p; ++s) fb_order(two_p ? 2 * (p - s) - 1 : p - s, m, fb[s]);
     // finish time of F/B per (stage, mb); -1 = not run
     std::vector<int> fin_f(p * m, -1), fin_b(p * m, -1);
     std::vector<size_t> ptr(p, 0);
@@ -106,7 +118,7 @@ std::vector<std::vector<Op>> zbh1_policy_all(int p, int m) {
                     ready = fin_f[s * m + nx.mb] >= 0 && fin_f[s * m + nx.mb] <= t &&
                             (s == p - 1 || (fin_b[(s + 1) * m + nx.mb] >= 0 && fin_b[(s + 1) * m + nx.mb] <= t));
                 if (ready) {
-                    if (nx.kind == 'F' && held[s] >= p) {
+                    if (nx.kind == 'F' && held[s] >= limit) {
                         if (!pending[s].empty()) choice[s] = {'W', pending[s].front()};
                     } else {
                         choice[s] = nx;
@@ -147,14 +159,18 @@ void stage_order(zb_sched_kind kind, int s, int p, int m, std::vector<Op>& o) {
         order_gpipe(s, p, m, o);
     } else if (kind == ZB_SCHED_1F1B) {
         order_1f1b(s, p, m, o);
+    } else if (kind == ZB_SCHED_ZB2P) {
+        o = zb_policy_all(p, m, 2 * p, true)[s];
     } else if (m >= p) {
         order_zbh1_closed(s, p, m, o);
     } else {
-        o = zbh1_policy_all(p, m)[s];
+        o = zb_policy_all(p, m, p, false)[s];
     }
 }
 
-bool valid_kind(int k) { return k == ZB_SCHED_1F1B || k == ZB_SCHED_ZBH1 || k == ZB_SCHED_GPIPE; }
+bool valid_kind(int k) {
+    return k == ZB_SCHED_1F1B || k == ZB_SCHED_ZBH1 || k == ZB_SCHED_GPIPE || k == ZB_SCHED_ZB2P;
+}
 
 }  // namespace
 
@@ -168,6 +184,7 @@ extern "C" zb_status zb_schedule(zb_sched_kind kind, int32_t stage, int32_t p, i
     std::vector<Op> o;
     o.reserve(3 * m);
     stage_order(kind, stage, p, m, o);
+    if (o.size() != static_cast<size_t>(3 * m)) return ZB_ERR_ORDER;  // policy run did not finish
     for (int i = 0; i < 3 * m; ++i) {
         out[i].kind = static_cast<uint8_t>(o[i].kind);
         out[i].pad[0] = out[i].pad[1] = out[i].pad[2] = 0;
@@ -176,17 +193,20 @@ extern "C" zb_status zb_schedule(zb_sched_kind kind, int32_t stage, int32_t p, i
     return ZB_OK;
 }
 
-extern "C" zb_status zb_schedule_bubble(zb_sched_kind kind, int32_t p, int32_t m, int32_t* makespan,
-                                        double* idle_over_compute, double* idle_over_wall) {
-    if (!valid_kind(kind) || p < 1 || m < 1 || p > 4096 || m > (1 << 20)) return ZB_ERR_ARG;
-    const bool split = kind == ZB_SCHED_ZBH1;
+// Unit-time run of the p stages' orders: finish time of every op's stage
+// window, and the makespan.  Returns false if the orders deadlock.
+namespace {
+bool run_unit_model(zb_sched_kind kind, int p, int m, int* span_out, long long* window_idle_out) {
+    const bool split = kind == ZB_SCHED_ZBH1 || kind == ZB_SCHED_ZB2P;
     std::vector<std::vector<Op>> orders(p);
-    for (int s = 0; s < p; ++s) stage_order(kind, s, p, m, orders[s]);
-    // finish times per (kind, stage, mb)
+    for (int s = 0; s < p; ++s) {
+        stage_order(kind, s, p, m, orders[s]);
+        if (orders[s].size() != static_cast<size_t>(3 * m)) return false;
+    }
     auto idx = [m](int s, int i) { return s * m + i; };
     std::vector<int> ff(p * m, -1), fb(p * m, -1), fw(p * m, -1);
     std::vector<size_t> ptr(p, 0);
-    std::vector<int> free_at(p, 0);
+    std::vector<int> free_at(p, 0), first(p, -1), last(p, 0);
     size_t placed = 0, total = static_cast<size_t>(3) * m * p;
     int span = 0;
     while (placed < total) {
@@ -219,6 +239,8 @@ extern "C" zb_status zb_schedule_bubble(zb_sched_kind kind, int32_t p, int32_t m
                 if (!ok) break;
                 const int fin = ready + 1;
                 (op.kind == 'F' ? ff : op.kind == 'B' ? fb : fw)[idx(s, op.mb)] = fin;
+                if (first[s] < 0) first[s] = ready;
+                last[s] = fin;
                 free_at[s] = fin;
                 span = std::max(span, fin);
                 ++ptr[s];
@@ -226,8 +248,33 @@ extern "C" zb_status zb_schedule_bubble(zb_sched_kind kind, int32_t p, int32_t m
                 progressed = true;
             }
         }
-        if (!progressed) return ZB_ERR_ORDER;  // orders deadlock (cannot happen for valid kinds)
+        if (!progressed) return false;
     }
+    long long window_idle = 0;
+    for (int s = 0; s < p; ++s) window_idle += (last[s] - first[s]) - 3LL * m;
+    *span_out = span;
+    *window_idle_out = window_idle;
+    return true;
+}
+}  // namespace
+
+extern "C" zb_status zb_schedule_window_idle(zb_sched_kind kind, int32_t p, int32_t m, int64_t* idle_units,
+                                             double* idle_over_compute) {
+    if (!valid_kind(kind) || p < 1 || m < 1 || p > 4096 || m > (1 << 20)) return ZB_ERR_ARG;
+    int span = 0;
+    long long idle = 0;
+    if (!run_unit_model(kind, p, m, &span, &idle)) return ZB_ERR_ORDER;
+    if (idle_units) *idle_units = idle;
+    if (idle_over_compute) *idle_over_compute = static_cast<double>(idle) / (3.0 * m * p);
+    return ZB_OK;
+}
+
+extern "C" zb_status zb_schedule_bubble(zb_sched_kind kind, int32_t p, int32_t m, int32_t* makespan,
+                                        double* idle_over_compute, double* idle_over_wall) {
+    if (!valid_kind(kind) || p < 1 || m < 1 || p > 4096 || m > (1 << 20)) return ZB_ERR_ARG;
+    int span = 0;
+    long long window_idle = 0;
+    if (!run_unit_model(kind, p, m, &span, &window_idle)) return ZB_ERR_ORDER;
     const double compute = 3.0 * m * p;
     const double idle = static_cast<double>(p) * span - compute;
     if (makespan) *makespan = span;

@@ -84,8 +84,11 @@ typedef enum {
                            each W right after its B */
     ZB_SCHED_ZBH1 = 1,  /* [G4] ZB-1F1B: 1F1B order of F and B, W deferred into
                            slots that would idle, at most p microbatches held */
-    ZB_SCHED_GPIPE = 2  /* the guide's section "1. The GPipe Bubble": all F,
+    ZB_SCHED_GPIPE = 2, /* the guide's section "1. The GPipe Bubble": all F,
                            then each B followed by its W */
+    ZB_SCHED_ZB2P = 3   /* [G4] ZB-2p: the ZB-H1 policy with 2(p-s)-1 warm-up
+                           forwards and at most 2p microbatches held; no idle
+                           inside any stage's own window when m >= 2p - 1 */
 } zb_sched_kind;
 
 typedef struct {
@@ -99,8 +102,8 @@ typedef struct {
  * `*n_out`.  Errors: ZB_ERR_ARG (p < 1, m < 1, stage outside [0, p),
  * null n_out, out null with cap > 0); ZB_ERR_CAPACITY when cap < 3m (then
  * *n_out = 3m and nothing is written).  For ZB-H1 with m >= p the order is
- * emitted in closed form; with m < p it comes from a unit-time run of the
- * policy.  Both give every W after its B after its F. */
+ * emitted in closed form; with m < p, and for ZB-2p, it comes from a
+ * unit-time run of the policy.  All give every W after its B after its F. */
 zb_status zb_schedule(zb_sched_kind kind, int32_t stage, int32_t p, int32_t m,
                       zb_op* out, int32_t cap, int32_t* n_out);
 
@@ -112,6 +115,14 @@ zb_status zb_schedule(zb_sched_kind kind, int32_t stage, int32_t p, int32_t m,
 zb_status zb_schedule_bubble(zb_sched_kind kind, int32_t p, int32_t m,
                              int32_t* makespan, double* idle_over_compute,
                              double* idle_over_wall);
+
+/* Same model, idle counted inside each stage's own window (from its first op's
+ * start to its last op's end) instead of over the common makespan: the sense
+ * in which the guide's section "Core Innovation 2" says ZB-2p leaves every GPU
+ * busy.  Returns the summed idle units and idle / compute.  Any output
+ * pointer may be NULL. */
+zb_status zb_schedule_window_idle(zb_sched_kind kind, int32_t p, int32_t m,
+                                  int64_t* idle_units, double* idle_over_compute);
 
 /* ========================================================================
  * Per-step operations (stateless).  One call per step of the hot path; the
@@ -182,12 +193,12 @@ zb_status zb_op_rmsnorm_backward_gamma(const void* dn, const void* x, const floa
  * workspace.  Others run where all device memory belongs to another allocator,
  * so a cudaMalloc of their own would fail or synchronise the device.  These
  * callers cannot provide `scratch`, so this variant keeps the partial sums in
- * a fixed 4 MiB float32 array inside the library.
+ * a fixed 512 KiB float32 array inside the library.
  *  - Every GPU that loads the library holds that array until the process exits.
  *  - Size limit: zb_op_rmsnorm_backward_gamma_scratch_bytes(tokens, hidden)
  *    must not exceed 4 * zb_op_rmsnorm_backward_gamma_noalloc_max_floats()
- *    bytes (4 MiB), which admits at least T = 4096 at H = 8192.  Larger sizes
- *    return ZB_ERR_SHAPE and enqueue nothing.
+ *    bytes (512 KiB); that admits every token count for hidden <= 131072.
+ *    Larger sizes return ZB_ERR_SHAPE and enqueue nothing.
  *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *    routine.
  *  - The first call on a device looks up the array's device address (with that
@@ -301,9 +312,15 @@ zb_status zb_backward_input(zb_stage_t st, int32_t mb, const void* dy, void* dx,
  * Errors: ZB_ERR_NO_MB, ZB_ERR_ORDER (B not run yet). */
 zb_status zb_backward_weight(zb_stage_t st, int32_t mb, void* stream);
 
-/* Runs W for every microbatch whose B ran and whose W did not, in ascending
- * microbatch id (so the sums are bitwise reproducible).  The accumulators
- * then hold the sum over all microbatches once `stream` gets there. */
+/* Runs W for every microbatch whose B ran and whose W did not, then
+ * releases their stash slots.  The accumulators hold the sum over all
+ * microbatches once `stream` gets there.  Microbatches of max_tokens tokens
+ * in consecutive stash slots are done as one W over their concatenated
+ * tokens: one GEMM per weight with k * max_tokens contraction length and one
+ * float32 add into each accumulator element, instead of k.  That is exact
+ * arithmetic (every op but the weight contractions acts per token), and it
+ * rounds differently from k separate W calls.  The batches run in ascending
+ * slot order, so a given sequence of calls always gives the same bits. */
 zb_status zb_wgrad_flush(zb_stage_t st, void* stream);
 
 /* Synchronises `stream` and reads the device status word (see

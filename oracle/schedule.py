@@ -32,6 +32,14 @@ Orders:
   ceiling) contradicts that hard ceiling and is not used.  The listing's
   first three rules alone do not give the section's own (p-1)/(3m) bubble
   (at p=4, m=8 they take 29 units where this reading takes 3m+p-1 = 27).
+* ZB-2p (section "Core Innovation 2", item 2: the in-flight limit doubles to
+  2p, the warm-up and cool-down bubbles vanish and every GPU computes without
+  idle waiting).  Reading: the same policy with a ceiling of 2p and 2(p-s)-1
+  forwards before the first B of stage s.  In the unit-time model every
+  stage is then busy from its first op to its last (``window_idle`` = 0,
+  for m >= 2p - 1) while holding up to 2p microbatches; over the common
+  makespan nothing changes, since 3m + p - 1 is already the shortest
+  possible when communication is free.
 """
 from __future__ import annotations
 
@@ -99,15 +107,29 @@ def simulate_orders(orders, p, split):
     return start
 
 
-def simulate_zbh1(p, m, limit=None):
+def fb_order(s, p, m, warm):
+    """F/B order of stage s: `warm` forwards, then B and F alternate, then the last B."""
+    warm = min(warm, m)
+    out = [(F, i) for i in range(warm)]
+    for j in range(m - warm):
+        out += [(B, j), (F, warm + j)]
+    out += [(B, i) for i in range(m - warm, m)]
+    return out
+
+
+def simulate_zbh1(p, m, limit=None, warm=None):
     """Time-stepped run of the ZB-H1 policy on all p stages.
 
+    ``limit`` is the in-flight ceiling (default p) and ``warm(s)`` the number of
+    forwards stage s runs before its first B (default p - s, as in 1F1B).
     Returns (orders, start): per-stage lists of (kind, mb) and the start time
     of every op.
     """
     if limit is None:
         limit = p
-    fb = [[op for op in order_1f1b(s, p, m) if op[0] != W] for s in range(p)]
+    if warm is None:
+        warm = lambda s: p - s  # noqa: E731
+    fb = [fb_order(s, p, m, warm(s)) for s in range(p)]
     ptr = [0] * p
     orders = [[] for _ in range(p)]
     start = {}
@@ -160,6 +182,11 @@ def simulate_zbh1(p, m, limit=None):
     return orders, start
 
 
+def simulate_zb2p(p, m):
+    """ZB-2p: the ZB-H1 policy with ceiling 2p and 2(p - s) - 1 warm-up forwards."""
+    return simulate_zbh1(p, m, limit=2 * p, warm=lambda s: 2 * (p - s) - 1)
+
+
 def orders_for(kind, p, m):
     """Per-stage orders for "gpipe", "1f1b" or "zbh1"."""
     if kind == "gpipe":
@@ -168,13 +195,15 @@ def orders_for(kind, p, m):
         return [order_1f1b(s, p, m) for s in range(p)]
     if kind == "zbh1":
         return simulate_zbh1(p, m)[0]
+    if kind == "zb2p":
+        return simulate_zb2p(p, m)[0]
     raise ValueError(kind)
 
 
 def timeline(kind, p, m):
     """(orders, start times) of a schedule under the unit-time model."""
     orders = orders_for(kind, p, m)
-    split = kind == "zbh1"
+    split = kind in ("zbh1", "zb2p")
     return orders, simulate_orders(orders, p, split)
 
 
@@ -204,3 +233,14 @@ def peak_in_flight(order):
         elif kind == W:
             cur -= 1
     return peak
+
+
+def window_idle(kind, p, m):
+    """Idle units inside each stage's own active window (its first op's start to
+    its last op's end), summed over the stages."""
+    orders, start = timeline(kind, p, m)
+    idle = 0
+    for s, order in enumerate(orders):
+        ts = [start[(k, s, i)] for k, i in order]
+        idle += (max(ts) + 1 - min(ts)) - len(order)
+    return idle

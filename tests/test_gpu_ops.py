@@ -201,3 +201,38 @@ def test_wait_timeout_is_reported_and_cleared():
     assert st == -7 and code == 9
     assert zb.zb_device_status()[0] == 0
     test_backward_input(127, 320, 576)
+
+
+@pytest.mark.parametrize("t,n_in,n_out", [(4096, 4096, 512), (4000, 4032, 320)])
+def test_backward_input_many_tiles(t, n_in, n_out):
+    """256 CTA-pair tiles: the last wave runs as half tiles (ragged in the second case)."""
+    rng = np.random.default_rng(21)
+    dyb, dy = draw_bf16(rng, (t, n_out))
+    wb, w = draw_bf16(rng, (n_out, n_in), 0.05)
+    dx = empty_bf16(t, n_in)
+    zb.zb_op_backward_input(bf16_from_bits(dyb), bf16_from_bits(wb), dx, t, n_in, n_out)
+    assert_close(f64_from_bf16(dx), dy @ w, "backward input, many tiles")
+
+
+@pytest.mark.parametrize("t,n_in,n_out", [(300, 4096, 4096), (129, 4032, 4000 // 64 * 64)])
+def test_backward_weight_many_tiles(t, n_in, n_out):
+    rng = np.random.default_rng(22)
+    xb, x = draw_bf16(rng, (t, n_in))
+    dyb, dy = draw_bf16(rng, (t, n_out))
+    dw = torch.zeros(n_out, n_in, dtype=torch.float32, device="cuda")
+    zb.zb_op_backward_weight(bf16_from_bits(dyb), bf16_from_bits(xb), dw, t, n_in, n_out)
+    assert_close(dw.cpu().numpy(), dy.T @ x, "backward weight, many tiles")
+
+
+def test_backward_input_swiglu_many_tiles():
+    rng = np.random.default_rng(23)
+    t, hidden, ffn = 4096, 256, 4096
+    dyb, dy = draw_bf16(rng, (t, hidden))
+    wb, w = draw_bf16(rng, (hidden, ffn), 0.05)
+    gub, gu = draw_bf16(rng, (t, 2 * ffn), 1.3)
+    dgu = empty_bf16(t, 2 * ffn)
+    zb.zb_op_backward_input_swiglu(bf16_from_bits(dyb), bf16_from_bits(wb), bf16_from_bits(gub), dgu, t, hidden, ffn)
+    dg, du = S.swiglu_grads(dy @ w, gu[:, :ffn], gu[:, ffn:])
+    got = f64_from_bf16(dgu)
+    assert_close(got[:, :ffn], dg, "dg, many tiles")
+    assert_close(got[:, ffn:], du, "du, many tiles")

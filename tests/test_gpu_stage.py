@@ -269,3 +269,25 @@ def test_stage_runs_are_bitwise_reproducible():
     for li in range(2):
         for k in first[li]:
             assert torch.equal(first[li][k], st.grads[li][k])
+
+
+def test_flush_batches_consecutive_full_microbatches():
+    """zb_wgrad_flush runs the pending W of consecutive full stash slots as one W over their
+    concatenated tokens (the concatenated-batch identity): it must agree with separate W calls
+    to float32 summation order and with the oracle to the stage tolerance.  Microbatch 2 is
+    short, so it splits the pending slots into the runs {0, 1}, {2}, {3, 4}."""
+    c = SMALL_TF
+    tok = [128, 128, 77, 128, 128]
+    inp = synth.stage_inputs(c["kind"], 2, 256, 512, 4, 2, 64, n_mb=5, seed=11, tokens_per_mb=tok)
+    st_batched = make_gpu_stage(c, inp, 128, 5)
+    run_gpu(st_batched, inp, [("F", i) for i in range(5)] + [("B", i) for i in range(5)])  # W in the flush
+    st_single = make_gpu_stage(c, inp, 128, 5)
+    run_gpu(st_single, inp, [("F", i) for i in range(5)] + [("B", i) for i in range(5)] + [("W", i) for i in range(5)])
+    _, g_ref = run_oracle(c, inp)
+    for li in range(2):
+        for k, ref in g_ref[li].items():
+            a = st_batched.grads[li][k].double()
+            b = st_single.grads[li][k].double()
+            assert (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item() < 1e-5, (li, k)
+            assert_close(a.cpu().numpy(), ref, f"flushed d{k}", fro_tol=stage_fro_tol(2))
+    assert st_batched.stats()[:1] == (0,)

@@ -128,3 +128,38 @@ def test_planted_simulator_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(S, "_deps", no_wait_downstream)
     with pytest.raises(AssertionError):
         test_printed_bubble_values()
+
+
+@pytest.mark.parametrize("p", [1, 2, 3, 4, 5, 8])
+def test_zb2p_claims(p):
+    """"Zero-Bubble Pipeline Parallelism Guide for LLMs", section "Core Innovation 2",
+    item 2 (ZB-2p): at most 2p microbatches held, and no GPU idles once m is large enough
+    (here: no idle inside any stage's own window for m >= 2p - 1)."""
+    for m in range(2 * p - 1, 2 * p + 12):
+        orders = S.orders_for("zb2p", p, m)
+        assert max(S.peak_in_flight(o) for o in orders) <= 2 * p
+        assert S.window_idle("zb2p", p, m) == 0
+        _, start = S.timeline("zb2p", p, m)
+        assert S.makespan(start) == 3 * m + p - 1
+
+
+def test_zbh1_window_idle_is_the_ramp():
+    """ZB-H1 keeps idle inside the stages' windows: stage s waits s units for its first
+    input or p-1-s units at the end, p(p-1)/2 in all; ZB-2p removes it."""
+    for p in (2, 4, 8):
+        for m in (2 * p, 3 * p):
+            assert S.window_idle("zbh1", p, m) == p * (p - 1) // 2
+            assert S.window_idle("zb2p", p, m) == 0
+
+
+@pytest.mark.parametrize("p,m", [(1, 1), (2, 1), (4, 2), (4, 8), (8, 3), (8, 16), (5, 13)])
+def test_zb2p_invariants(p, m):
+    orders, start = S.timeline("zb2p", p, m)
+    for order in orders:
+        assert len(order) == 3 * m
+        pos = {op: j for j, op in enumerate(order)}
+        for i in range(m):
+            assert pos[(S.F, i)] < pos[(S.B, i)] < pos[(S.W, i)]
+    for (k, s, i), t in start.items():
+        for d in S._deps(k, s, i, p, True):
+            assert start[d] + 1 <= t
