@@ -23,10 +23,18 @@ Readings where the pages are silent (the pages show a single linear only):
   qkv = n1 W_qkv^T; a = A(qkv); h = x + a W_o^T; then the mlp part.
 * RMSNorm(x; g) = g * x * r with r = (mean_j x_j^2 + eps)^(-1/2) per token.
 * W_gu = [W_gate; W_up]: gate rows first.
-* A is a weight-free stand-in for the attention core: head h of the output is
-  q_h + k_j + v_j with j = floor(h / (n_heads / n_kv_heads)) (a grouped-query
-  broadcast sum).  It is linear and per token, so every identity the tests use
-  still holds.
+* A is the attention core, in one of two forms (``shp["attention"]``):
+  - "standin" (the default): a weight-free stand-in; head h of the output is
+    q_h + k_j + v_j with j = floor(h / (n_heads / n_kv_heads)) (a
+    grouped-query broadcast sum).  It is linear and per token, so every
+    identity the tests use still holds.
+  - "causal": softmax attention with a causal mask and grouped K/V heads,
+    a_h = softmax(q_h k_j^T / sqrt(head_dim), keys <= query) v_j, over
+    independent sequences of ``shp["seq_len"]`` consecutive tokens of the
+    microbatch (0: the whole microbatch is one sequence; a last, shorter
+    sequence takes the remaining tokens).  No position encoding is applied.
+    Tokens mix only inside a sequence, so the concatenated-batch identity
+    holds for microbatches made of whole sequences.
 * Weight gradients accumulate: the caller's float64 accumulators start at zero
   and every W adds into them (section "Memory Management & Activation
   Rollback": gradients are accumulated in place in fixed buffers).
@@ -133,6 +141,85 @@ def attention_standin_grad(da, n_heads, n_kv_heads, head_dim):
     return np.concatenate([da, dkv, dkv], axis=1)
 
 
+def _heads(qkv, n_heads, n_kv_heads, head_dim):
+    t, d = qkv.shape[0], head_dim
+    q = qkv[:, : n_heads * d].reshape(t, n_heads, d)
+    k = qkv[:, n_heads * d : (n_heads + n_kv_heads) * d].reshape(t, n_kv_heads, d)
+    v = qkv[:, (n_heads + n_kv_heads) * d :].reshape(t, n_kv_heads, d)
+    return q, k, v
+
+
+def sequences(t, seq_len):
+    """(start, end) of the consecutive sequences of a microbatch of t tokens."""
+    step = seq_len if seq_len else max(t, 1)
+    return [(s0, min(t, s0 + step)) for s0 in range(0, t, step)]
+
+
+def causal_probs(q, k, scale):
+    """Softmax over keys of scale * q k^T with keys after the query masked out."""
+    n = q.shape[0]
+    scores = scale * (q @ k.T)
+    scores = np.where(np.tril(np.ones((n, n), dtype=bool)), scores, -np.inf)
+    e = np.exp(scores - scores.max(axis=1, keepdims=True))
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def attention_causal(qkv, n_heads, n_kv_heads, head_dim, seq_len):
+    """a[:, head h] = softmax(q_h k_j^T / sqrt(d), causal) v_j per sequence, j = h // group."""
+    t = qkv.shape[0]
+    q, k, v = _heads(qkv, n_heads, n_kv_heads, head_dim)
+    group = n_heads // n_kv_heads
+    scale = 1.0 / np.sqrt(head_dim)
+    a = np.zeros((t, n_heads, head_dim))
+    for s0, s1 in sequences(t, seq_len):
+        for h in range(n_heads):
+            j = h // group
+            p = causal_probs(q[s0:s1, h], k[s0:s1, j], scale)
+            a[s0:s1, h] = p @ v[s0:s1, j]
+    return a.reshape(t, n_heads * head_dim)
+
+
+def attention_causal_grad(da, qkv, n_heads, n_kv_heads, head_dim, seq_len):
+    """Gradient of attention_causal with respect to qkv, given da.
+
+    With P = softmax(S), S = scale q k^T and a = P v:
+      dv += P^T da,  dP = da v^T,  dS = P * (dP - rowsum(dP * P)),
+      dq = scale dS k,  dk += scale dS^T q,
+    the sums over the heads of a group going to the shared k and v.
+    """
+    t = qkv.shape[0]
+    q, k, v = _heads(qkv, n_heads, n_kv_heads, head_dim)
+    group = n_heads // n_kv_heads
+    scale = 1.0 / np.sqrt(head_dim)
+    da3 = da.reshape(t, n_heads, head_dim)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for s0, s1 in sequences(t, seq_len):
+        for h in range(n_heads):
+            j = h // group
+            p = causal_probs(q[s0:s1, h], k[s0:s1, j], scale)
+            dv[s0:s1, j] += p.T @ da3[s0:s1, h]
+            dp = da3[s0:s1, h] @ v[s0:s1, j].T
+            ds = p * (dp - np.sum(dp * p, axis=1, keepdims=True))
+            dq[s0:s1, h] = scale * (ds @ k[s0:s1, j])
+            dk[s0:s1, j] += scale * (ds.T @ q[s0:s1, h])
+    return np.concatenate([dq.reshape(t, -1), dk.reshape(t, -1), dv.reshape(t, -1)], axis=1)
+
+
+def attention_forward(qkv, shp):
+    if shp.get("attention", "standin") == "causal":
+        return attention_causal(qkv, shp["n_heads"], shp["n_kv_heads"], shp["head_dim"], shp.get("seq_len", 0))
+    return attention_standin(qkv, shp["n_heads"], shp["n_kv_heads"], shp["head_dim"])
+
+
+def attention_backward(da, qkv, shp):
+    if shp.get("attention", "standin") == "causal":
+        return attention_causal_grad(da, qkv, shp["n_heads"], shp["n_kv_heads"], shp["head_dim"],
+                                     shp.get("seq_len", 0))
+    return attention_standin_grad(da, shp["n_heads"], shp["n_kv_heads"], shp["head_dim"])
+
+
 # ----------------------------------------------------------------------------
 # F: forward of one layer and of the stage
 # ----------------------------------------------------------------------------
@@ -147,9 +234,9 @@ def layer_forward(x, prm, shp):
     if kind == "transformer":
         n1, r1 = rmsnorm(x, prm["gamma1"], shp["eps"])
         qkv = n1 @ prm["w_qkv"].T
-        a = attention_standin(qkv, shp["n_heads"], shp["n_kv_heads"], shp["head_dim"])
+        a = attention_forward(qkv, shp)
         h = x + a @ prm["w_o"].T
-        saved.update({"n1": n1, "r1": r1, "a": a})
+        saved.update({"n1": n1, "r1": r1, "a": a, "qkv": qkv})
     else:
         h = x
     n2, r2 = rmsnorm(h, prm["gamma2"], shp["eps"])
@@ -194,7 +281,7 @@ def layer_backward_input(dy, prm, saved, shp):
     if kind == "mlp":
         return dh, kept
     da = dh @ prm["w_o"]  # B of the output projection
-    dqkv = attention_standin_grad(da, shp["n_heads"], shp["n_kv_heads"], shp["head_dim"])
+    dqkv = attention_backward(da, saved["qkv"], shp)
     dn1 = dqkv @ prm["w_qkv"]  # B of qkv
     dx = dh + rmsnorm_input_grad(dn1, saved["x"], saved["r1"], prm["gamma1"])
     kept.update({"dh": dh, "dqkv": dqkv, "dn1": dn1})
@@ -290,9 +377,12 @@ def stage_backward_fused(dy, params, saved, shp):
         da = dh @ prm["w_o"]
         nh, nkv, d = shp["n_heads"], shp["n_kv_heads"], shp["head_dim"]
         t = da.shape[0]
-        da_heads = da.reshape(t, nkv, nh // nkv, d)
-        dk = da_heads.sum(axis=2).reshape(t, nkv * d)
-        dqkv = np.hstack([da, dk, dk])
+        if shp.get("attention", "standin") == "causal":
+            dqkv = _causal_grad_by_rows(da, sv["qkv"], nh, nkv, d, shp.get("seq_len", 0))
+        else:
+            da_heads = da.reshape(t, nkv, nh // nkv, d)
+            dk = da_heads.sum(axis=2).reshape(t, nkv * d)
+            dqkv = np.hstack([da, dk, dk])
         gr["w_qkv"] = dqkv.T @ sv["n1"]
         dn1 = dqkv @ prm["w_qkv"]
         xh1 = sv["x"] * sv["r1"][:, None]
@@ -303,6 +393,33 @@ def stage_backward_fused(dy, params, saved, shp):
         grads.append(gr)
     grads.reverse()
     return dy, grads
+
+
+def _causal_grad_by_rows(da, qkv, nh, nkv, d, seq_len):
+    """The causal attention gradient written query row by query row, with the
+    softmax Jacobian diag(p) - p p^T formed explicitly (for the fused backward)."""
+    t = qkv.shape[0]
+    q = qkv[:, : nh * d]
+    k = qkv[:, nh * d : (nh + nkv) * d]
+    v = qkv[:, (nh + nkv) * d :]
+    out = np.zeros_like(qkv)
+    rep = nh // nkv
+    step = seq_len if seq_len else max(t, 1)
+    for h in range(nh):
+        qc = slice(h * d, (h + 1) * d)
+        kc = slice((h // rep) * d, (h // rep + 1) * d)
+        for i in range(t):
+            s0 = (i // step) * step
+            keys = np.arange(s0, i + 1)
+            z = (k[keys][:, kc] @ q[i, qc]) / np.sqrt(d)
+            p = np.exp(z - z.max())
+            p = p / p.sum()
+            jac = np.diag(p) - np.outer(p, p)
+            dz = jac @ (v[keys][:, kc] @ da[i, qc])
+            out[i, qc] += (dz @ k[keys][:, kc]) / np.sqrt(d)
+            out[keys, nh * d + kc.start : nh * d + kc.stop] += np.outer(dz, q[i, qc]) / np.sqrt(d)
+            out[keys, (nh + nkv) * d + kc.start : (nh + nkv) * d + kc.stop] += np.outer(p, da[i, qc])
+    return out
 
 
 # ----------------------------------------------------------------------------

@@ -28,6 +28,12 @@ SHAPES = {
                 head_dim=0, eps=1e-5),
     "linear": dict(kind="linear", n_layers=1, hidden=8, ffn=12, n_heads=0, n_kv_heads=0,
                    head_dim=0, eps=1e-5),
+    # causal softmax attention: sequences of 3 tokens (the 4- to 6-token cases hold a
+    # whole sequence and a shorter last one), 4 query heads on 2 kv heads
+    "causal": dict(kind="transformer", n_layers=2, hidden=16, ffn=8, n_heads=4, n_kv_heads=2,
+                   head_dim=4, eps=1e-5, attention="causal", seq_len=3),
+    "causal_one_seq": dict(kind="transformer", n_layers=1, hidden=8, ffn=8, n_heads=2, n_kv_heads=1,
+                           head_dim=4, eps=1e-5, attention="causal", seq_len=0),
 }
 
 
@@ -112,12 +118,35 @@ def torch_forward(x, params, shp):
             rep = nh // nkv
             kk = k.reshape(t, nkv, 1, d).expand(t, nkv, rep, d).reshape(t, nh * d)
             vv = v.reshape(t, nkv, 1, d).expand(t, nkv, rep, d).reshape(t, nh * d)
-            h = x + (q + kk + vv) @ prm["w_o"].t()
+            if shp.get("attention") == "causal":
+                a = torch_causal_attention(q, kk, vv, nh, d, shp["seq_len"])
+            else:
+                a = q + kk + vv
+            h = x + a @ prm["w_o"].t()
         else:
             h = x
         gate, up = torch.chunk(norm(h, prm["gamma2"]) @ prm["w_gu"].t(), 2, dim=1)
         x = h + (torch.nn.functional.silu(gate) * up) @ prm["w_down"].t()
     return x
+
+
+def torch_causal_attention(q, k, v, nh, d, seq_len):
+    """Per head and per sequence: masked scores, softmax, weighted values (k, v already
+    repeated to one per query head)."""
+    t = q.shape[0]
+    step = seq_len or t
+    outs = []
+    for s0 in range(0, t, step):
+        s1 = min(t, s0 + step)
+        n = s1 - s0
+        qh = q[s0:s1].reshape(n, nh, d).transpose(0, 1)
+        kh = k[s0:s1].reshape(n, nh, d).transpose(0, 1)
+        vh = v[s0:s1].reshape(n, nh, d).transpose(0, 1)
+        scores = qh @ kh.transpose(1, 2) / d ** 0.5
+        future = torch.triu(torch.ones(n, n, dtype=torch.bool), diagonal=1)
+        w = torch.softmax(scores.masked_fill(future, float("-inf")), dim=-1)
+        outs.append((w @ vh).transpose(0, 1).reshape(n, nh * d))
+    return torch.cat(outs)
 
 
 def autograd_grads(params, x, G, shp):
@@ -173,14 +202,16 @@ def test_split_equals_fused(name):
     assert split_vs_fused_err(params, x, G, shp) < 1e-12
 
 
-@pytest.mark.parametrize("name", ["transformer", "mlp", "linear"])
+@pytest.mark.parametrize("name", ["transformer", "mlp", "linear", "causal"])
 def test_concat_identity(name):
-    """sum over microbatches of dW(mb) == dW(concatenation of the microbatches)."""
+    """sum over microbatches of dW(mb) == dW(concatenation of the microbatches); with
+    causal attention the microbatches hold whole sequences."""
     shp = SHAPES[name]
     params, _, _ = make_case(shp)
     rng = np.random.default_rng(7)
     out = shp["ffn"] if shp["kind"] == "linear" else shp["hidden"]
-    mbs = [(rng.standard_normal((t, shp["hidden"])), rng.standard_normal((t, out))) for t in (3, 5, 2)]
+    sizes = (3, 6, 3) if shp.get("attention") == "causal" else (3, 5, 2)
+    mbs = [(rng.standard_normal((t, shp["hidden"])), rng.standard_normal((t, out))) for t in sizes]
     st = S.StageOracle(params, shp)
     dxs = []
     for i, (x, g) in enumerate(mbs):
@@ -222,6 +253,35 @@ def test_forward_closed_forms():
     assert np.array_equal(y, [[-1.0, -1.0, -1.0]])
 
 
+def test_causal_attention_special_cases():
+    """Closed forms of the causal attention core, and the library's own attention routine."""
+    rng = np.random.default_rng(3)
+    t, nh, nkv, d = 7, 4, 2, 8
+    qkv = rng.standard_normal((t, (nh + 2 * nkv) * d))
+    q, k, v = S._heads(qkv, nh, nkv, d)
+    # sequences of one token: each query sees only its own key, so a_h = v_j
+    a = S.attention_causal(qkv, nh, nkv, d, 1).reshape(t, nh, d)
+    for h in range(nh):
+        assert np.allclose(a[:, h], v[:, h // 2], rtol=0, atol=1e-15)
+    # q = 0: equal weights over the keys so far, so a is the running mean of v
+    q0 = qkv.copy()
+    q0[:, : nh * d] = 0.0
+    a = S.attention_causal(q0, nh, nkv, d, 0).reshape(t, nh, d)
+    run_mean = np.cumsum(v, axis=0) / np.arange(1, t + 1)[:, None, None]
+    for h in range(nh):
+        assert np.allclose(a[:, h], run_mean[:, h // 2], rtol=1e-14, atol=1e-14)
+    # sequences of 3: the second sequence does not see the first
+    a3 = S.attention_causal(qkv, nh, nkv, d, 3)
+    assert np.allclose(a3[3:6], S.attention_causal(qkv[3:6], nh, nkv, d, 0), rtol=0, atol=1e-15)
+    # torch's scaled_dot_product_attention (float64, causal) on the same heads
+    tq = torch.tensor(q).transpose(0, 1)
+    tk = torch.tensor(k).repeat_interleave(nh // nkv, dim=1).transpose(0, 1)
+    tv = torch.tensor(v).repeat_interleave(nh // nkv, dim=1).transpose(0, 1)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
+    got = S.attention_causal(qkv, nh, nkv, d, 0).reshape(t, nh, d)
+    assert np.allclose(got, ref.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
 def test_linear_textbook_case():
     """Section "Core Innovation 1": dX = dY W (weights [out, in]) and dW = dY^T X.
 
@@ -257,6 +317,32 @@ def _bad_standin_grad(da, nh, nkv, d):
     return np.concatenate([da, dkv, dkv], axis=1)
 
 
+def _bad_causal_grad(da, qkv, nh, nkv, d, seq_len):
+    """Drops the rowsum(dP * P) term of the softmax backward."""
+    t = qkv.shape[0]
+    q, k, v = S._heads(qkv, nh, nkv, d)
+    da3 = da.reshape(t, nh, d)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s0, s1 in S.sequences(t, seq_len):
+        for h in range(nh):
+            j = h // (nh // nkv)
+            p = S.causal_probs(q[s0:s1, h], k[s0:s1, j], 1 / np.sqrt(d))
+            dv[s0:s1, j] += p.T @ da3[s0:s1, h]
+            ds = p * (da3[s0:s1, h] @ v[s0:s1, j].T)
+            dq[s0:s1, h] = ds @ k[s0:s1, j] / np.sqrt(d)
+            dk[s0:s1, j] += ds.T @ q[s0:s1, h] / np.sqrt(d)
+    return np.concatenate([dq.reshape(t, -1), dk.reshape(t, -1), dv.reshape(t, -1)], axis=1)
+
+
+def _bad_causal_mask(q, k, scale):
+    """Lets each query see the next key too."""
+    n = q.shape[0]
+    scores = scale * (q @ k.T)
+    scores = np.where(np.tril(np.ones((n, n), dtype=bool), k=1), scores, -np.inf)
+    e = np.exp(scores - scores.max(axis=1, keepdims=True))
+    return e / e.sum(axis=1, keepdims=True)
+
+
 def _bad_gamma_grad(dn, x, r):
     return np.sum(dn * x, axis=0)  # dropped r
 
@@ -272,6 +358,8 @@ MUTANTS = {
     "standin_no_group_sum": ("attention_standin_grad", _bad_standin_grad),
     "gamma_dropped_r": ("rmsnorm_gamma_grad", _bad_gamma_grad),
     "rmsnorm_eps_outside": ("rmsnorm", _bad_rmsnorm_fwd),
+    "causal_no_rowsum": ("attention_causal_grad", _bad_causal_grad),
+    "causal_mask_off_by_one": ("causal_probs", _bad_causal_mask),
 }
 
 
@@ -279,7 +367,7 @@ MUTANTS = {
 def test_planted_mistakes_are_caught(mutant, monkeypatch):
     name, fn = MUTANTS[mutant]
     monkeypatch.setattr(S, name, fn)
-    shp = SHAPES["gqa4"]
+    shp = SHAPES["causal" if mutant.startswith("causal") else "gqa4"]
     params, x, G = make_case(shp, tokens=3, seed=5)
     caught = (autograd_max_rel_err(params, x, G, shp) > 1e-6
               or fd_max_rel_err(params, x, G, shp) > 1e-6)
