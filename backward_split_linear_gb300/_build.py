@@ -22,7 +22,7 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libzb.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["gemm.cu", "rowops.cu", "noalloc.cu", "api.cpp", "schedule.cpp"]
+SOURCES = ["gemm.cu", "attention.cu", "rowops.cu", "noalloc.cu", "api.cpp", "schedule.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

@@ -41,7 +41,7 @@ class zb_op(ctypes.Structure):
 class zb_stage_config(ctypes.Structure):
     _fields_ = [("kind", c_int32), ("n_layers", c_int32), ("hidden", c_int32), ("ffn", c_int32),
                 ("n_heads", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32), ("eps", c_float),
-                ("max_tokens", c_int32), ("max_inflight", c_int32)]
+                ("max_tokens", c_int32), ("max_inflight", c_int32), ("attention", c_int32), ("seq_len", c_int32)]
 
 
 class zb_kernel_stats(ctypes.Structure):
@@ -50,7 +50,8 @@ class zb_kernel_stats(ctypes.Structure):
 
 
 KERNEL_CLASSES = ["gemm_forward", "gemm_backward_input", "gemm_backward_weight", "row_backward_input",
-                  "row_backward_weight", "row_forward"]
+                  "row_backward_weight", "row_forward", "attn_forward", "attn_backward"]
+ATTENTION_KINDS = {"standin": 0, "causal": 1}
 
 
 class zb_layer_params(ctypes.Structure):
@@ -67,6 +68,8 @@ _SIGS = {
                                      ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
     "zb_schedule_window_idle": (c_int32, [c_int32, c_int32, c_int32, ctypes.POINTER(ctypes.c_int64),
                                           ctypes.POINTER(ctypes.c_double)]),
+    "zb_schedule_search": (c_int32, [c_int32] * 7 + [ctypes.POINTER(zb_op), c_int32, ctypes.POINTER(c_int32),
+                                     ctypes.POINTER(c_int32), ctypes.POINTER(ctypes.c_int64)]),
     "zb_op_linear_forward": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                        c_void_p]),
     "zb_op_backward_input": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]),
@@ -86,6 +89,9 @@ _SIGS = {
                                         c_void_p]),
     "zb_op_swiglu_forward": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_void_p]),
     "zb_op_attention_forward": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p]),
+    "zb_op_attention_stat_stride": (c_int32, [c_int32]),
+    "zb_op_attention_causal_forward": (c_int32, [c_void_p, c_void_p, c_void_p] + [c_int32] * 5 + [c_void_p]),
+    "zb_op_attention_causal_backward": (c_int32, [c_void_p] * 6 + [c_int32] * 5 + [c_void_p]),
     "zb_device_status": (c_int32, [c_void_p, c_int32, ctypes.POINTER(c_int32)]),
     "zb_selftest_wait_timeout": (c_int32, [c_int32, c_void_p]),
     "zb_stage_workspace_bytes": (c_size_t, [ctypes.POINTER(zb_stage_config)]),
@@ -175,6 +181,17 @@ def zb_schedule_raw(kind, stage, p, m, cap):
     return st, n.value, [(chr(buf[i].kind), buf[i].mb) for i in range(min(max(n.value, 0), cap))]
 
 
+def zb_schedule_search(stage, p, m, mem_limit, t_f, t_b, t_w):
+    """(order of `stage`, chosen ceiling, makespan) of the memory-limited search."""
+    arr = (zb_op * (3 * m))()
+    n = c_int32(0)
+    limit = c_int32(0)
+    span = ctypes.c_int64(0)
+    _check(lib().zb_schedule_search(stage, p, m, mem_limit, t_f, t_b, t_w, arr, 3 * m, ctypes.byref(n),
+                                    ctypes.byref(limit), ctypes.byref(span)), "zb_schedule_search")
+    return [(chr(arr[i].kind), arr[i].mb) for i in range(n.value)], limit.value, span.value
+
+
 def zb_schedule_bubble(kind, p, m):
     """(makespan, idle / compute, idle / wall) of the unit-time pipeline model."""
     span = c_int32(0)
@@ -262,6 +279,23 @@ def zb_op_attention_forward(qkv, a, tokens, n_heads, n_kv_heads, head_dim, strea
                                          _stream(stream)), "zb_op_attention_forward")
 
 
+def zb_op_attention_stat_stride(tokens):
+    return lib().zb_op_attention_stat_stride(tokens)
+
+
+def zb_op_attention_causal_forward(qkv, a, lse, tokens, n_heads, n_kv_heads, head_dim, seq_len=0, stream=None):
+    _check(lib().zb_op_attention_causal_forward(_ptr(qkv), _ptr(a), _ptr(lse), tokens, n_heads, n_kv_heads,
+                                                head_dim, seq_len, _stream(stream)),
+           "zb_op_attention_causal_forward")
+
+
+def zb_op_attention_causal_backward(qkv, a, da, lse, dvec, dqkv, tokens, n_heads, n_kv_heads, head_dim,
+                                    seq_len=0, stream=None):
+    _check(lib().zb_op_attention_causal_backward(_ptr(qkv), _ptr(a), _ptr(da), _ptr(lse), _ptr(dvec), _ptr(dqkv),
+                                                 tokens, n_heads, n_kv_heads, head_dim, seq_len, _stream(stream)),
+           "zb_op_attention_causal_backward")
+
+
 def zb_device_status(stream=None, reset=False):
     """(status, code): status is ZB_OK or ZB_ERR_DEVICE_TIMEOUT; never raises on a timeout."""
     code = c_int32(0)
@@ -279,9 +313,9 @@ def zb_selftest_wait_timeout(limit_us, stream=None):
 
 
 def make_config(kind, n_layers, hidden, ffn, n_heads=0, n_kv_heads=0, head_dim=0, eps=1e-5, max_tokens=128,
-                max_inflight=1):
+                max_inflight=1, attention="standin", seq_len=0):
     return zb_stage_config(LAYER_KINDS[kind], n_layers, hidden, ffn, n_heads, n_kv_heads, head_dim, eps,
-                           max_tokens, max_inflight)
+                           max_tokens, max_inflight, ATTENTION_KINDS[attention], seq_len)
 
 
 def zb_stage_workspace_bytes(cfg):

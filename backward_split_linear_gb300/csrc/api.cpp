@@ -58,8 +58,22 @@ inline zb_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ZB_OK : 
 
 // ------------------------------------------------------------ op bodies (checked by callers)
 
+// K-split scratch of a stage (see GemmArgs); the per-step ops run without it.
+struct SplitWs {
+    uint32_t* flags;
+    float* partial;
+    int tiles;
+};
+
+void set_split(GemmArgs& g, const SplitWs* ws) {
+    if (!ws) return;
+    g.split_flags = ws->flags;
+    g.split_partial = ws->partial;
+    g.split_tiles = ws->tiles;
+}
+
 zb_status run_linear_forward(const void* x, const void* w, const void* residual, void* y, int t,
-                             int in, int out, cudaStream_t s) {
+                             int in, int out, cudaStream_t s, const SplitWs* ws = nullptr) {
     GemmArgs g{};
     g.kind = GemmKind::Forward;
     g.epi = residual ? Epilogue::AddResidual : Epilogue::StoreBf16;
@@ -74,11 +88,12 @@ zb_status run_linear_forward(const void* x, const void* w, const void* residual,
     g.ldo = out;
     g.aux = residual;
     g.ld_aux = out;
+    set_split(g, ws);
     return cuda_status(zbk::launch_gemm(g, s));
 }
 
 zb_status run_backward_input(const void* dy, const void* w, void* dx, int t, int in, int out,
-                             int64_t ldo, cudaStream_t s) {
+                             int64_t ldo, cudaStream_t s, const SplitWs* ws = nullptr) {
     GemmArgs g{};
     g.kind = GemmKind::BackwardInput;
     g.epi = Epilogue::StoreBf16;
@@ -91,11 +106,12 @@ zb_status run_backward_input(const void* dy, const void* w, void* dx, int t, int
     g.k = out;
     g.out = dx;
     g.ldo = ldo;
+    set_split(g, ws);
     return cuda_status(zbk::launch_gemm(g, s));
 }
 
 zb_status run_backward_input_swiglu(const void* dy, const void* w_down, const void* gu, void* dgu,
-                                    int t, int hidden, int ffn, cudaStream_t s) {
+                                    int t, int hidden, int ffn, cudaStream_t s, const SplitWs* ws = nullptr) {
     GemmArgs g{};
     g.kind = GemmKind::BackwardInput;
     g.epi = Epilogue::SwigluBwd;
@@ -111,6 +127,7 @@ zb_status run_backward_input_swiglu(const void* dy, const void* w_down, const vo
     g.aux = gu;
     g.ld_aux = 2 * static_cast<int64_t>(ffn);
     g.ffn = ffn;
+    set_split(g, ws);
     return cuda_status(zbk::launch_gemm(g, s));
 }
 
@@ -130,7 +147,7 @@ zb_status run_backward_input_attention(const void* dh, const void* w_o, void* dq
 }
 
 zb_status run_backward_weight(const void* dy, const void* x, float* dw, int t, int in, int out,
-                              cudaStream_t s) {
+                              cudaStream_t s, const SplitWs* ws = nullptr) {
     GemmArgs g{};
     g.kind = GemmKind::BackwardWeight;
     g.epi = Epilogue::AccumF32;
@@ -143,6 +160,7 @@ zb_status run_backward_weight(const void* dy, const void* x, float* dw, int t, i
     g.k = t;
     g.out = dw;
     g.ldo = in;
+    set_split(g, ws);
     return cuda_status(zbk::launch_gemm(g, s));
 }
 
@@ -150,6 +168,36 @@ bool heads_ok(int32_t nh, int32_t nkv, int32_t hd) {
     if (nh <= 0 || nkv <= 0 || hd <= 0 || hd % 8 != 0 || nh % nkv != 0) return false;
     if (!feature_ok(nh * hd) || !feature_ok((nh + 2 * nkv) * hd)) return false;
     return true;
+}
+
+// Causal attention: head_dim 64 or 128, sequences of a multiple of 128 tokens (or one sequence).
+bool causal_ok(int32_t nh, int32_t nkv, int32_t hd, int32_t seq_len) {
+    return heads_ok(nh, nkv, hd) && (hd == 64 || hd == 128) && seq_len >= 0 && seq_len % 128 == 0;
+}
+
+// Floats per head row of the attention statistics (lse, rowsum): whole 128-row blocks.
+int32_t stat_stride(int32_t tokens) { return std::max<int32_t>(128, (tokens + 127) / 128 * 128); }
+
+zbk::AttnShape attn_shape(int t, int nh, int nkv, int hd, int seq_len, int ld_stat) {
+    zbk::AttnShape a;
+    a.tokens = t;
+    a.n_heads = nh;
+    a.n_kv_heads = nkv;
+    a.head_dim = hd;
+    a.seq_len = seq_len;
+    a.ld_stat = ld_stat;
+    return a;
+}
+
+// Query-key pairs a causal mask leaves visible over the sequences of t tokens.
+double causal_pairs(int t, int seq_len) {
+    const int step = seq_len > 0 ? seq_len : std::max(t, 1);
+    double n = 0.0;
+    for (int s0 = 0; s0 < t; s0 += step) {
+        const double len = std::min(t, s0 + step) - s0;
+        n += len * (len + 1.0) / 2.0;
+    }
+    return n;
 }
 
 }  // namespace
@@ -292,6 +340,33 @@ extern "C" zb_status zb_op_swiglu_forward(const void* gu, void* s, int32_t token
     return cuda_status(zbk::launch_swiglu_forward(gu, s, tokens, ffn, as_stream(stream)));
 }
 
+extern "C" int32_t zb_op_attention_stat_stride(int32_t tokens) { return tokens_ok(tokens) ? stat_stride(tokens) : 0; }
+
+extern "C" zb_status zb_op_attention_causal_forward(const void* qkv, void* a, float* lse, int32_t tokens,
+                                                    int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                                    int32_t seq_len, void* stream) {
+    if (!tokens_ok(tokens) || !causal_ok(n_heads, n_kv_heads, head_dim, seq_len)) return ZB_ERR_SHAPE;
+    if (!rows_ok(qkv, tokens) || !rows_ok(a, tokens) || !rows_ok(lse, tokens)) return ZB_ERR_ARG;
+    ZB_TRY(device_ok());
+    return cuda_status(zbk::launch_attention_causal_forward(
+        attn_shape(tokens, n_heads, n_kv_heads, head_dim, seq_len, stat_stride(tokens)), qkv, a, lse,
+        as_stream(stream)));
+}
+
+extern "C" zb_status zb_op_attention_causal_backward(const void* qkv, const void* a, const void* da,
+                                                     const float* lse, float* dvec, void* dqkv, int32_t tokens,
+                                                     int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                                     int32_t seq_len, void* stream) {
+    if (!tokens_ok(tokens) || !causal_ok(n_heads, n_kv_heads, head_dim, seq_len)) return ZB_ERR_SHAPE;
+    const void* rows[] = {qkv, a, da, lse, dvec, dqkv};
+    for (const void* p : rows)
+        if (!rows_ok(p, tokens)) return ZB_ERR_ARG;
+    ZB_TRY(device_ok());
+    return cuda_status(zbk::launch_attention_causal_backward(
+        attn_shape(tokens, n_heads, n_kv_heads, head_dim, seq_len, stat_stride(tokens)), qkv, a, da, lse, dvec,
+        dqkv, as_stream(stream)));
+}
+
 extern "C" zb_status zb_op_attention_forward(const void* qkv, void* a, int32_t tokens, int32_t n_heads,
                                              int32_t n_kv_heads, int32_t head_dim, void* stream) {
     if (!tokens_ok(tokens) || !heads_ok(n_heads, n_kv_heads, head_dim)) return ZB_ERR_SHAPE;
@@ -321,6 +396,7 @@ struct Region {
 // What one layer keeps for B and W.
 struct LayerSlot {
     Region x, r1, n1, a, h, r2, n2, gu, s, dy, dn2, dh, dqkv, dn1;
+    Region qkv, lse;  // causal attention only: its input and row statistics, for B
 };
 
 enum class MbState { Forwarded, BackwardInputDone };
@@ -335,8 +411,14 @@ struct Layout {
     std::vector<LayerSlot> layers;
     size_t slot_bytes = 0;  // stash bytes of one microbatch
     size_t qkv_tmp = kNone;      // forward temporary, offset from the workspace start
+    size_t da_tmp = kNone;       // causal attention: gradient of a, B temporary
+    size_t dvec = kNone;         // causal attention: rowsum(dO * O), B temporary
+    int32_t ld_stat = 0;         // causal attention: floats per head row of lse / dvec
     size_t gamma_scratch = kNone;
     size_t gamma_scratch_bytes = 0;
+    size_t split_flags = kNone;  // K-split scratch of the GEMMs (flags, then partial tiles)
+    size_t split_partial = kNone;
+    int split_tiles = 0;
     size_t total = 0;
 };
 
@@ -347,6 +429,9 @@ zb_status check_config(const zb_stage_config* c) {
     if (c->n_layers < 1 || c->n_layers > 4096 || c->max_inflight < 1 || c->max_inflight > 4096 ||
         !(c->eps >= 0.f) || c->max_tokens < 1 || c->max_tokens > kMaxTokens)
         return ZB_ERR_ARG;
+    if (c->attention != ZB_ATTN_STANDIN && c->attention != ZB_ATTN_CAUSAL) return ZB_ERR_ARG;
+    if (c->attention == ZB_ATTN_STANDIN && c->seq_len != 0) return ZB_ERR_ARG;
+    if (c->attention == ZB_ATTN_CAUSAL && c->kind != ZB_LAYER_TRANSFORMER) return ZB_ERR_ARG;
     switch (c->kind) {
         case ZB_LAYER_LINEAR:
             if (c->n_layers != 1) return ZB_ERR_ARG;
@@ -358,6 +443,8 @@ zb_status check_config(const zb_stage_config* c) {
         case ZB_LAYER_TRANSFORMER:
             if (!feature_ok(c->hidden) || !feature_ok(c->ffn)) return ZB_ERR_SHAPE;
             if (!heads_ok(c->n_heads, c->n_kv_heads, c->head_dim) || c->n_heads * c->head_dim != c->hidden)
+                return ZB_ERR_SHAPE;
+            if (c->attention == ZB_ATTN_CAUSAL && !causal_ok(c->n_heads, c->n_kv_heads, c->head_dim, c->seq_len))
                 return ZB_ERR_SHAPE;
             return ZB_OK;
     }
@@ -393,6 +480,10 @@ Layout make_layout(const zb_stage_config& c) {
                 s.dh = take(T * H * 2);
                 s.dqkv = take(T * static_cast<size_t>(qkv_width(c)) * 2);
                 s.dn1 = take(T * H * 2);
+                if (c.attention == ZB_ATTN_CAUSAL) {
+                    s.qkv = take(T * static_cast<size_t>(qkv_width(c)) * 2);
+                    s.lse = take(static_cast<size_t>(c.n_heads) * stat_stride(c.max_tokens) * 4);
+                }
             } else {
                 s.h = s.x;  // MLP layer: h = x
             }
@@ -406,7 +497,13 @@ Layout make_layout(const zb_stage_config& c) {
         L.layers.push_back(s);
     }
     size_t total = off;
-    if (c.kind == ZB_LAYER_TRANSFORMER) {
+    if (c.kind == ZB_LAYER_TRANSFORMER && c.attention == ZB_ATTN_CAUSAL) {
+        L.ld_stat = stat_stride(c.max_tokens);
+        L.da_tmp = total;
+        total += round_up(T * H * 2);
+        L.dvec = total;
+        total += round_up(static_cast<size_t>(c.n_heads) * L.ld_stat * 4);
+    } else if (c.kind == ZB_LAYER_TRANSFORMER) {
         L.qkv_tmp = total;
         total += round_up(T * static_cast<size_t>(qkv_width(c)) * 2);
     }
@@ -419,6 +516,25 @@ Layout make_layout(const zb_stage_config& c) {
             static_cast<int>(std::min<size_t>(T * slots, static_cast<size_t>(kMaxTokens))), c.hidden);
         L.gamma_scratch = total;
         total += round_up(L.gamma_scratch_bytes);
+    }
+    // K-split scratch for the largest GEMM output of the stage, up to the
+    // largest launch that may split.
+    {
+        const int64_t Tt = static_cast<int64_t>(c.max_tokens);
+        auto tiles = [](int64_t m, int64_t n) { return ((m + 255) / 256) * ((n + 255) / 256); };
+        int64_t most = 0;
+        const int64_t Hh = c.hidden, Ff = c.ffn;
+        if (c.kind == ZB_LAYER_LINEAR) {
+            most = std::max({tiles(Tt, Ff), tiles(Tt, Hh), tiles(Ff, Hh)});
+        } else {
+            most = std::max({tiles(Tt, 2 * Ff), tiles(Tt, Hh), tiles(2 * Ff, Hh), tiles(Hh, Ff)});
+            if (c.kind == ZB_LAYER_TRANSFORMER) most = std::max(most, tiles(qkv_width(c), Hh));
+        }
+        L.split_tiles = static_cast<int>(std::min<int64_t>(most, zbk::kSplitMaxTiles));
+        L.split_flags = total;
+        total += round_up(static_cast<size_t>(L.split_tiles) * zbk::kSplitTileFlagBytes);
+        L.split_partial = total;
+        total += round_up(static_cast<size_t>(L.split_tiles) * zbk::kSplitTilePartialBytes);
     }
     L.total = total;
     return L;
@@ -462,6 +578,7 @@ struct zb_stage {
     std::map<int32_t, MbEntry> mbs;
     int32_t inflight = 0;
     int32_t peak = 0;
+    bool split_zeroed = false;  // K-split flags cleared on the device
 
     template <typename T = void>
     T* at(int slot, const Region& r) const {
@@ -483,6 +600,21 @@ zb_status traced(zb_stage* st, zb_kernel_class cls, int launches, double flops, 
     if (cudaEventRecord(b, s) != cudaSuccess) return ZB_ERR_CUDA;
     st->tr.recs.push_back(Tracer::Rec{cls, launches, flops, bytes, a, b});
     return r;
+}
+
+// The stage's K-split scratch; its flags are cleared on `s` before first use.
+zb_status stage_split_ws(zb_stage* st, cudaStream_t s, SplitWs* out) {
+    const Layout& L = st->lay;
+    if (!st->split_zeroed) {
+        if (cudaMemsetAsync(st->ws + L.split_flags, 0, static_cast<size_t>(L.split_tiles) * zbk::kSplitTileFlagBytes,
+                            s) != cudaSuccess)
+            return ZB_ERR_CUDA;
+        st->split_zeroed = true;
+    }
+    out->flags = reinterpret_cast<uint32_t*>(st->ws + L.split_flags);
+    out->partial = reinterpret_cast<float*>(st->ws + L.split_partial);
+    out->tiles = L.split_tiles;
+    return ZB_OK;
 }
 
 // Algorithmic work of one GEMM launch (every operand read once, every result
@@ -530,10 +662,12 @@ zb_status stage_forward_body(zb_stage* st, int slot, const void* x, int t, void*
     const double T = t;
     ZB_TRY(stash_copy(st, ZB_KCLASS_ROW_FORWARD, st->at(slot, st->lay.layers[0].x), x, static_cast<size_t>(t) * H * 2, s));
     if (t == 0) return ZB_OK;
+    SplitWs ws;
+    ZB_TRY(stage_split_ws(st, s, &ws));
     if (c.kind == ZB_LAYER_LINEAR) {
         const zb_layer_params& p = st->prm[0];
         return traced(st, ZB_KCLASS_GEMM_FORWARD, 1, gemm_flops(T, F, H), fwd_bytes(T, F, H, false), s, [&] {
-            return run_linear_forward(st->at(slot, st->lay.layers[0].x), p.w, nullptr, y, t, H, F, s);
+            return run_linear_forward(st->at(slot, st->lay.layers[0].x), p.w, nullptr, y, t, H, F, s, &ws);
         });
     }
     for (int l = 0; l < c.n_layers; ++l) {
@@ -542,20 +676,31 @@ zb_status stage_forward_body(zb_stage* st, int slot, const void* x, int t, void*
         void* xin = st->at(slot, L.x);
         void* yout = l + 1 < c.n_layers ? st->at(slot, st->lay.layers[l + 1].x) : y;
         if (c.kind == ZB_LAYER_TRANSFORMER) {
-            void* qkv = st->ws + st->lay.qkv_tmp;
+            const bool causal = c.attention == ZB_ATTN_CAUSAL;
+            void* qkv = causal ? st->at(slot, L.qkv) : st->ws + st->lay.qkv_tmp;
             ZB_TRY(traced(st, ZB_KCLASS_ROW_FORWARD, 1, 0.0, 4.0 * T * H + 4.0 * T, s, [&] {
                 return cuda_status(zbk::launch_rmsnorm_forward(xin, p.gamma1, c.eps, st->at(slot, L.n1),
                                                                st->at<float>(slot, L.r1), t, H, s));
             }));
             ZB_TRY(traced(st, ZB_KCLASS_GEMM_FORWARD, 1, gemm_flops(T, Q, H), fwd_bytes(T, Q, H, false), s, [&] {
-                return run_linear_forward(st->at(slot, L.n1), p.w_qkv, nullptr, qkv, t, H, Q, s);
+                return run_linear_forward(st->at(slot, L.n1), p.w_qkv, nullptr, qkv, t, H, Q, s, &ws);
             }));
-            ZB_TRY(traced(st, ZB_KCLASS_ROW_FORWARD, 1, 0.0, 2.0 * T * (Q + H), s, [&] {
-                return cuda_status(zbk::launch_attention_forward(qkv, st->at(slot, L.a), t, c.n_heads,
-                                                                 c.n_kv_heads, c.head_dim, s));
-            }));
+            if (causal) {
+                const double pairs = causal_pairs(t, c.seq_len) * c.n_heads;
+                ZB_TRY(traced(st, ZB_KCLASS_ATTN_FORWARD, 1, 4.0 * c.head_dim * pairs, 2.0 * T * (Q + H) + 4.0 * T * c.n_heads, s,
+                              [&] {
+                                  return cuda_status(zbk::launch_attention_causal_forward(
+                                      attn_shape(t, c.n_heads, c.n_kv_heads, c.head_dim, c.seq_len, st->lay.ld_stat), qkv,
+                                      st->at(slot, L.a), st->at<float>(slot, L.lse), s));
+                              }));
+            } else {
+                ZB_TRY(traced(st, ZB_KCLASS_ROW_FORWARD, 1, 0.0, 2.0 * T * (Q + H), s, [&] {
+                    return cuda_status(zbk::launch_attention_forward(qkv, st->at(slot, L.a), t, c.n_heads,
+                                                                     c.n_kv_heads, c.head_dim, s));
+                }));
+            }
             ZB_TRY(traced(st, ZB_KCLASS_GEMM_FORWARD, 1, gemm_flops(T, H, H), fwd_bytes(T, H, H, true), s, [&] {
-                return run_linear_forward(st->at(slot, L.a), p.w_o, xin, st->at(slot, L.h), t, H, H, s);
+                return run_linear_forward(st->at(slot, L.a), p.w_o, xin, st->at(slot, L.h), t, H, H, s, &ws);
             }));
         }
         void* h = st->at(slot, L.h);
@@ -564,12 +709,12 @@ zb_status stage_forward_body(zb_stage* st, int slot, const void* x, int t, void*
                                                            st->at<float>(slot, L.r2), t, H, s));
         }));
         ZB_TRY(traced(st, ZB_KCLASS_GEMM_FORWARD, 1, gemm_flops(T, 2.0 * F, H), fwd_bytes(T, 2.0 * F, H, false), s,
-                      [&] { return run_linear_forward(st->at(slot, L.n2), p.w_gu, nullptr, st->at(slot, L.gu), t, H, 2 * F, s); }));
+                      [&] { return run_linear_forward(st->at(slot, L.n2), p.w_gu, nullptr, st->at(slot, L.gu), t, H, 2 * F, s, &ws); }));
         ZB_TRY(traced(st, ZB_KCLASS_ROW_FORWARD, 1, 0.0, 6.0 * T * F, s, [&] {
             return cuda_status(zbk::launch_swiglu_forward(st->at(slot, L.gu), st->at(slot, L.s), t, F, s));
         }));
         ZB_TRY(traced(st, ZB_KCLASS_GEMM_FORWARD, 1, gemm_flops(T, H, F), fwd_bytes(T, H, F, true), s, [&] {
-            return run_linear_forward(st->at(slot, L.s), p.w_down, h, yout, t, F, H, s);
+            return run_linear_forward(st->at(slot, L.s), p.w_down, h, yout, t, F, H, s, &ws);
         }));
     }
     return ZB_OK;
@@ -585,9 +730,11 @@ zb_status stage_backward_input_body(zb_stage* st, int slot, const void* dy, void
     const int out_dim = c.kind == ZB_LAYER_LINEAR ? F : H;
     ZB_TRY(stash_copy(st, ZB_KCLASS_ROW_BACKWARD_INPUT, st->at(slot, st->lay.layers[top].dy), dy, static_cast<size_t>(t) * out_dim * 2, s));
     if (t == 0) return ZB_OK;
+    SplitWs ws;
+    ZB_TRY(stage_split_ws(st, s, &ws));
     if (c.kind == ZB_LAYER_LINEAR)
         return traced(st, ZB_KCLASS_GEMM_BACKWARD_INPUT, 1, gemm_flops(T, H, F), dgrad_bytes(T, H, F), s, [&] {
-            return run_backward_input(st->at(slot, st->lay.layers[0].dy), st->prm[0].w, dx, t, H, F, H, s);
+            return run_backward_input(st->at(slot, st->lay.layers[0].dy), st->prm[0].w, dx, t, H, F, H, s, &ws);
         });
     for (int l = top; l >= 0; --l) {
         const zb_layer_params& p = st->prm[l];
@@ -598,11 +745,11 @@ zb_status stage_backward_input_body(zb_stage* st, int slot, const void* dy, void
         void* dn2 = st->at(slot, L.dn2);
         // a1: down projection B with the SwiGLU backward fused; [g|u] becomes [dg|du]
         ZB_TRY(traced(st, ZB_KCLASS_GEMM_BACKWARD_INPUT, 1, gemm_flops(T, F, H), dgrad_swiglu_bytes(T, F, H), s,
-                      [&] { return run_backward_input_swiglu(dyl, p.w_down, gu, gu, t, H, F, s); }));
+                      [&] { return run_backward_input_swiglu(dyl, p.w_down, gu, gu, t, H, F, s, &ws); }));
         // a2: gate|up B, then RMSNorm backward onto the residual gradient
         void* dh = c.kind == ZB_LAYER_TRANSFORMER ? st->at(slot, L.dh) : dx_out;
         ZB_TRY(traced(st, ZB_KCLASS_GEMM_BACKWARD_INPUT, 1, gemm_flops(T, H, 2.0 * F), dgrad_bytes(T, H, 2.0 * F), s,
-                      [&] { return run_backward_input(gu, p.w_gu, dn2, t, H, 2 * F, H, s); }));
+                      [&] { return run_backward_input(gu, p.w_gu, dn2, t, H, 2 * F, H, s, &ws); }));
         ZB_TRY(traced(st, ZB_KCLASS_ROW_BACKWARD_INPUT, 1, 0.0, rms_bwd_bytes(T, H), s, [&] {
             return cuda_status(zbk::launch_rmsnorm_backward_input(dn2, st->at(slot, L.h), st->at<float>(slot, L.r2),
                                                                   p.gamma2, dyl, dh, t, H, s));
@@ -611,15 +758,31 @@ zb_status stage_backward_input_body(zb_stage* st, int slot, const void* dy, void
             void* dqkv = st->at(slot, L.dqkv);
             void* dn1 = st->at(slot, L.dn1);
             const double kv = static_cast<double>(c.n_kv_heads) * c.head_dim;
-            // a3: output projection B (into the q columns of dqkv) and the stand-in backward
-            ZB_TRY(traced(st, ZB_KCLASS_GEMM_BACKWARD_INPUT, 1, gemm_flops(T, H, H), dgrad_bytes(T, H, H), s,
-                          [&] { return run_backward_input(dh, p.w_o, dqkv, t, H, H, Q, s); }));
-            ZB_TRY(traced(st, ZB_KCLASS_ROW_BACKWARD_INPUT, 1, 0.0, 2.0 * T * H + 4.0 * T * kv, s, [&] {
-                return cuda_status(zbk::launch_attention_backward_kv(dqkv, t, c.n_heads, c.n_kv_heads, c.head_dim, s));
-            }));
+            if (c.attention == ZB_ATTN_CAUSAL) {
+                // a3: output projection B into a temporary, then the attention backward
+                // (rowsum, dK/dV, dQ) writes every column of dqkv
+                void* da = st->ws + st->lay.da_tmp;
+                ZB_TRY(traced(st, ZB_KCLASS_GEMM_BACKWARD_INPUT, 1, gemm_flops(T, H, H), dgrad_bytes(T, H, H), s,
+                              [&] { return run_backward_input(dh, p.w_o, da, t, H, H, H, s, &ws); }));
+                const double pairs = causal_pairs(t, c.seq_len) * c.n_heads;
+                ZB_TRY(traced(st, ZB_KCLASS_ATTN_BACKWARD, 3, 10.0 * c.head_dim * pairs,
+                              2.0 * T * (2.0 * Q + 2.0 * H) + 8.0 * T * c.n_heads, s, [&] {
+                                  return cuda_status(zbk::launch_attention_causal_backward(
+                                      attn_shape(t, c.n_heads, c.n_kv_heads, c.head_dim, c.seq_len, st->lay.ld_stat),
+                                      st->at(slot, L.qkv), st->at(slot, L.a), da, st->at<float>(slot, L.lse),
+                                      reinterpret_cast<float*>(st->ws + st->lay.dvec), dqkv, s));
+                              }));
+            } else {
+                // a3: output projection B (into the q columns of dqkv) and the stand-in backward
+                ZB_TRY(traced(st, ZB_KCLASS_GEMM_BACKWARD_INPUT, 1, gemm_flops(T, H, H), dgrad_bytes(T, H, H), s,
+                              [&] { return run_backward_input(dh, p.w_o, dqkv, t, H, H, Q, s, &ws); }));
+                ZB_TRY(traced(st, ZB_KCLASS_ROW_BACKWARD_INPUT, 1, 0.0, 2.0 * T * H + 4.0 * T * kv, s, [&] {
+                    return cuda_status(zbk::launch_attention_backward_kv(dqkv, t, c.n_heads, c.n_kv_heads, c.head_dim, s));
+                }));
+            }
             // a4: qkv B, then RMSNorm backward onto dh
             ZB_TRY(traced(st, ZB_KCLASS_GEMM_BACKWARD_INPUT, 1, gemm_flops(T, H, Q), dgrad_bytes(T, H, Q), s,
-                          [&] { return run_backward_input(dqkv, p.w_qkv, dn1, t, H, Q, H, s); }));
+                          [&] { return run_backward_input(dqkv, p.w_qkv, dn1, t, H, Q, H, s, &ws); }));
             ZB_TRY(traced(st, ZB_KCLASS_ROW_BACKWARD_INPUT, 1, 0.0, rms_bwd_bytes(T, H), s, [&] {
                 return cuda_status(zbk::launch_rmsnorm_backward_input(dn1, st->at(slot, L.x), st->at<float>(slot, L.r1),
                                                                       p.gamma1, dh, dx_out, t, H, s));
@@ -635,9 +798,11 @@ zb_status stage_backward_weight_body(zb_stage* st, int slot, int t, cudaStream_t
     const zb_stage_config& c = st->cfg;
     const int H = c.hidden, F = c.ffn, Q = qkv_width(c);
     const double T = t;
+    SplitWs ws;
+    ZB_TRY(stage_split_ws(st, s, &ws));
     auto wgrad = [&](const void* dyv, const void* xv, float* dw, int in, int out) {
         return traced(st, ZB_KCLASS_GEMM_BACKWARD_WEIGHT, 1, gemm_flops(out, in, T), wgrad_bytes(out, in, T), s,
-                      [&] { return run_backward_weight(dyv, xv, dw, t, in, out, s); });
+                      [&] { return run_backward_weight(dyv, xv, dw, t, in, out, s, &ws); });
     };
     if (c.kind == ZB_LAYER_LINEAR) {
         const LayerSlot& L = st->lay.layers[0];

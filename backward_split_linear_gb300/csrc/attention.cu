@@ -1,0 +1,896 @@
+// Causal softmax attention with grouped K/V heads on tcgen05 (sm_103a).
+//
+// The attention core between the qkv and output projections of a layer:
+//   a_h = softmax(q_h k_j^T / sqrt(d), keys <= query) v_j,  j = h / (n_heads / n_kv_heads),
+// over independent sequences of seq_len consecutive tokens (0: one sequence).
+// The linears around it are the ones whose backward Zero-Bubble splits
+// ("Zero-Bubble Pipeline Parallelism Guide for LLMs", "Core Innovation 1");
+// the core has no weights, so all of its backward belongs to B.
+//
+// Three kernels, each one CTA per 128-row tile, 192 threads:
+//   warp 0     one thread issues TMA loads
+//   warp 1     allocates tensor memory; one thread issues tcgen05.mma
+//   warps 2-5  one row each: softmax / gradient arithmetic, epilogue
+//
+//   attn_causal_fwd_kernel   (head h, query block):  S = Q K^T -> online softmax ->
+//                     O += P V over the key blocks up to the diagonal; writes
+//                     a and the row log-sum-exp (base 2) for the backward.
+//   attn_causal_dkdv_kernel  (kv head j, key block): for every query head of group j
+//                     and every query block from the diagonal on:
+//                     S^T = K Q^T, dP^T = V dO^T, P^T = exp2(S^T c - lse),
+//                     dS^T = P^T (dP^T - D); dV += P^T dO, dK += dS^T Q.
+//   attn_causal_dq_kernel    (head h, query block): S = Q K^T, dP = dO V^T, dS as
+//                     above, dQ += dS K over the key blocks up to the diagonal.
+// dQ has its own kernel (it recomputes S and dP) so that no two CTAs add into
+// the same output: results are the same bits on every run.  D = rowsum(dO * O)
+// comes from a small row kernel first.
+//
+// Tiles are 128 rows x d columns of bf16 in 128-byte-swizzled layout: d / 64
+// blocks of 128 rows x 128 bytes (16 KiB each), as TMA writes them.  A tile
+// serves as a K-major operand (contraction over d) or, through another
+// descriptor, as an MN-major one (contraction over its 128 rows).  P and dS
+// are written from registers in the same layout.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace zbk {
+
+namespace {
+
+constexpr int kAttnThreads = 192;
+constexpr int kRows = 128;             // query and key block
+constexpr uint32_t kPTile = 128 * 256;  // 128 x 128 bf16
+
+struct AttnParams {
+    int tokens;
+    int n_heads, n_kv_heads;
+    int seq_len;    // 0: the whole microbatch is one sequence
+    int n_blocks;   // ceil(tokens / 128)
+    int ld_stat;    // floats per head row of lse / dvec
+    void* out;      // forward: a [T, n_heads d]; backward: dqkv [T, (n_heads + 2 n_kv_heads) d]
+    int64_t ld_out;
+    float* lse;        // [n_heads][ld_stat]: log2 of the softmax denominator, in units of the scaled score
+    const float* dvec;  // [n_heads][ld_stat]: rowsum(dO * O)
+    float scale_log2;   // log2(e) / sqrt(d)
+    float scale;        // 1 / sqrt(d)
+    int* status;
+};
+
+__device__ __forceinline__ void seq_bounds(const AttnParams& p, int t0, int& s0, int& s1) {
+    if (p.seq_len > 0) {
+        s0 = (t0 / p.seq_len) * p.seq_len;
+        s1 = min(p.tokens, s0 + p.seq_len);
+    } else {
+        s0 = 0;
+        s1 = p.tokens;
+    }
+}
+
+// K-major operand from a tile whose rows are the M (or N) index and whose
+// columns are the contraction: step kk covers columns 16 kk .. 16 kk + 15.
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) {
+    return smem_desc_sw128(tile + static_cast<uint32_t>(kk >> 2) * 16384u + static_cast<uint32_t>(kk & 3) * 32u,
+                           16, 1024);
+}
+
+// MN-major operand from the same kind of tile: the contraction runs over its
+// 128 rows (step kk = rows 16 kk .. +15), the MN index over its columns.
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) {
+    return smem_desc_sw128(tile + static_cast<uint32_t>(kk) * 2048u, 16384, 1024);
+}
+
+// Byte offset of element (row, col) in a swizzled tile (col 8-aligned: one 16 B chunk).
+__device__ __forceinline__ uint32_t swz_chunk(int row, int col) {
+    const int block = col >> 6;
+    const int chunk = ((col & 63) >> 3) ^ (row & 7);
+    return static_cast<uint32_t>(block * 16384 + row * 128 + chunk * 16);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// A wait taken by every lane of a warp, with one verdict for the warp (the
+// tensor-memory loads that follow are warp-wide).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* status) {
+    const bool ok = mbar_wait(bar, parity, status, kSiteAttn);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Loads one 128-row tile (d / 64 boxes) of columns col .. col + d - 1 at row r0.
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, int col, int r0) {
+#pragma unroll
+    for (int b = 0; b < D / 64; ++b) tma_load_2d(dst + b * 16384u, map, bar, col + 64 * b, r0);
+}
+
+// ------------------------------------------------------------------------ forward
+
+template <int D>
+struct FwdSmem {
+    static constexpr uint32_t kTile = D * 256;
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kKV = kTile;                 // stage s: K at kKV + 2 s kTile, V after it
+    static constexpr uint32_t kP = kKV + 4 * kTile;
+    static constexpr uint32_t kBars = kP + kPTile;
+    static constexpr size_t kBytes = 1024 + kBars + 16 * 8;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_causal_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const AttnParams p) {
+    using L = FwdSmem<D>;
+    constexpr uint32_t kTile = L::kTile;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t s_q = base + L::kQ, s_kv = base + L::kKV, s_p = base + L::kP;
+    const uint32_t bars = base + L::kBars;
+    const uint32_t q_full = bars;
+    auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bars + 8u * (3 + s); };
+    auto s_full = [&](int s) { return bars + 8u * (5 + s); };
+    auto s_free = [&](int s) { return bars + 8u * (7 + s); };
+    const uint32_t p_full = bars + 8u * 9, p_free = bars + 8u * 10, drain = bars + 8u * 11;
+    const uint32_t tmem_slot = bars + 8u * 12;
+    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qb = p.n_blocks - 1 - static_cast<int>(blockIdx.x) / p.n_heads;  // longest rows first
+    const int h = static_cast<int>(blockIdx.x) % p.n_heads;
+    const int g = h / (p.n_heads / p.n_kv_heads);
+    const int q0 = qb * kRows;
+    int s0, s1;
+    seq_bounds(p, q0, s0, s1);
+    const int kb0 = s0 / kRows;
+    const int nk = qb - kb0 + 1;
+    const int qcol = h * D, kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+            mbar_init(s_full(s), 1);
+            mbar_init(s_free(s), 128);
+        }
+        mbar_init(p_full, 128);
+        mbar_init(p_free, 1);
+        mbar_init(drain, 1);
+        mbar_fence_init();
+        tma_prefetch_map(&map_qkv);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+    const uint32_t t_o = tmem_base + 256;  // columns 0-255: two score buffers; 256..: O
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, kTile);
+            load_tile<D>(s_q, &map_qkv, q_full, qcol, q0);
+            int issued[2] = {0, 0};
+            for (int j = 0; j < nk; ++j) {
+                const int st = j & 1;
+                if (!mbar_wait(kv_empty(st), ((j >> 1) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(kv_full(st), 2 * kTile);
+                const int k0 = (kb0 + j) * kRows;
+                load_tile<D>(s_kv + 2 * st * kTile, &map_qkv, kv_full(st), kcol, k0);
+                load_tile<D>(s_kv + (2 * st + 1) * kTile, &map_qkv, kv_full(st), vcol, k0);
+                ++issued[st];
+            }
+            mbar_wait(q_full, 0, p.status, kSiteDrain);
+            for (int s = 0; s < 2; ++s)
+                if (issued[s] > 0) mbar_wait(kv_full(s), (issued[s] - 1) & 1, p.status, kSiteDrain);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_o = mma_idesc_bf16(128, D, false, true);
+            bool ok = mbar_wait(q_full, 0, p.status, kSiteAttn);
+            for (int j = 0; ok && j <= nk; ++j) {
+                if (j < nk) {
+                    const int st = j & 1;
+                    if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.status, kSiteAttn) ||
+                        !mbar_wait(s_free(st), ((j >> 1) & 1) ^ 1u, p.status, kSiteAttn)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t k_tile = s_kv + 2 * st * kTile;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_bf16(tmem_base + st * 128, kdesc(s_q, kk), kdesc(k_tile, kk), idesc_s, kk > 0);
+                    umma_commit(s_full(st));
+                }
+                if (j > 0) {
+                    const int jj = j - 1, st = jj & 1;
+                    if (!mbar_wait(p_full, jj & 1, p.status, kSiteAttn)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t v_tile = s_kv + (2 * st + 1) * kTile;
+#pragma unroll
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        umma_bf16(t_o, kdesc(s_p, kk), mndesc(v_tile, kk), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(kv_empty(st));
+                    umma_commit(p_free);
+                }
+            }
+            umma_commit(drain);
+            mbar_wait(drain, 0, p.status, kSiteDrain);
+        }
+    } else {
+        // ---------------- softmax rows
+        const int qw = warp & 3;
+        const int row = qw * 32 + lane;
+        const int q = q0 + row;
+        const uint32_t t_row = static_cast<uint32_t>(qw * 32) << 16;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nk && ok; ++j) {
+            const int sb = j & 1;
+            if (!warp_wait(s_full(sb), (j >> 1) & 1, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_load_32(tmem_base + t_row + sb * 128 + 32 * c, r);
+                tmem_wait_load();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(r[e]);
+            }
+            tc_fence_before();
+            mbar_arrive(s_free(sb));
+            const int k0 = (kb0 + j) * kRows;
+            const int lim = min(q - k0, s1 - 1 - k0);  // last visible key column of this row
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                s[c] = c <= lim ? s[c] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[c]);
+            }
+            if (j > 0 && !warp_wait(p_free, (j - 1) & 1, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (j == 0) {
+                m = mx;
+            } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
+                // A row's maximum rose far above its reference: the warp rescales
+                // O and l of all its rows to their new maxima (the tensor-memory
+                // loads and stores are warp-wide, so the decision is the warp's;
+                // rescaling to any larger reference is exact).
+                const float m_new = fmaxf(m, mx);
+                const float alpha = ex2(m - m_new);
+                l *= alpha;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_load_32(t_o + t_row + 32 * c, r);
+                    tmem_wait_load();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    tmem_store_32(t_o + t_row + 32 * c, r);
+                }
+                tmem_wait_store();
+                m = m_new;
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < 16; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = ex2(s[8 * c8 + 2 * e] - m);
+                    const float b = ex2(s[8 * c8 + 2 * e + 1] - m);
+                    sum += a + b;
+                    w[e] = pack_bf16x2(a, b);
+                }
+                st_shared_v4(s_p + swz_chunk(row, 8 * c8), w[0], w[1], w[2], w[3]);
+            }
+            l += sum;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        if (ok && warp_wait(p_free, (nk - 1) & 1, p.status)) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            const bool valid = q < s1;
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(q) * p.ld_out + h * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_load_32(t_o + t_row + 32 * c, r);
+                tmem_wait_load();
+                if (valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        d4[k] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
+                                           pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
+                                           pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
+                                           pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
+                }
+            }
+            if (valid) p.lse[static_cast<int64_t>(h) * p.ld_stat + q] = m + lg2(l);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ------------------------------------------------------------------------ backward: dq
+
+template <int D>
+struct DqSmem {
+    static constexpr uint32_t kTile = D * 256;
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kDO = kTile;
+    static constexpr uint32_t kKV = 2 * kTile;     // stage s: K at kKV + 2 s kTile, V after it
+    static constexpr uint32_t kDS = kKV + 4 * kTile;
+    static constexpr uint32_t kBars = kDS + kPTile;
+    static constexpr size_t kBytes = 1024 + kBars + 16 * 8;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_causal_dq_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
+                   const AttnParams p) {
+    using L = DqSmem<D>;
+    constexpr uint32_t kTile = L::kTile;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t s_q = base + L::kQ, s_do = base + L::kDO, s_kv = base + L::kKV, s_ds = base + L::kDS;
+    const uint32_t bars = base + L::kBars;
+    const uint32_t q_full = bars;
+    auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bars + 8u * (3 + s); };
+    const uint32_t sp_full = bars + 8u * 5, sp_free = bars + 8u * 6, ds_full = bars + 8u * 7,
+                   ds_free = bars + 8u * 8, drain = bars + 8u * 9;
+    const uint32_t tmem_slot = bars + 8u * 10;
+    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qb = p.n_blocks - 1 - static_cast<int>(blockIdx.x) / p.n_heads;
+    const int h = static_cast<int>(blockIdx.x) % p.n_heads;
+    const int g = h / (p.n_heads / p.n_kv_heads);
+    const int q0 = qb * kRows;
+    int s0, s1;
+    seq_bounds(p, q0, s0, s1);
+    const int kb0 = s0 / kRows;
+    const int nk = qb - kb0 + 1;
+    const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        mbar_init(sp_full, 1);
+        mbar_init(sp_free, 128);
+        mbar_init(ds_full, 128);
+        mbar_init(ds_free, 1);
+        mbar_init(drain, 1);
+        mbar_fence_init();
+        tma_prefetch_map(&map_qkv);
+        tma_prefetch_map(&map_do);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+    const uint32_t t_s = tmem_base, t_dp = tmem_base + 128, t_dq = tmem_base + 256;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, 2 * kTile);
+            load_tile<D>(s_q, &map_qkv, q_full, h * D, q0);
+            load_tile<D>(s_do, &map_do, q_full, h * D, q0);
+            int issued[2] = {0, 0};
+            for (int j = 0; j < nk; ++j) {
+                const int st = j & 1;
+                if (!mbar_wait(kv_empty(st), ((j >> 1) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(kv_full(st), 2 * kTile);
+                const int k0 = (kb0 + j) * kRows;
+                load_tile<D>(s_kv + 2 * st * kTile, &map_qkv, kv_full(st), kcol, k0);
+                load_tile<D>(s_kv + (2 * st + 1) * kTile, &map_qkv, kv_full(st), vcol, k0);
+                ++issued[st];
+            }
+            mbar_wait(q_full, 0, p.status, kSiteDrain);
+            for (int s = 0; s < 2; ++s)
+                if (issued[s] > 0) mbar_wait(kv_full(s), (issued[s] - 1) & 1, p.status, kSiteDrain);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_q = mma_idesc_bf16(128, D, false, true);
+            bool ok = mbar_wait(q_full, 0, p.status, kSiteAttn);
+            for (int j = 0; ok && j < nk; ++j) {
+                const int st = j & 1;
+                if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.status, kSiteAttn) ||
+                    !mbar_wait(sp_free, (j & 1) ^ 1u, p.status, kSiteAttn))
+                    break;
+                tc_fence_after();
+                const uint32_t k_tile = s_kv + 2 * st * kTile, v_tile = k_tile + kTile;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(t_s, kdesc(s_q, kk), kdesc(k_tile, kk), idesc_s, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(t_dp, kdesc(s_do, kk), kdesc(v_tile, kk), idesc_s, kk > 0);
+                umma_commit(sp_full);
+                if (!mbar_wait(ds_full, j & 1, p.status, kSiteAttn)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_bf16(t_dq, kdesc(s_ds, kk), mndesc(k_tile, kk), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(kv_empty(st));
+                umma_commit(ds_free);
+            }
+            umma_commit(drain);
+            mbar_wait(drain, 0, p.status, kSiteDrain);
+        }
+    } else {
+        const int qw = warp & 3;
+        const int row = qw * 32 + lane;
+        const int q = q0 + row;
+        const uint32_t t_row = static_cast<uint32_t>(qw * 32) << 16;
+        const bool valid = q < s1;
+        const float lse = valid ? p.lse[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
+        const float dv = valid ? p.dvec[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
+        bool ok = true;
+        for (int j = 0; j < nk; ++j) {
+            if (!warp_wait(sp_full, j & 1, p.status) || !warp_wait(ds_free, (j & 1) ^ 1u, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int k0 = (kb0 + j) * kRows;
+            const int lim = valid ? min(q - k0, s1 - 1 - k0) : -1;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rs[32], rp[32];
+                tmem_load_32(t_s + t_row + 32 * c, rs);
+                tmem_load_32(t_dp + t_row + 32 * c, rp);
+                tmem_wait_load();
+                if (c == 3) {
+                    tc_fence_before();
+                    mbar_arrive(sp_free);
+                }
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float ds2[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int i = 8 * c8 + 2 * e + u;
+                            const int col = 32 * c + i;
+                            const float pr = col <= lim ? ex2(__uint_as_float(rs[i]) * p.scale_log2 - lse) : 0.f;
+                            ds2[u] = pr * (__uint_as_float(rp[i]) - dv);
+                        }
+                        w[e] = pack_bf16x2(ds2[0], ds2[1]);
+                    }
+                    st_shared_v4(s_ds + swz_chunk(row, 32 * c + 8 * c8), w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(ds_full);
+        }
+        if (ok && warp_wait(ds_free, (nk - 1) & 1, p.status)) {
+            tc_fence_after();
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(q) * p.ld_out + h * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_load_32(t_dq + t_row + 32 * c, r);
+                tmem_wait_load();
+                if (valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+                    const float sc = p.scale;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        d4[k] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * k]) * sc, __uint_as_float(r[8 * k + 1]) * sc),
+                                           pack_bf16x2(__uint_as_float(r[8 * k + 2]) * sc, __uint_as_float(r[8 * k + 3]) * sc),
+                                           pack_bf16x2(__uint_as_float(r[8 * k + 4]) * sc, __uint_as_float(r[8 * k + 5]) * sc),
+                                           pack_bf16x2(__uint_as_float(r[8 * k + 6]) * sc, __uint_as_float(r[8 * k + 7]) * sc));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ------------------------------------------------------------------------ backward: dk, dv
+
+template <int D>
+struct DkvSmem {
+    static constexpr uint32_t kTile = D * 256;
+    static constexpr uint32_t kK = 0;
+    static constexpr uint32_t kV = kTile;
+    static constexpr uint32_t kQ = 2 * kTile;
+    static constexpr uint32_t kDO = 3 * kTile;
+    static constexpr uint32_t kPT = 4 * kTile;      // P^T
+    static constexpr uint32_t kDST = kPT + kPTile;  // dS^T
+    static constexpr uint32_t kStat = kDST + kPTile;  // lse and dvec of the 128 queries (1 KiB)
+    static constexpr uint32_t kBars = kStat + 1024;
+    static constexpr size_t kBytes = 1024 + kBars + 16 * 8;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_causal_dkdv_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
+                     const AttnParams p) {
+    using L = DkvSmem<D>;
+    constexpr uint32_t kTile = L::kTile;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t s_k = base + L::kK, s_v = base + L::kV, s_q = base + L::kQ, s_do = base + L::kDO;
+    const uint32_t s_pt = base + L::kPT, s_dst = base + L::kDST, s_stat = base + L::kStat;
+    const float* stat_lse = reinterpret_cast<const float*>(smem_raw + (s_stat - raw));
+    const float* stat_dv = stat_lse + 128;
+    const uint32_t bars = base + L::kBars;
+    const uint32_t kv_full = bars, qd_full = bars + 8, qd_empty = bars + 16, sp_full = bars + 24,
+                   sp_free = bars + 32, pd_full = bars + 40, pd_free = bars + 48, drain = bars + 56;
+    const uint32_t tmem_slot = bars + 64;
+    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = p.n_heads / p.n_kv_heads;
+    const int kb = static_cast<int>(blockIdx.x) / p.n_kv_heads;  // earliest keys (most work) first
+    const int g = static_cast<int>(blockIdx.x) % p.n_kv_heads;
+    const int k0 = kb * kRows;
+    int s0, s1;
+    seq_bounds(p, k0, s0, s1);
+    const int qb_last = (s1 - 1) / kRows;
+    const int n_it = group * (qb_last - kb + 1);  // (query block, head of the group) pairs
+    const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        mbar_init(qd_full, 1);
+        mbar_init(qd_empty, 1);
+        mbar_init(sp_full, 1);
+        mbar_init(sp_free, 128);
+        mbar_init(pd_full, 128);
+        mbar_init(pd_free, 1);
+        mbar_init(drain, 1);
+        mbar_fence_init();
+        tma_prefetch_map(&map_qkv);
+        tma_prefetch_map(&map_do);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+    const uint32_t t_s = tmem_base, t_dp = tmem_base + 128, t_dv = tmem_base + 256, t_dk = tmem_base + 256 + D;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(kv_full, 2 * kTile);
+            load_tile<D>(s_k, &map_qkv, kv_full, kcol, k0);
+            load_tile<D>(s_v, &map_qkv, kv_full, vcol, k0);
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int qb = kb + it / group;
+                const int h = g * group + it % group;
+                if (!mbar_wait(qd_empty, (it & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(qd_full, 2 * kTile + 1024);
+                load_tile<D>(s_q, &map_qkv, qd_full, h * D, qb * kRows);
+                load_tile<D>(s_do, &map_do, qd_full, h * D, qb * kRows);
+                bulk_load_1d(s_stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + qb * kRows, 512, qd_full);
+                bulk_load_1d(s_stat + 512, p.dvec + static_cast<int64_t>(h) * p.ld_stat + qb * kRows, 512, qd_full);
+                ++issued;
+            }
+            mbar_wait(kv_full, 0, p.status, kSiteDrain);
+            if (issued > 0) mbar_wait(qd_full, (issued - 1) & 1, p.status, kSiteDrain);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_g = mma_idesc_bf16(128, D, false, true);
+            bool ok = mbar_wait(kv_full, 0, p.status, kSiteAttn);
+            for (int it = 0; ok && it < n_it; ++it) {
+                if (!mbar_wait(qd_full, it & 1, p.status, kSiteAttn) ||
+                    !mbar_wait(sp_free, (it & 1) ^ 1u, p.status, kSiteAttn))
+                    break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(t_s, kdesc(s_k, kk), kdesc(s_q, kk), idesc_s, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(t_dp, kdesc(s_v, kk), kdesc(s_do, kk), idesc_s, kk > 0);
+                umma_commit(sp_full);
+                if (!mbar_wait(pd_full, it & 1, p.status, kSiteAttn)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_bf16(t_dv, kdesc(s_pt, kk), mndesc(s_do, kk), idesc_g, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_bf16(t_dk, kdesc(s_dst, kk), mndesc(s_q, kk), idesc_g, (it > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(qd_empty);
+                umma_commit(pd_free);
+            }
+            umma_commit(drain);
+            mbar_wait(drain, 0, p.status, kSiteDrain);
+        }
+    } else {
+        // ---------------- one key row per thread
+        const int qw = warp & 3;
+        const int row = qw * 32 + lane;
+        const int k = k0 + row;
+        const uint32_t t_row = static_cast<uint32_t>(qw * 32) << 16;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int q0 = (kb + it / group) * kRows;
+            if (!warp_wait(qd_full, it & 1, p.status) || !warp_wait(sp_full, it & 1, p.status) ||
+                !warp_wait(pd_free, (it & 1) ^ 1u, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // query column c is visible to this key when k <= q0 + c < s1
+            const int first = k - q0;
+            const int last = s1 - 1 - q0;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rs[32], rp[32];
+                tmem_load_32(t_s + t_row + 32 * c, rs);
+                tmem_load_32(t_dp + t_row + 32 * c, rp);
+                tmem_wait_load();
+                if (c == 3) {
+                    tc_fence_before();
+                    mbar_arrive(sp_free);
+                }
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t wp[4], wd[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float pv[2], dsv[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int i = 8 * c8 + 2 * e + u;
+                            const int col = 32 * c + i;
+                            const bool vis = col >= first && col <= last;
+                            // statistics past the sequence end are not written: never read them into a value
+                            const float pr = vis ? ex2(__uint_as_float(rs[i]) * p.scale_log2 - stat_lse[col]) : 0.f;
+                            pv[u] = pr;
+                            dsv[u] = vis ? pr * (__uint_as_float(rp[i]) - stat_dv[col]) : 0.f;
+                        }
+                        wp[e] = pack_bf16x2(pv[0], pv[1]);
+                        wd[e] = pack_bf16x2(dsv[0], dsv[1]);
+                    }
+                    const uint32_t off = swz_chunk(row, 32 * c + 8 * c8);
+                    st_shared_v4(s_pt + off, wp[0], wp[1], wp[2], wp[3]);
+                    st_shared_v4(s_dst + off, wd[0], wd[1], wd[2], wd[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(pd_full);
+        }
+        if (ok && n_it > 0 && warp_wait(pd_free, (n_it - 1) & 1, p.status)) {
+            tc_fence_after();
+            const bool valid = k < s1;
+            uint16_t* dk_dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(k) * p.ld_out + kcol;
+            uint16_t* dv_dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(k) * p.ld_out + vcol;
+#pragma unroll 1
+            for (int pass = 0; pass < 2; ++pass) {
+                const uint32_t t_acc = pass == 0 ? t_dk : t_dv;
+                uint16_t* dst = pass == 0 ? dk_dst : dv_dst;
+                const float sc = pass == 0 ? p.scale : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_load_32(t_acc + t_row + 32 * c, r);
+                    tmem_wait_load();
+                    if (valid) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]) * sc, __uint_as_float(r[8 * q + 1]) * sc),
+                                               pack_bf16x2(__uint_as_float(r[8 * q + 2]) * sc, __uint_as_float(r[8 * q + 3]) * sc),
+                                               pack_bf16x2(__uint_as_float(r[8 * q + 4]) * sc, __uint_as_float(r[8 * q + 5]) * sc),
+                                               pack_bf16x2(__uint_as_float(r[8 * q + 6]) * sc, __uint_as_float(r[8 * q + 7]) * sc));
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ------------------------------------------------------------------------ D = rowsum(dO * O)
+
+// One warp per (token, head): dvec[h][t] = sum_c da[t, h d + c] * a[t, h d + c].
+__global__ void attn_causal_rowsum_kernel(const uint16_t* __restrict__ da, const uint16_t* __restrict__ a, float* dvec,
+                                 int tokens, int n_heads, int head_dim, int ld_stat) {
+    const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= static_cast<int64_t>(tokens) * n_heads) return;
+    const int t = static_cast<int>(wid / n_heads), h = static_cast<int>(wid % n_heads);
+    const int64_t off = static_cast<int64_t>(t) * n_heads * head_dim + static_cast<int64_t>(h) * head_dim;
+    float acc = 0.f;
+    for (int c = 4 * lane; c < head_dim; c += 128) {
+        const uint2 x = *reinterpret_cast<const uint2*>(da + off + c);
+        const uint2 y = *reinterpret_cast<const uint2*>(a + off + c);
+        acc += bf16_lo(x.x) * bf16_lo(y.x) + bf16_hi(x.x) * bf16_hi(y.x) + bf16_lo(x.y) * bf16_lo(y.y) +
+               bf16_hi(x.y) * bf16_hi(y.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) dvec[static_cast<int64_t>(h) * ld_stat + t] = acc;
+}
+
+// ------------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// [rows, cols] bf16, row stride ld elements; boxes of 64 columns x 128 rows, 128B swizzle.
+bool attn_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld) {
+    auto fn = attn_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, size_t bytes) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+AttnParams make_params(const AttnShape& s) {
+    AttnParams p{};
+    p.tokens = s.tokens;
+    p.n_heads = s.n_heads;
+    p.n_kv_heads = s.n_kv_heads;
+    p.seq_len = s.seq_len;
+    p.n_blocks = (s.tokens + kRows - 1) / kRows;
+    p.ld_stat = s.ld_stat;
+    p.scale = 1.0f / sqrtf(static_cast<float>(s.head_dim));
+    p.scale_log2 = 1.4426950408889634f * p.scale;
+    p.status = status_word();
+    return p;
+}
+
+template <int D>
+cudaError_t fwd_launch(const AttnShape& s, const void* qkv, void* a, float* lse, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] { err = set_smem(attn_causal_fwd_kernel<D>, FwdSmem<D>::kBytes); });
+    if (err != cudaSuccess) return err;
+    const int qkv_w = (s.n_heads + 2 * s.n_kv_heads) * D;
+    CUtensorMap m;
+    if (!attn_map(&m, qkv, s.tokens, qkv_w, qkv_w)) return cudaErrorInvalidValue;
+    AttnParams p = make_params(s);
+    if (!p.status) return cudaErrorInvalidDevice;
+    p.out = a;
+    p.ld_out = static_cast<int64_t>(s.n_heads) * D;
+    p.lse = lse;
+    attn_causal_fwd_kernel<D><<<p.n_blocks * s.n_heads, kAttnThreads, FwdSmem<D>::kBytes, stream>>>(m, p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const void* da, const float* lse,
+                       float* dvec, void* dqkv, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = set_smem(attn_causal_dq_kernel<D>, DqSmem<D>::kBytes);
+        if (err == cudaSuccess) err = set_smem(attn_causal_dkdv_kernel<D>, DkvSmem<D>::kBytes);
+    });
+    if (err != cudaSuccess) return err;
+    const int qkv_w = (s.n_heads + 2 * s.n_kv_heads) * D;
+    const int hw = s.n_heads * D;
+    CUtensorMap mq, md;
+    if (!attn_map(&mq, qkv, s.tokens, qkv_w, qkv_w) || !attn_map(&md, da, s.tokens, hw, hw))
+        return cudaErrorInvalidValue;
+    AttnParams p = make_params(s);
+    if (!p.status) return cudaErrorInvalidDevice;
+    p.out = dqkv;
+    p.ld_out = qkv_w;
+    p.lse = const_cast<float*>(lse);
+    p.dvec = dvec;
+    const int64_t warps = static_cast<int64_t>(s.tokens) * s.n_heads;
+    attn_causal_rowsum_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(da), static_cast<const uint16_t*>(a), dvec, s.tokens, s.n_heads, D, s.ld_stat);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    attn_causal_dkdv_kernel<D><<<p.n_blocks * s.n_kv_heads, kAttnThreads, DkvSmem<D>::kBytes, stream>>>(mq, md, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    attn_causal_dq_kernel<D><<<p.n_blocks * s.n_heads, kAttnThreads, DqSmem<D>::kBytes, stream>>>(mq, md, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention_causal_forward(const AttnShape& s, const void* qkv, void* a, float* lse,
+                                            cudaStream_t stream) {
+    if (s.tokens <= 0) return cudaSuccess;
+    if (s.head_dim == 128) return fwd_launch<128>(s, qkv, a, lse, stream);
+    if (s.head_dim == 64) return fwd_launch<64>(s, qkv, a, lse, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention_causal_backward(const AttnShape& s, const void* qkv, const void* a, const void* da,
+                                             const float* lse, float* dvec, void* dqkv, cudaStream_t stream) {
+    if (s.tokens <= 0) return cudaSuccess;
+    if (s.head_dim == 128) return bwd_launch<128>(s, qkv, a, da, lse, dvec, dqkv, stream);
+    if (s.head_dim == 64) return bwd_launch<64>(s, qkv, a, da, lse, dvec, dqkv, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace zbk

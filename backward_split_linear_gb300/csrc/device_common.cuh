@@ -22,6 +22,8 @@ enum WaitSite : int {
     kSiteEpiTmemFull = 4,    // epilogue waiting for a finished accumulator
     kSiteDrain = 5,          // teardown waiting for copies / MMAs in flight
     kSitePairTmem = 6,       // the two CTAs of a pair got different tensor-memory addresses
+    kSiteSplitFlag = 7,      // K-split epilogue waiting for the other half's partial tile
+    kSiteAttn = 8,           // attention kernels (any of their pipeline waits)
     kSiteSelftest = 9,       // zb_selftest_wait_timeout
 };
 
@@ -108,6 +110,44 @@ static __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t par
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (try_once()) return true;
+        if (*reinterpret_cast<volatile int*>(status) != 0) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicCAS(status, 0, site);
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- global flags
+
+// Exchange with acquire-release semantics at GPU scope: the caller sees every
+// write that the thread which stored the old value made before storing it.
+__device__ __forceinline__ uint32_t atom_exch_acq_rel(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Store that publishes every earlier write of this thread at GPU scope.
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until *p == v, with the same limits as mbar_wait.
+static __device__ __noinline__ bool wait_value(const uint32_t* p, uint32_t v, int* status, int site,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+    if (ld_acquire(p) == v) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ld_acquire(p) == v) return true;
         if (*reinterpret_cast<volatile int*>(status) != 0) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             atomicCAS(status, 0, site);
@@ -270,6 +310,39 @@ __device__ __forceinline__ void tmem_load_32(uint32_t taddr, uint32_t (&r)[32]) 
 
 __device__ __forceinline__ void tmem_wait_load() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers into tensor memory
+// (the inverse of tmem_load_32).
+__device__ __forceinline__ void tmem_store_32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_store() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Makes this thread's ordinary shared-memory writes visible to the async proxy
+// (tensor-core MMAs and TMA reading shared memory).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 1D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
 }
 
 // Shared-memory matrix descriptor for tcgen05.mma with 128-byte swizzling.

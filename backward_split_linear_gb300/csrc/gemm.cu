@@ -26,6 +26,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -76,7 +77,37 @@ struct KParams {
     // 64-element MN blocks, the stride-dimension offset between 8-row K groups.
     uint32_t mn_lbo;
     uint32_t mn_sbo;
+    // K split (CTA-pair kernel only): split == 2 makes two work units per tile,
+    // unit 2t + h covering k-blocks [0, kb_split) for h = 0 and
+    // [kb_split, k_blocks) for h = 1; split == 1 is one unit per tile.
+    int split;
+    int kb_split;
+    int num_units;
+    uint32_t* flags;   // one word per 32 rows of a tile: 2 epoch (claimed), 2 epoch + 1 (partial written)
+    float* partial;    // one float32 256 x 256 tile per output tile
+    uint32_t epoch;
 };
+
+struct Unit {
+    int tile, half, kb0, kb1;
+};
+
+template <bool SPLIT>
+__device__ __forceinline__ Unit unit_of(const KParams& p, int u) {
+    Unit w;
+    if (SPLIT) {
+        w.tile = u >> 1;
+        w.half = u & 1;
+        w.kb0 = w.half ? p.kb_split : 0;
+        w.kb1 = w.half ? p.k_blocks : p.kb_split;
+    } else {
+        w.tile = u;
+        w.half = 0;
+        w.kb0 = 0;
+        w.kb1 = p.k_blocks;
+    }
+    return w;
+}
 
 // Tile index -> (tile row, tile column) under the grouped raster.
 __device__ __forceinline__ void tile_coords(const KParams& p, int tile, int& tm, int& tn) {
@@ -308,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
             const uint32_t aph = (static_cast<uint32_t>(it) >> 1) & 1u;
-            if (!mbar_wait(tfull_bar(acc), aph, p.status, kSiteEpiTmemFull)) break;
+            // one verdict per warp: the tensor-memory loads below are warp-wide
+            if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, p.status, kSiteEpiTmemFull))) break;
             tc_fence_after();
             int tm, tn;
             tile_coords(p, tile, tm, tn);
@@ -384,7 +416,7 @@ constexpr int kPairNumBars = 2 * kPairStages + 5;
 constexpr size_t kPairSmemBytes = 1024 + kPairStages * kPairStage + kPairNumBars * 8 + 16;
 static_assert(kPairSmemBytes <= 232448, "shared memory");
 
-template <bool A_MN, bool B_MN, int EPI, int NACC>
+template <bool A_MN, bool B_MN, int EPI, int NACC, bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const KParams p) {
@@ -442,12 +474,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+            for (int u = pair; ok && u < p.num_units; u += npairs) {
+                const Unit w = unit_of<SPLIT>(p, u);
                 int tm, tn;
-                tile_coords(p, tile, tm, tn);
+                tile_coords(p, w.tile, tm, tn);
                 const int m0 = tm * kPairM + static_cast<int>(rank) * kHalf;
                 const int n0 = tn * kPairN + static_cast<int>(rank) * kHalf;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -497,13 +530,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < p.num_tiles; tile += npairs, ++it) {
+            for (int u = pair; ok && u < p.num_units; u += npairs, ++it) {
+                const Unit w = unit_of<SPLIT>(p, u);
                 const int acc = it % NACC;
                 const uint32_t aph = static_cast<uint32_t>(it / NACC) & 1u;
                 if (!mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, p.status, kSiteMmaTmemEmpty)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait_cluster(full_bar(stage), phase, p.status, kSiteMmaFull)) {
                         ok = false;
                         break;
@@ -517,7 +551,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                  : smem_desc_sw128(a0 + k * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, p.mn_lbo, p.mn_sbo)
                                                  : smem_desc_sw128(b0 + k * 32, 16, 1024);
-                        umma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        umma_bf16_pair(d, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
                     }
                     umma_commit_pair(empty_bar(stage), 0x3);
                     if (++stage == kPairStages) {
@@ -536,22 +570,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int row = q * 32 + lane;
         int it = 0;
-        for (int tile = pair; tile < p.num_tiles; tile += npairs, ++it) {
+        for (int u = pair; u < p.num_units; u += npairs, ++it) {
+            const Unit w = unit_of<SPLIT>(p, u);
             const int acc = it % NACC;
             const uint32_t aph = static_cast<uint32_t>(it / NACC) & 1u;
-            if (!mbar_wait_cluster(tfull_bar(acc), aph, p.status, kSiteEpiTmemFull)) break;
+            // one verdict per warp: the tensor-memory loads below are warp-wide
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(tfull_bar(acc), aph, p.status, kSiteEpiTmemFull)))
+                break;
             tc_fence_after();
             int tm, tn;
-            tile_coords(p, tile, tm, tn);
-            const int m = tm * kPairM + static_cast<int>(rank) * kHalf + row;
+            tile_coords(p, w.tile, tm, tn);
+            const int trow = static_cast<int>(rank) * kHalf + row;  // row inside the 256-row tile
+            const int m = tm * kPairM + trow;
             const int n_base = tn * kPairN;
             const bool row_ok = m < p.m;
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kPairN);
+            // K split: per warp (32 rows of the tile), the half whose
+            // accumulator is ready first stores it as float32 partial rows and
+            // marks them written; the other half adds them to its own and runs
+            // the epilogue.  Which half is first does not change the result
+            // (p0 + p1 == p1 + p0).  The decision is taken once per warp, by
+            // lane 0, because the tensor-memory loads below are warp-wide; the
+            // second half waits only on a warp that is already past its MMAs
+            // and has no waits left before it marks the rows.
+            bool store_partial = false;
+            bool give_up = false;
+            uint32_t* flag = nullptr;
+            const float* prow =
+                SPLIT ? p.partial + (static_cast<size_t>(w.tile) * kPairM + static_cast<size_t>(trow)) * kPairN
+                      : nullptr;
+            if constexpr (SPLIT) {
+                flag = p.flags + static_cast<size_t>(w.tile) * 8 + rank * 4 + static_cast<uint32_t>(q);
+                const uint32_t claimed = 2u * p.epoch;
+                uint32_t old = 0;
+                if (lane == 0) old = atom_exch_acq_rel(flag, claimed);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                store_partial = old != claimed && old != claimed + 1u;
+                if (old == claimed) {
+                    int ready = 1;
+                    if (lane == 0) ready = wait_value(flag, claimed + 1u, p.status, kSiteSplitFlag) ? 1 : 0;
+                    give_up = __shfl_sync(0xffffffffu, ready, 0) == 0;
+                }
+                __syncwarp();  // the partial rows read below come after lane 0's acquire
+            }
+            const bool run_epi = row_ok && !store_partial && !give_up;
 #pragma unroll 1
             for (int c = 0; c < kPairN / 32; ++c) {
                 const int n = n_base + c * 32;
-                const bool ok = row_ok && n < p.n;
+                const bool ok = run_epi && n < p.n;
                 uint4 x0[4], x1[4];
                 if constexpr (EPI == static_cast<int>(Epilogue::AddResidual) ||
                               EPI == static_cast<int>(Epilogue::SwigluBwd)) {
@@ -578,7 +645,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     else
                         mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
                 }
-                if (ok) epilogue_chunk<EPI>(p, m, n, r, x0, x1);
+                if (SPLIT && store_partial) {
+                    float4* dst = reinterpret_cast<float4*>(const_cast<float*>(prow) + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                             __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                } else if (ok) {
+                    if constexpr (SPLIT) {
+                        const float4* src = reinterpret_cast<const float4*>(prow + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 v = src[j];
+                            r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
+                            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
+                            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
+                            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                        }
+                    }
+                    epilogue_chunk<EPI>(p, m, n, r, x0, x1);
+                }
+            }
+            if (SPLIT && store_partial) {
+                __syncwarp();  // every lane's partial rows before lane 0's release
+                if (lane == 0) {
+                    __threadfence();
+                    st_release(flag, 2u * p.epoch + 1u);
+                }
             }
         }
     }
@@ -643,10 +736,10 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const K
 // kernel checks this and reports kSitePairTmem otherwise).
 constexpr int kPairAccums = 2;
 
-template <bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_pair_variant(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& p,
-                                cudaStream_t stream) {
-    auto kern = gemm_pair_kernel<A_MN, B_MN, EPI, kPairAccums>;
+template <bool A_MN, bool B_MN, int EPI, bool SPLIT>
+cudaError_t launch_pair_split_variant(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& p,
+                                      cudaStream_t stream) {
+    auto kern = gemm_pair_kernel<A_MN, B_MN, EPI, kPairAccums, SPLIT>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
@@ -662,9 +755,16 @@ cudaError_t launch_pair_variant(const CUtensorMap& ma, const CUtensorMap& mb, co
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-    const int pairs = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+    const int pairs = p.num_units < max_clusters ? p.num_units : max_clusters;
     kern<<<2 * pairs, kThreads, kPairSmemBytes, stream>>>(ma, mb, p);
     return cudaGetLastError();
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_pair_variant(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& p,
+                                cudaStream_t stream) {
+    return p.split == 2 ? launch_pair_split_variant<A_MN, B_MN, EPI, true>(ma, mb, p, stream)
+                        : launch_pair_split_variant<A_MN, B_MN, EPI, false>(ma, mb, p, stream);
 }
 
 // DRAM bytes a raster fetches, modelled wave by wave: a wave reads the A
@@ -793,6 +893,40 @@ cudaError_t dispatch_pair(const GemmArgs& g, const CUtensorMap& ma, const CUtens
     return cudaErrorInvalidValue;
 }
 
+// Clusters of the CTA-pair kernel that fit on the current device at once (the
+// same for every variant: same threads, shared memory and cluster shape).
+int pair_max_clusters() {
+    static int counts[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!counts[dev]) {
+        auto kern = gemm_pair_kernel<false, true, static_cast<int>(Epilogue::StoreBf16), kPairAccums, false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kPairSmemBytes)) != cudaSuccess)
+            return 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(sm_count()));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kPairSmemBytes;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+// Share of the launch's worker slots (waves x workers) that do work.
+double fill(int units, int workers) {
+    const int waves = (units + workers - 1) / workers;
+    return static_cast<double>(units) / (static_cast<double>(waves) * workers);
+}
+
+// Each K-split launch tags the flags it writes with a new epoch, so the flags
+// never need clearing between launches.
+std::atomic<uint32_t> g_split_epoch{0};
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
@@ -825,7 +959,28 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     p.tiles_n = (g.n + tile_n - 1) / tile_n;
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_blocks = (g.k + BK - 1) / BK;
-    const int waves_of = pair ? sms / 2 : sms;
+    p.split = 1;
+    p.kb_split = p.k_blocks;
+    p.num_units = p.num_tiles;
+    // Split K in two when that fills the last wave markedly better and each
+    // half keeps at least 128 k-blocks (K >= 16384); only with caller scratch
+    // for the tiles.  On GB300 a split of shorter contractions lost more to
+    // the extra partial-tile traffic and the shorter pipelines than the fuller
+    // last wave won: 4096 x 4096 outputs with K = 4096 ran at 1071 TFLOP/s
+    // split against 1279 unsplit, while K = 28672 went from 1477 to 1587.
+    if (pair && g.split_flags && g.split_partial && p.k_blocks >= 256 && p.num_tiles <= g.split_tiles &&
+        p.num_tiles <= kSplitMaxTiles) {
+        const int pairs = pair_max_clusters();
+        if (pairs > 0 && fill(2 * p.num_tiles, pairs) > 1.08 * fill(p.num_tiles, pairs)) {
+            p.split = 2;
+            p.kb_split = p.k_blocks / 2;
+            p.num_units = 2 * p.num_tiles;
+            p.flags = g.split_flags;
+            p.partial = g.split_partial;
+            p.epoch = ++g_split_epoch;
+        }
+    }
+    const int waves_of = pair ? sms / 2 / p.split : sms;
     const Raster r = choose_raster(p.tiles_m, p.tiles_n, tile_m, tile_n, g.k, std::min(p.num_tiles, waves_of));
     p.group = r.group;
     p.group_m = r.group_m ? 1 : 0;

@@ -35,7 +35,25 @@ struct GemmArgs {
     const void* aux;   // residual or [g | u]
     int64_t ld_aux;
     int ffn;           // SwigluBwd: column offset of u in aux and of du in out
+    // Optional K-split scratch.  A CTA-pair launch whose last wave of tiles
+    // would leave many SMs idle may cut K in two halves computed by different
+    // CTA pairs; the half that finishes second adds the other's float32
+    // partial tile.  `split_flags` holds kSplitTileFlagBytes per tile and must
+    // be zeroed once before its first use (it is never reset: each launch
+    // tags its flags with a new epoch); `split_partial` holds
+    // kSplitTilePartialBytes per tile.  Launches whose tiles do not fit in
+    // `split_tiles` do not split.  Launches sharing the scratch must not overlap.
+    uint32_t* split_flags;
+    float* split_partial;
+    int split_tiles;
 };
+
+constexpr size_t kSplitTileFlagBytes = 8 * 4;            // one word per 32 rows of a 256 x 256 tile
+constexpr size_t kSplitTilePartialBytes = 256 * 256 * 4;  // one float32 tile
+// Launches of more tiles never split: scratch for 512 tiles is 128 MiB, and at
+// 76 CTA pairs such launches run seven waves or more, so their last wave
+// costs little.
+constexpr int kSplitMaxTiles = 512;
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
 
@@ -70,6 +88,20 @@ cudaError_t launch_attention_forward(const void* qkv, void* a, int tokens, int n
 cudaError_t launch_attention_backward_kv(void* dqkv, int tokens, int n_heads, int n_kv_heads,
                                          int head_dim, cudaStream_t stream);
 cudaError_t launch_selftest_wait(int limit_us, cudaStream_t stream);
+
+// Causal softmax attention with grouped K/V heads (attention.cu).  qkv is
+// [tokens, (n_heads + 2 n_kv_heads) head_dim] bf16 (q heads, then k, then v),
+// a and da are [tokens, n_heads head_dim] bf16, lse and dvec are float32
+// [n_heads][ld_stat] with ld_stat a multiple of 128 and >= tokens rounded up
+// to 128.  head_dim is 64 or 128; seq_len is 0 or a multiple of 128.
+struct AttnShape {
+    int tokens, n_heads, n_kv_heads, head_dim, seq_len, ld_stat;
+};
+cudaError_t launch_attention_causal_forward(const AttnShape& s, const void* qkv, void* a, float* lse,
+                                            cudaStream_t stream);
+// Writes all of dqkv (dq, dk, dv); dvec is scratch of the lse's shape.
+cudaError_t launch_attention_causal_backward(const AttnShape& s, const void* qkv, const void* a, const void* da,
+                                             const float* lse, float* dvec, void* dqkv, cudaStream_t stream);
 
 // Device status word of the current device (see zb_device_status).
 int* status_word();

@@ -16,6 +16,13 @@
 // s; every stage then works without idle from its first op to its last when
 // m >= 2p - 1.  Emitted by a step-by-step run of the policy.
 //
+// Memory-limited orders ("Zero Bubble Pipeline Parallelism", abstract: a
+// search for the best schedule under a memory limit; the guide: ZB-H1 holds
+// p microbatches, ZB-2p 2p): the same policy with a ceiling L in [p, 2p] and
+// min(L - s, 2(p - s) - 1) forwards before the first B of stage s, run with
+// measured op durations; zb_schedule_search takes the L within the memory
+// limit whose run ends first.
+//
 // ZB-H1, m >= p, in closed form for stage s:
 //   F_0 .. F_{p-s-1}
 //   B_j, F_{p-s+j}            for j = 0 .. s-1
@@ -154,6 +161,84 @@ std::vector<std::vector<Op>> zb_policy_all(int p, int m, int limit, bool two_p) 
     return out;
 }
 
+// The same policy with op durations t_f, t_b, t_w: stages decide whenever
+// they are free, all on the state at that moment; time then jumps to the next
+// end of an op.  warm[s] forwards precede stage s's first B.  Returns false
+// (and leaves `out` incomplete) if the run cannot go on.
+bool zb_policy_timed(int p, int m, int limit, const std::vector<int>& warm, long long t_f, long long t_b,
+                     long long t_w, std::vector<std::vector<Op>>& out, long long* span) {
+    std::vector<std::vector<Op>> fb(p);
+    out.assign(p, {});
+    for (int s = 0; s < p; ++s) fb_order(warm[s], m, fb[s]);
+    std::vector<long long> fin_f(static_cast<size_t>(p) * m, -1), fin_b(static_cast<size_t>(p) * m, -1);
+    std::vector<size_t> ptr(p, 0);
+    std::vector<int> held(p, 0);
+    std::vector<long long> busy(p, 0);
+    std::vector<std::vector<int>> pending(p);
+    long long done = 0, t = 0, end = 0;
+    const long long total = 3LL * m * p;
+    std::vector<Op> choice(p);
+    while (done < total) {
+        for (int s = 0; s < p; ++s) {
+            choice[s] = Op{0, -1};
+            if (busy[s] > t) continue;
+            if (ptr[s] < fb[s].size()) {
+                const Op nx = fb[s][ptr[s]];
+                bool ready;
+                if (nx.kind == 'F') {
+                    const long long d = s == 0 ? 0 : fin_f[static_cast<size_t>(s - 1) * m + nx.mb];
+                    ready = d >= 0 && d <= t;
+                } else {
+                    const long long f = fin_f[static_cast<size_t>(s) * m + nx.mb];
+                    const long long b = s == p - 1 ? 0 : fin_b[static_cast<size_t>(s + 1) * m + nx.mb];
+                    ready = f >= 0 && f <= t && b >= 0 && b <= t;
+                }
+                if (ready) {
+                    if (nx.kind == 'F' && held[s] >= limit) {
+                        if (!pending[s].empty()) choice[s] = {'W', pending[s].front()};
+                    } else {
+                        choice[s] = nx;
+                    }
+                } else if (!pending[s].empty()) {
+                    choice[s] = {'W', pending[s].front()};
+                }
+            } else if (!pending[s].empty()) {
+                choice[s] = {'W', pending[s].front()};
+            }
+        }
+        for (int s = 0; s < p; ++s) {
+            const Op op = choice[s];
+            if (op.mb < 0) continue;
+            const long long d = op.kind == 'F' ? t_f : (op.kind == 'B' ? t_b : t_w);
+            busy[s] = t + d;
+            end = std::max(end, t + d);
+            out[s].push_back(op);
+            ++done;
+            if (op.kind == 'W') {
+                pending[s].erase(pending[s].begin());
+                --held[s];
+            } else {
+                ++ptr[s];
+                if (op.kind == 'F') {
+                    fin_f[static_cast<size_t>(s) * m + op.mb] = t + d;
+                    ++held[s];
+                } else {
+                    fin_b[static_cast<size_t>(s) * m + op.mb] = t + d;
+                    pending[s].push_back(op.mb);
+                }
+            }
+        }
+        if (done == total) break;
+        long long next = -1;
+        for (int s = 0; s < p; ++s)
+            if (busy[s] > t && (next < 0 || busy[s] < next)) next = busy[s];
+        if (next < 0) return false;
+        t = next;
+    }
+    *span = end;
+    return true;
+}
+
 void stage_order(zb_sched_kind kind, int s, int p, int m, std::vector<Op>& o) {
     if (kind == ZB_SCHED_GPIPE) {
         order_gpipe(s, p, m, o);
@@ -280,5 +365,40 @@ extern "C" zb_status zb_schedule_bubble(zb_sched_kind kind, int32_t p, int32_t m
     if (makespan) *makespan = span;
     if (idle_over_compute) *idle_over_compute = idle / compute;
     if (idle_over_wall) *idle_over_wall = idle / (static_cast<double>(p) * span);
+    return ZB_OK;
+}
+
+extern "C" zb_status zb_schedule_search(int32_t stage, int32_t p, int32_t m, int32_t mem_limit, int32_t t_f,
+                                        int32_t t_b, int32_t t_w, zb_op* out, int32_t cap, int32_t* n_out,
+                                        int32_t* chosen_limit, int64_t* makespan) {
+    if (p < 1 || m < 1 || stage < 0 || stage >= p || !n_out || (cap > 0 && !out) || cap < 0 || mem_limit < p ||
+        t_f < 1 || t_b < 1 || t_w < 1 || static_cast<long long>(p) * m > (1LL << 20))
+        return ZB_ERR_ARG;
+    *n_out = 3 * m;
+    if (cap < 3 * m) return ZB_ERR_CAPACITY;
+    int best_limit = -1;
+    long long best_span = -1;
+    std::vector<std::vector<Op>> best, cur;
+    const int top = std::min(2 * p, mem_limit);
+    for (int limit = p; limit <= top; ++limit) {
+        std::vector<int> warm(p);
+        for (int s = 0; s < p; ++s) warm[s] = std::min(limit - s, 2 * (p - s) - 1);
+        long long span = 0;
+        if (!zb_policy_timed(p, m, limit, warm, t_f, t_b, t_w, cur, &span)) return ZB_ERR_ORDER;
+        if (best_limit < 0 || span < best_span) {
+            best_limit = limit;
+            best_span = span;
+            best.swap(cur);
+        }
+    }
+    const std::vector<Op>& o = best[stage];
+    if (o.size() != static_cast<size_t>(3 * m)) return ZB_ERR_ORDER;
+    for (int i = 0; i < 3 * m; ++i) {
+        out[i].kind = static_cast<uint8_t>(o[i].kind);
+        out[i].pad[0] = out[i].pad[1] = out[i].pad[2] = 0;
+        out[i].mb = o[i].mb;
+    }
+    if (chosen_limit) *chosen_limit = best_limit;
+    if (makespan) *makespan = best_span;
     return ZB_OK;
 }

@@ -33,12 +33,12 @@ class Stage:
     """One pipeline stage on the current CUDA device."""
 
     def __init__(self, kind, n_layers, hidden, ffn, n_heads=0, n_kv_heads=0, head_dim=0, eps=1e-5,
-                 max_tokens=128, max_inflight=1, params=None, device="cuda"):
+                 max_tokens=128, max_inflight=1, params=None, device="cuda", attention="standin", seq_len=0):
         self.kind = kind
         self.hidden, self.ffn = hidden, ffn
         self.out_dim = ffn if kind == "linear" else hidden
         self.cfg = zb.make_config(kind, n_layers, hidden, ffn, n_heads, n_kv_heads, head_dim, eps,
-                                  max_tokens, max_inflight)
+                                  max_tokens, max_inflight, attention, seq_len)
         nbytes = zb.zb_stage_workspace_bytes(self.cfg)
         if nbytes == 0:
             raise zb.ZBError(-1, "zb_stage_workspace_bytes (invalid config)")
@@ -62,13 +62,13 @@ class Stage:
 
     @staticmethod
     def from_synth(kind, n_layers, hidden, ffn, n_heads=0, n_kv_heads=0, head_dim=0, eps=1e-5,
-                   max_tokens=128, max_inflight=1, params_bits=None, device="cuda"):
+                   max_tokens=128, max_inflight=1, params_bits=None, device="cuda", attention="standin", seq_len=0):
         params = []
         for layer in params_bits:
             params.append({k: (bf16_from_bits(v, device) if v.dtype == np.uint16
                                else torch.from_numpy(v).to(device)) for k, v in layer.items()})
         return Stage(kind, n_layers, hidden, ffn, n_heads, n_kv_heads, head_dim, eps, max_tokens,
-                     max_inflight, params, device)
+                     max_inflight, params, device, attention, seq_len)
 
     def zero_grads(self):
         for g in self.grads:

@@ -34,6 +34,9 @@ if ROOT not in sys.path:
 WORKLOADS = {
     "llama8b_stage": dict(kind="transformer", n_layers=4, hidden=4096, ffn=14336, n_heads=32, n_kv_heads=8,
                           head_dim=128, tokens=4096, m=8),
+    # the same stage with the causal softmax attention core (one 4096-token sequence per microbatch)
+    "llama8b_stage_causal": dict(kind="transformer", n_layers=4, hidden=4096, ffn=14336, n_heads=32, n_kv_heads=8,
+                                 head_dim=128, tokens=4096, m=8, attention="causal", seq_len=0),
     "llama70b_stage": dict(kind="transformer", n_layers=2, hidden=8192, ffn=28672, n_heads=64, n_kv_heads=8,
                            head_dim=128, tokens=4096, m=8),
     "tiny_stage": dict(kind="mlp", n_layers=2, hidden=256, ffn=1024, n_heads=0, n_kv_heads=0, head_dim=0,
@@ -59,6 +62,126 @@ def gemm_flops_per_mb(w):
         q = (w["n_heads"] + 2 * w["n_kv_heads"]) * w["head_dim"]
         per_layer += 2.0 * t * (q * h + h * h)
     return per_layer * w["n_layers"]
+
+
+# ---------------------------------------------------------------- ncu summaries
+
+GEMM_SOURCES = ("gemm.cu", "device_common.cuh", "launch.h")
+EPILOGUES = {0: "bf16 store", 1: "residual epilogue", 2: "SwiGLU backward epilogue", 3: "float32 red.add epilogue"}
+
+
+def gemm_source_sha():
+    """sha256 over the GEMM kernel sources: a stored traffic figure holds only for these bytes."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "backward_split_linear_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def kernel_label(name):
+    """Readable label of a kernel name from an ncu CSV; GEMMs by pass (F, B, W) and epilogue."""
+    import re
+
+    m = re.search(r"(gemm_pair_kernel|gemm_kernel)<([^>]*)>", name)
+    if not m:
+        base = re.sub(r"^void ", "", name).replace("(anonymous namespace)::", "").replace("<unnamed>::", "").replace("unnamed>::", "")
+        base = re.sub(r"^zbk::", "", base)
+        return base.split("(")[0]
+    args = [a.strip() for a in m.group(2).split(",")]
+    if m.group(1) == "gemm_kernel":
+        args = args[1:]  # leading tile width
+    a_mn, b_mn, epi = args[0] in ("true", "1"), args[1] in ("true", "1"), int(args[2])
+    pas = "W" if a_mn else ("B" if b_mn else "F")
+    fam = "gemm_pair_kernel" if m.group(1) == "gemm_pair_kernel" else "gemm_kernel (one CTA)"
+    return f"{fam} {pas} ({EPILOGUES.get(epi, epi)})"
+
+
+def _ncu_value(value, unit):
+    v = float(value.replace(",", ""))
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+             "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1.0,
+             "ns": 1e-9, "us": 1e-6, "ms": 1e-3, "s": 1.0}
+    return v * scale.get(unit, 1.0)
+
+
+def read_ncu_csv(paths):
+    """Launches of one or more ncu --csv logs (a list, or names joined by commas), in order:
+    list of (kernel name, {metric: value in bytes or seconds})."""
+    import csv
+
+    if isinstance(paths, str):
+        paths = paths.split(",")
+    launches = {}
+    for f, path in enumerate(paths):
+        with open(path) as fh:
+            lines = [l for l in fh if l.startswith('"')]
+        for row in csv.DictReader(lines):
+            if not (row.get("ID") or "").isdigit() or not row.get("Metric Name"):
+                continue
+            key = (f, int(row["ID"]))
+            name, met = launches.setdefault(key, (row["Kernel Name"], {}))
+            met[row["Metric Name"]] = _ncu_value(row["Metric Value"], row.get("Metric Unit", ""))
+    return [launches[k] for k in sorted(launches)]
+
+
+def summarize_ncu(path, command, title):
+    """Markdown summary of an ncu CSV: launches, time and share per kernel; DRAM bytes if captured.
+
+    When DRAM bytes are present, a closing line gives the mean DRAM bytes per launch of the
+    B and W GEMMs with the sha256 of the GEMM sources; bench.py reports it as the roofline's
+    traffic while the sources are unchanged."""
+    rows = {}
+    for name, met in read_ncu_csv(path):
+        r = rows.setdefault(kernel_label(name), {"n": 0, "s": 0.0, "rd": 0.0, "wr": 0.0})
+        r["n"] += 1
+        r["s"] += met.get("gpu__time_duration.sum", 0.0)
+        r["rd"] += met.get("dram__bytes_read.sum", 0.0)
+        r["wr"] += met.get("dram__bytes_write.sum", 0.0)
+    total = sum(r["s"] for r in rows.values()) or 1.0
+    dram = any(r["rd"] or r["wr"] for r in rows.values())
+    out = [f"# {title}", "", "Command (GB300, one GPU; the same command exited 0 without ncu just before):", "",
+           "```", command, "```", "",
+           "Per-launch times under ncu are serialised and cold-cache: compare shares, not absolutes.", ""]
+    head = "| kernel | launches | total ms | share |" + (" DRAM read MB / launch | DRAM write MB / launch |" if dram else "")
+    out += [head, "|---|---:|---:|---:|" + ("---:|---:|" if dram else "")]
+    for label, r in sorted(rows.items(), key=lambda kv: -kv[1]["s"]):
+        line = f"| {label} | {r['n']} | {1e3 * r['s']:.2f} | {100 * r['s'] / total:.1f} % |"
+        if dram:
+            line += f" {r['rd'] / r['n'] / 1e6:.1f} | {r['wr'] / r['n'] / 1e6:.1f} |"
+        out.append(line)
+    out.append(f"| **total** | {sum(r['n'] for r in rows.values())} | {1e3 * total:.2f} | 100 % |" +
+               (" | |" if dram else ""))
+    if dram:
+        bw = [r for label, r in rows.items() if label.startswith("gemm") and (" B (" in label or " W (" in label)]
+        n = sum(r["n"] for r in bw)
+        if n:
+            per = sum(r["rd"] + r["wr"] for r in bw) / n
+            out += ["", f"gemm_bw_dram_bytes_per_launch: {per:.0f}", f"gemm_source_sha256: {gemm_source_sha()}"]
+    return "\n".join(out) + "\n"
+
+
+def profiled_gemm_traffic(workload, w_mode):
+    """DRAM bytes per B/W GEMM launch from the committed ncu summary of this workload, or None
+    when there is none or the GEMM sources changed since it was taken."""
+    if w_mode != "per-microbatch":
+        return None, "no capture for this W mode"
+    path = os.path.join(ROOT, "profiles", f"gemm_traffic_{workload}.md")
+    try:
+        with open(path) as fh:
+            text = fh.read()
+    except OSError:
+        return None, "no capture"
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.split(":")[0] in ("gemm_bw_dram_bytes_per_launch", "gemm_source_sha256"):
+            k, v = line.split(":", 1)
+            vals[k] = v.strip()
+    if vals.get("gemm_source_sha256") != gemm_source_sha() or "gemm_bw_dram_bytes_per_launch" not in vals:
+        return None, "GEMM sources changed since the capture"
+    return float(vals["gemm_bw_dram_bytes_per_launch"]), f"profiles/gemm_traffic_{workload}.md"
 
 
 def measured_peaks():
@@ -152,7 +275,8 @@ def oracle_sample(w, sample_tokens, seed=0, params_f64=None):
     from oracle import stage as S
 
     shp = dict(kind=w["kind"], n_layers=w["n_layers"], hidden=w["hidden"], ffn=w["ffn"], n_heads=w["n_heads"],
-               n_kv_heads=w["n_kv_heads"], head_dim=w["head_dim"], eps=1e-5)
+               n_kv_heads=w["n_kv_heads"], head_dim=w["head_dim"], eps=1e-5,
+               attention=w.get("attention", "standin"), seq_len=w.get("seq_len", 0))
     if params_f64 is None:
         inp = synth.stage_inputs(w["kind"], w["n_layers"], w["hidden"], w["ffn"], w["n_heads"], w["n_kv_heads"],
                                  w["head_dim"], tokens=sample_tokens, n_mb=1, seed=seed, gamma="ones")
@@ -250,7 +374,8 @@ def run_ours(args, w):
     inp = synth.stage_inputs(w["kind"], w["n_layers"], w["hidden"], w["ffn"], w["n_heads"], w["n_kv_heads"],
                              w["head_dim"], tokens=t, n_mb=m, seed=rank, gamma="ones")
     st = Stage.from_synth(w["kind"], w["n_layers"], w["hidden"], w["ffn"], w["n_heads"], w["n_kv_heads"],
-                          w["head_dim"], 1e-5, t, m, inp["params"])
+                          w["head_dim"], 1e-5, t, m, inp["params"], attention=w.get("attention", "standin"),
+                          seq_len=w.get("seq_len", 0))
     xs = [bf16_from_bits(b) for b in inp["x"]]
     dys = [bf16_from_bits(b) for b in inp["dy"]]
     out_dim = st.out_dim
@@ -261,7 +386,8 @@ def run_ours(args, w):
         # consecutive full stash slots into one W over their concatenated tokens.
         order = [("F", i) for i in range(m)] + [("B", i) for i in range(m)] + [("X", -1)]
     else:
-        order = zb.zb_schedule("zbh1", 0, m, m)
+        pipe = args.pipeline or m
+        order = zb.zb_schedule("zbh1", args.stage, pipe, m)
     stream = torch.cuda.current_stream()
     n_b = sum(1 for k, _ in order if k != "F")
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_b)]
@@ -366,6 +492,8 @@ def run_ours(args, w):
                "note": "B+W GEMM FLOPs over the whole step: H2D of x and dy, F, B, W, D2H of dx"}
 
     peaks = measured_peaks()
+    traffic, traffic_src = profiled_gemm_traffic(args.workload, args.w_mode) if not args.overridden else (
+        None, "workload overridden")
     gemm = {k: trace[k] for k in ("gemm_backward_input", "gemm_backward_weight")}
     g_ms = sum(c["ms"] for c in gemm.values())
     g_launch = sum(c["launches"] for c in gemm.values())
@@ -377,7 +505,8 @@ def run_ours(args, w):
     r_ach = r_bytes / (r_ms * 1e-3) / 1e9 if r_ms > 0 else None
     roofline = {"bound": "tensor", "kernel": "gemm_kernel (B and W GEMMs, tcgen05)",
                 "achieved": g_ach, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": g_ach / peaks["bf16_tflops_sustained"], "traffic": None,
+                "frac": g_ach / peaks["bf16_tflops_sustained"], "traffic": traffic,
+                "traffic_source": traffic_src,
                 "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
                 "launches": g_launch, "flops_per_launch": g_flops / max(1, g_launch),
                 "ms_per_launch": g_ms / max(1, g_launch)}
@@ -406,8 +535,11 @@ def run_ours(args, w):
                 "w": 100 * w_flops / (w_ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
                 "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peaks["source"] + " sustained"},
             "step_ms_with_forward": total_ms / args.steps,
+            # F, B and W of the whole order: the same GEMM FLOPs three times over the step
+            "fbw_tflops": whole_job_tflops(3 * flops_mb * m * args.steps, world, total_ms),
             "config": {"workload": args.workload, **{k: v for k, v in w.items()},
-                       "order": ("ZB-H1 order of stage 0, p = m (library generator)" if args.w_mode != "flush"
+                       "order": (f"ZB-H1 order of stage {args.stage} of p = {args.pipeline or m} (library generator)"
+                                 if args.w_mode != "flush"
                                  else "F and B of every microbatch, then one flush (W batched over the "
                                       "concatenated tokens of consecutive full stash slots)"),
                        "w_mode": args.w_mode,
@@ -420,6 +552,29 @@ def run_ours(args, w):
                        "samples": cs["samples"]},
             "trace": {k: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k, v in trace.items()},
         }
+        # the memory-limited order search fed with this run's per-microbatch F, B and W times
+        f_ms = sum(trace[k]["ms"] for k in ("gemm_forward", "row_forward", "attn_forward"))
+        n_mb = m * args.steps
+        t_f, t_b, t_w = (max(1, round(1e3 * v / n_mb)) for v in (f_ms, b_ms, w_ms))
+        search = {"p": 8, "m": 16, "t_us": {"F": t_f, "B": t_b, "W": t_w}, "by_memory_limit": {}}
+        for mem in (8, 12, 16):
+            _, limit, span = zb.zb_schedule_search(0, 8, 16, mem, t_f, t_b, t_w)
+            work = 16 * (t_f + t_b + t_w)
+            search["by_memory_limit"][mem] = {"ceiling": limit, "makespan_ms": span / 1e3,
+                                              "bubble_over_wall": (span - work) / span}
+        line["schedule_search"] = search
+        if w.get("attention") == "causal":
+            # the attention core's own work: not in the metric (which counts the linears), reported beside it
+            af, ab = trace["attn_forward"], trace["attn_backward"]
+            line["attention"] = {
+                "kind": "causal softmax, grouped K/V heads", "seq_len": w.get("seq_len", 0) or t,
+                "fwd_tflops": af["flops"] / (af["ms"] * 1e-3) / 1e12 if af["ms"] else None,
+                "bwd_tflops": ab["flops"] / (ab["ms"] * 1e-3) / 1e12 if ab["ms"] else None,
+                "bwd_flops_counted": "5 products of 2 d per visible query-key pair (the kernels do 7: "
+                                     "dQ recomputes S and dP)",
+                "bwd_share_of_b_time": ab["ms"] / b_ms if b_ms else None,
+                "b_tflops_with_attention": (b_flops + ab["flops"]) / (b_ms * 1e-3) / 1e12,
+            }
         print(json.dumps(line), flush=True)
     st.close()
     if dist is not None:
@@ -517,10 +672,27 @@ def main():
                                      "rmsnorm_backward_gamma"],
                     help="time one per-step op instead of the stage (with --shape T,IN,OUT)")
     ap.add_argument("--shape", default="4096,4096,14336")
+    ap.add_argument("--stage", type=int, default=0, help="pipeline stage whose ZB-H1 order the step runs")
+    ap.add_argument("--pipeline", type=int, default=0, help="pipeline depth p of that order (default: m)")
+    ap.add_argument("--layers", type=int, help="override the workload's layer count (small ncu captures)")
+    ap.add_argument("--microbatches", type=int, help="override the workload's microbatch count")
+    ap.add_argument("--summarize-ncu", metavar="CSV[,CSV...]", help="print a markdown summary of ncu --csv logs")
+    ap.add_argument("--ncu-command", default="", help="the command that wrote the CSV (for the summary)")
+    ap.add_argument("--title", default="ncu launch list")
     args = ap.parse_args()
+    if args.summarize_ncu:
+        sys.stdout.write(summarize_ncu(args.summarize_ncu, args.ncu_command, args.title))
+        return 0
     if args.op:
         return run_op(args)
-    w = WORKLOADS[args.workload]
+    w = dict(WORKLOADS[args.workload])
+    args.overridden = False
+    if args.layers:
+        w["n_layers"] = args.layers
+        args.overridden = True
+    if args.microbatches:
+        w["m"] = args.microbatches
+        args.overridden = True
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -124,6 +124,23 @@ zb_status zb_schedule_bubble(zb_sched_kind kind, int32_t p, int32_t m,
 zb_status zb_schedule_window_idle(zb_sched_kind kind, int32_t p, int32_t m,
                                   int64_t* idle_units, double* idle_over_compute);
 
+/* Memory-limited ZB order with measured op times.  "Zero Bubble Pipeline
+ * Parallelism" (the abstract: an algorithm finds the best schedule for a
+ * given configuration and memory limit) and the guide's section "Core
+ * Innovation 2" (ZB-H1 holds p microbatches, ZB-2p 2p).  Reading: for each
+ * ceiling L in [p, min(2p, mem_limit)], the ZB-H1 policy holding at most L
+ * microbatches, with min(L - s, 2(p - s) - 1) forwards before the first B of
+ * stage s (ZB-H1 at L = p, ZB-2p at L = 2p), run on all p stages with F, B and
+ * W taking t_f, t_b and t_w (positive integers in any one unit; communication
+ * free).  The L whose run ends first wins (the smallest on ties); `out` gets
+ * stage `stage`'s order under it.  *chosen_limit and *makespan (in the unit of
+ * the durations) are written when not NULL.
+ * Errors: ZB_ERR_ARG (mem_limit < p, a duration < 1, p m > 2^20, bad stage),
+ * ZB_ERR_CAPACITY (cap < 3m; *n_out = 3m). */
+zb_status zb_schedule_search(int32_t stage, int32_t p, int32_t m, int32_t mem_limit, int32_t t_f,
+                             int32_t t_b, int32_t t_w, zb_op* out, int32_t cap, int32_t* n_out,
+                             int32_t* chosen_limit, int64_t* makespan);
+
 /* ========================================================================
  * Per-step operations (stateless).  One call per step of the hot path; the
  * stage calls below are built from exactly these launches.
@@ -225,6 +242,33 @@ zb_status zb_op_attention_forward(const void* qkv, void* a, int32_t tokens,
                                   int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                   void* stream);
 
+/* Causal softmax attention with grouped K/V heads: the attention core in
+ * its full form.  The pages name the qkv and output projections around it but
+ * not the core itself; this is the usual one, without position encoding.
+ * For head h, with j = h / (nh / nkv):
+ *   a_h = softmax(q_h k_j^T / sqrt(hd), keys <= query) v_j
+ * over independent sequences of seq_len consecutive tokens (0: the `tokens`
+ * rows are one sequence; the last sequence may be shorter than seq_len).
+ *  - qkv [T, (nh + 2 nkv) hd] bf16 (q heads, then k heads, then v heads);
+ *    a and da [T, nh hd] bf16; dqkv like qkv.
+ *  - lse float32 [nh][zb_op_attention_stat_stride(T)]: per head and query
+ *    row, log2 of the softmax denominator in units of the scaled score.  The
+ *    forward writes it; the backward reads it.  dvec is caller-owned float32
+ *    scratch of the same shape (contents ignored).
+ *  - hd is 64 or 128; seq_len is 0 or a multiple of 128.  Other shapes
+ *    return ZB_ERR_SHAPE.
+ *  - The backward writes every column of dqkv.  Each output element is
+ *    written by one thread after a fixed-order sum, so results are bitwise
+ *    reproducible. */
+int32_t zb_op_attention_stat_stride(int32_t tokens);
+zb_status zb_op_attention_causal_forward(const void* qkv, void* a, float* lse, int32_t tokens,
+                                         int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                         int32_t seq_len, void* stream);
+zb_status zb_op_attention_causal_backward(const void* qkv, const void* a, const void* da,
+                                          const float* lse, float* dvec, void* dqkv,
+                                          int32_t tokens, int32_t n_heads, int32_t n_kv_heads,
+                                          int32_t head_dim, int32_t seq_len, void* stream);
+
 /* Device status word shared by all kernels of the library on the current
  * device: 0 = fine, else the code of the first wait that ran out.  Reading
  * synchronises `stream`; `reset` != 0 clears the word afterwards.  Returns
@@ -248,6 +292,13 @@ typedef enum {
                                  h = x + a W_o^T; then the MLP part */
 } zb_layer_kind;
 
+/* The attention core A of a TRANSFORMER layer. */
+typedef enum {
+    ZB_ATTN_STANDIN = 0,  /* weight-free stand-in a_h = q_h + k_j + v_j (per token) */
+    ZB_ATTN_CAUSAL = 1    /* causal softmax attention, as zb_op_attention_causal_forward;
+                             the stash also keeps qkv and the row log-sum-exp */
+} zb_attention_kind;
+
 typedef struct {
     int32_t kind;          /* zb_layer_kind */
     int32_t n_layers;
@@ -259,6 +310,9 @@ typedef struct {
     float eps;             /* RMSNorm epsilon */
     int32_t max_tokens;    /* largest T of any microbatch */
     int32_t max_inflight;  /* stash slots: microbatches between F and W [G3] */
+    int32_t attention;     /* TRANSFORMER: zb_attention_kind */
+    int32_t seq_len;       /* ZB_ATTN_CAUSAL: tokens per sequence, 0 or a multiple of 128
+                              (0: each microbatch is one sequence) */
 } zb_stage_config;
 
 /* Per-layer device pointers.  Weights bf16 [out, in]; gamma float32 [H];
@@ -347,6 +401,8 @@ typedef enum {
                                         backward, and the stash copy of dy */
     ZB_KCLASS_ROW_BACKWARD_WEIGHT,   /* W row kernels: gamma-gradient reduction */
     ZB_KCLASS_ROW_FORWARD,           /* F row kernels and the stash copy of x */
+    ZB_KCLASS_ATTN_FORWARD,          /* F causal attention */
+    ZB_KCLASS_ATTN_BACKWARD,         /* B causal attention (rowsum, dK/dV, dQ kernels) */
     ZB_KCLASS_COUNT
 } zb_kernel_class;
 

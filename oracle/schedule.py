@@ -40,6 +40,15 @@ Orders:
   for m >= 2p - 1) while holding up to 2p microbatches; over the common
   makespan nothing changes, since 3m + p - 1 is already the shortest
   possible when communication is free.
+* Memory-limited orders ("Zero Bubble Pipeline Parallelism", the abstract: an
+  algorithm that finds the best schedule for a given model configuration and
+  memory limit; the guide's section "Core Innovation 2": ZB-H1 holds p
+  microbatches, ZB-2p holds 2p).  Reading: the same policy with a ceiling L
+  in [p, 2p] and min(L - s, 2(p - s) - 1) forwards before the first B of
+  stage s (p - s at L = p, ZB-2p's count at L = 2p), run with measured integer
+  durations t_F, t_B, t_W instead of unit times; the search takes the L no
+  larger than the memory limit with the shortest makespan (the smallest such
+  L on ties).
 """
 from __future__ import annotations
 
@@ -180,6 +189,83 @@ def simulate_zbh1(p, m, limit=None, warm=None):
                     pending_w[s].append(i)
         t += 1
     return orders, start
+
+
+def simulate_timed(p, m, limit, warm, t_f, t_b, t_w):
+    """The ZB-H1 policy of simulate_zbh1 with op durations t_f, t_b, t_w (integers).
+
+    Stages decide whenever they are free, all on the state at that moment, as
+    in the unit-time run; time then jumps to the next end of an op.  Returns
+    (orders, start, finish)."""
+    dur = {F: t_f, B: t_b, W: t_w}
+    fb = [fb_order(s, p, m, warm(s)) for s in range(p)]
+    ptr = [0] * p
+    orders = [[] for _ in range(p)]
+    start, finish = {}, {}
+    f_issued = [0] * p
+    w_issued = [0] * p
+    pending_w = [[] for _ in range(p)]
+    busy_until = [0] * p
+    t = 0
+    total = 3 * m * p
+    while len(start) < total:
+        decided = []
+        for s in range(p):
+            if busy_until[s] > t:
+                continue
+            op = None
+            if ptr[s] < len(fb[s]):
+                kind, i = fb[s][ptr[s]]
+                ready = all(d in finish and finish[d] <= t for d in _deps(kind, s, i, p, True))
+                if ready:
+                    if kind == F and f_issued[s] - w_issued[s] >= limit:
+                        if pending_w[s]:
+                            op = (W, pending_w[s][0])
+                    else:
+                        op = (kind, i)
+                elif pending_w[s]:
+                    op = (W, pending_w[s][0])
+            elif pending_w[s]:
+                op = (W, pending_w[s][0])
+            if op is not None:
+                decided.append((s, op))
+        for s, (kind, i) in decided:
+            start[(kind, s, i)] = t
+            finish[(kind, s, i)] = t + dur[kind]
+            busy_until[s] = t + dur[kind]
+            orders[s].append((kind, i))
+            if kind == W:
+                pending_w[s].pop(0)
+                w_issued[s] += 1
+            else:
+                ptr[s] += 1
+                if kind == F:
+                    f_issued[s] += 1
+                else:
+                    pending_w[s].append(i)
+        if len(start) < total:
+            later = [v for v in finish.values() if v > t]
+            if not later:
+                raise RuntimeError("timed simulation deadlocked")
+            t = min(later)
+    return orders, start, finish
+
+
+def limited_warm(p, limit):
+    """Forwards before the first B of stage s under a ceiling of `limit` held microbatches."""
+    return lambda s: min(limit - s, 2 * (p - s) - 1)
+
+
+def search_limit(p, m, mem_limit, t_f, t_b, t_w):
+    """The ceiling L in [p, min(2p, mem_limit)] whose order runs shortest with the given
+    durations (the smallest L on ties).  Returns (L, makespan, orders)."""
+    best = None
+    for limit in range(p, min(2 * p, mem_limit) + 1):
+        orders, _, finish = simulate_timed(p, m, limit, limited_warm(p, limit), t_f, t_b, t_w)
+        span = max(finish.values())
+        if best is None or span < best[1]:
+            best = (limit, span, orders)
+    return best
 
 
 def simulate_zb2p(p, m):

@@ -1,0 +1,69 @@
+"""Host logic of bench.py that needs no GPU: the ncu summary and the traffic lookup."""
+import bench
+
+HEADER = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+          '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n')
+
+
+def row(i, name, metric, unit, value):
+    return (f'"{i}","1","python","h","{name}","1","7","(192, 1, 1)","(152, 1, 1)","0","10.3","",'
+            f'"{metric}","{unit}","{value}"\n')
+
+
+W = "void zbk::(anonymous namespace)::gemm_pair_kernel<true, true, 3, 2>(CUtensorMap, CUtensorMap, KParams)"
+B = "void zbk::(anonymous namespace)::gemm_pair_kernel<false, true, 0, 2>(CUtensorMap, CUtensorMap, KParams)"
+F = "void zbk::(anonymous namespace)::gemm_pair_kernel<false, false, 1, 2>(CUtensorMap, CUtensorMap, KParams)"
+R = "void zbk::(anonymous namespace)::rmsnorm_bwd_kernel<2>(const unsigned short *, int)"
+# the form ncu's CSV prints on the GB300 box: bools as 0 / 1, anonymous namespaces as "unnamed>"
+B_NCU = "void unnamed>::gemm_pair_kernel<0, 1, 2, 2>(CUtensorMap_st, CUtensorMap_st, unnamed>::KParams)"
+
+
+def test_labels_of_ncu_names():
+    assert bench.kernel_label(B_NCU) == "gemm_pair_kernel B (SwiGLU backward epilogue)"
+    assert bench.kernel_label(W) == "gemm_pair_kernel W (float32 red.add epilogue)"
+    assert bench.kernel_label("void <unnamed>::dgamma_final_kernel(<unnamed>::GammaBatch)") == "dgamma_final_kernel"
+
+
+def test_summary_shares_and_gemm_traffic(tmp_path):
+    csv = tmp_path / "l.csv"
+    lines = ["==PROF== Connected to process\n", HEADER]
+    launches = [(0, F, 100.0, 10.0, 1.0), (1, B, 200.0, 20.0, 2.0), (2, W, 600.0, 30.0, 40.0), (3, R, 100.0, 5.0, 5.0)]
+    for i, name, us, rd_mb, wr_mb in launches:
+        lines.append(row(i, name, "gpu__time_duration.sum", "ns", f"{1000 * us:,.0f}"))
+        lines.append(row(i, name, "dram__bytes_read.sum", "Mbyte", rd_mb))
+        lines.append(row(i, name, "dram__bytes_write.sum", "byte", int(wr_mb * 1e6)))
+    csv.write_text("".join(lines))
+    text = bench.summarize_ncu(str(csv), "ncu ... python bench.py", "t")
+    assert "| gemm_pair_kernel W (float32 red.add epilogue) | 1 | 0.60 | 60.0 % | 30.0 | 40.0 |" in text
+    assert "| rmsnorm_bwd_kernel<2> | 1 | 0.10 | 10.0 % |" in text
+    assert "| **total** | 4 | 1.00 | 100 % |" in text
+    # B and W GEMM launches only: (20 + 2 + 30 + 40) MB over 2 launches
+    assert "gemm_bw_dram_bytes_per_launch: 46000000" in text
+    assert f"gemm_source_sha256: {bench.gemm_source_sha()}" in text
+
+
+def test_traffic_lookup_needs_matching_sources(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "gemm_source_sha", lambda: "abc")
+    assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] is None
+    (prof / "gemm_traffic_w.md").write_text("x\ngemm_bw_dram_bytes_per_launch: 123\ngemm_source_sha256: abc\n")
+    assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] == 123.0
+    assert bench.profiled_gemm_traffic("w", "flush")[0] is None
+    (prof / "gemm_traffic_w.md").write_text("gemm_bw_dram_bytes_per_launch: 123\ngemm_source_sha256: old\n")
+    assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] is None
+
+
+def test_summary_of_several_logs(tmp_path):
+    """Captures taken in chunks (ids restart at 0 in each log) add up launch by launch."""
+    paths = []
+    for f in range(2):
+        csv = tmp_path / f"c{f}.csv"
+        csv.write_text(HEADER + row(0, W, "gpu__time_duration.sum", "ns", "1000") +
+                       row(0, W, "dram__bytes_read.sum", "byte", "2000000") +
+                       row(0, W, "dram__bytes_write.sum", "byte", "0"))
+        paths.append(str(csv))
+    text = bench.summarize_ncu(",".join(paths), "cmd", "t")
+    assert "| gemm_pair_kernel W (float32 red.add epilogue) | 2 | 0.00 | 100.0 % | 2.0 | 0.0 |" in text
+    assert "gemm_bw_dram_bytes_per_launch: 2000000" in text

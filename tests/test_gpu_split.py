@@ -1,0 +1,90 @@
+"""GPU tests of the K-split GEMM path of the stage runtime.
+
+A stage launches its GEMMs with scratch for a K split: when a launch's tiles
+would leave the last wave of CTA pairs mostly idle, each tile's contraction is
+cut in two halves computed by different CTA pairs, and the half that finishes
+second adds the other's float32 partial.  The per-step ops never split, so
+they serve as the unsplit comparison on the same inputs.  Shapes here give
+256 to 400 output tiles of 256 x 256 (under five waves on 76 CTA pairs), with
+ragged tokens, features and contraction length.
+"""
+import numpy as np
+import pytest
+import torch
+
+from backward_split_linear_gb300 import binding as zb
+from backward_split_linear_gb300 import synth
+from backward_split_linear_gb300.runtime import Stage, bf16_from_bits, f64_from_bf16
+from parity import assert_close, errors
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _status_clean(cuda_device):
+    zb.zb_device_status(reset=True)
+    yield
+    st, code = zb.zb_device_status()
+    assert st == 0, f"device status word set: {code}"
+
+
+def run_linear_stage(inp, t, n_in, n_out):
+    st = Stage.from_synth("linear", 1, n_in, n_out, max_tokens=t, max_inflight=1, params_bits=inp["params"])
+    x = bf16_from_bits(inp["x"][0])
+    dy = bf16_from_bits(inp["dy"][0])
+    y = torch.empty(t, n_out, dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty(t, n_in, dtype=torch.bfloat16, device="cuda")
+    st.forward(0, x, y)
+    st.backward_input(0, dy, dx)
+    st.backward_weight(0)
+    st.sync()
+    dw = st.grads[0]["w"].clone()
+    st.close()
+    return y, dx, dw
+
+
+@pytest.mark.parametrize("t,n_in,n_out", [(4096, 4096, 14336), (4096, 4096, 4096), (4000, 4032, 6208)])
+def test_split_matches_unsplit_and_oracle(t, n_in, n_out):
+    inp = synth.stage_inputs("linear", 1, n_in, n_out, tokens=t, n_mb=1, seed=11)
+    y, dx, dw = run_linear_stage(inp, t, n_in, n_out)
+    # the same products through the per-step ops, which never split K
+    w = bf16_from_bits(inp["params"][0]["w"])
+    x = bf16_from_bits(inp["x"][0])
+    dy = bf16_from_bits(inp["dy"][0])
+    y_op = torch.empty_like(y)
+    dx_op = torch.empty_like(dx)
+    dw_op = torch.zeros_like(dw)
+    zb.zb_op_linear_forward(x, w, None, y_op, t, n_in, n_out)
+    zb.zb_op_backward_input(dy, w, dx_op, t, n_in, n_out)
+    zb.zb_op_backward_weight(dy, x, dw_op, t, n_in, n_out)
+    torch.cuda.synchronize()
+    # bf16 results differ from the unsplit ones only where the float32 sum,
+    # taken in another order, rounds to a neighbouring bf16 value
+    for name, a, b in (("y", y, y_op), ("dx", dx, dx_op)):
+        fro, mx = errors(f64_from_bf16(a), f64_from_bf16(b))
+        print(f"{name} split vs unsplit: frobenius {fro:.2e}, max {mx:.2e}")
+        assert fro < 1e-3 and mx < 1e-2, name
+    fro, _ = errors(dw.cpu().numpy(), dw_op.cpu().numpy())
+    print(f"dw split vs unsplit: frobenius {fro:.2e}")
+    assert fro < 1e-5
+    # against the float64 oracle on sampled rows (each row is an exact small product)
+    wf = synth.bf16_to_f64(inp["params"][0]["w"])
+    xf = synth.bf16_to_f64(inp["x"][0])
+    dyf = synth.bf16_to_f64(inp["dy"][0])
+    rng = np.random.default_rng(t + n_out)
+    rows = np.sort(np.append(rng.choice(t, 15, replace=False), t - 1))
+    assert_close(f64_from_bf16(y)[rows], xf[rows] @ wf.T, "sampled y rows")
+    assert_close(f64_from_bf16(dx)[rows], dyf[rows] @ wf, "sampled dx rows")
+    wrows = np.sort(np.append(rng.choice(n_out, 15, replace=False), n_out - 1))
+    assert_close(dw.cpu().numpy()[wrows], dyf[:, wrows].T @ xf, "sampled dW rows")
+
+
+def test_split_is_bitwise_reproducible():
+    """Either half of a tile may finish first; the result must not depend on which."""
+    t, n_in, n_out = 4096, 4096, 4096
+    inp = synth.stage_inputs("linear", 1, n_in, n_out, tokens=t, n_mb=1, seed=12)
+    first = run_linear_stage(inp, t, n_in, n_out)
+    for _ in range(2):
+        again = run_linear_stage(inp, t, n_in, n_out)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)

@@ -175,7 +175,12 @@ def test_config4_zbh1_order_full_size():
 
 def test_concat_identity_full_size():
     """8B-shaped stage, 4096 tokens: one microbatch vs the same tokens as two microbatches.
-    dx is identical bit for bit (every op is per token); dW agrees to float32 summation order."""
+    Every op except the weight contractions acts per token, so the two runs compute the same
+    dx and dW.  They do not round alike: the 4096-token launches may cut their contraction in
+    two (the K split), the 2048-token ones do not, so float32 sums run in another order, a few
+    bf16 roundings flip and the flips travel down both layers into the stashed gradients
+    that W contracts.  dx and dW are held to the two-layer stage tolerance; the exact
+    identity on equal stashes is test_flush_batches_consecutive_full_microbatches."""
     c = dict(LLAMA8B, n_layers=2)
     whole = synth.stage_inputs(c["kind"], 2, 4096, 14336, 32, 8, 128, tokens=4096, n_mb=1, seed=3)
     split = {"params": whole["params"],
@@ -185,12 +190,14 @@ def test_concat_identity_full_size():
     dx1 = run_gpu(st1, whole, plain_order(1))
     st2 = make_gpu_stage(c, split, 2048, 2)
     dx2 = run_gpu(st2, split, [("F", 0), ("F", 1), ("B", 0), ("B", 1), ("W", 1), ("W", 0)])
-    assert torch.equal(dx1[0], torch.cat([dx2[0], dx2[1]]))
+    assert_close(f64_from_bf16(torch.cat([dx2[0], dx2[1]])), f64_from_bf16(dx1[0]), "dx, two microbatches vs one",
+                 fro_tol=stage_fro_tol(2))
     for li in range(2):
         for k in st1.grads[li]:
             a = st1.grads[li][k].double()
             b = st2.grads[li][k].double()
-            assert (torch.linalg.norm(a - b) / torch.linalg.norm(a)).item() < 1e-5, (li, k)
+            fro = (torch.linalg.norm(a - b) / torch.linalg.norm(a)).item()
+            assert fro < stage_fro_tol(2), (li, k, fro)
 
 
 @pytest.mark.parametrize("tokens", [512, 1024, 2048, 4096, 8192])

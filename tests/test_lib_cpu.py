@@ -90,13 +90,16 @@ def test_stage_config_checks(zblib):
     assert zb.zb_stage_workspace_bytes(bad_heads) == 0
     bad_linear = zb.make_config("linear", 2, 256, 512)                 # a linear stage has one layer
     assert zb.zb_stage_workspace_bytes(bad_linear) == 0
-    # workspace grows linearly with the number of stash slots
-    one = zb.zb_stage_workspace_bytes(zb.make_config("mlp", 2, 256, 1024, max_tokens=128, max_inflight=1))
-    four = zb.zb_stage_workspace_bytes(zb.make_config("mlp", 2, 256, 1024, max_tokens=128, max_inflight=4))
+    # every stash slot adds one microbatch's stash: per MLP layer x, n2, dy, dn2 [T, H],
+    # [g|u] [T, 2F], s [T, F] in bf16 and rstd [T] in float32
+    T, H, F, L = 128, 256, 1024, 2
+    per_slot = L * (4 * T * H * 2 + T * 2 * F * 2 + T * F * 2 + T * 4)
+    one = zb.zb_stage_workspace_bytes(zb.make_config("mlp", L, H, F, max_tokens=T, max_inflight=1))
+    four = zb.zb_stage_workspace_bytes(zb.make_config("mlp", L, H, F, max_tokens=T, max_inflight=4))
+    assert one >= per_slot
+    assert four - one >= 3 * per_slot
     scratch = zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(128, 256)
     assert scratch > 0 and scratch % (256 * 4) == 0  # whole float32 rows of partial sums
-    # 3 more stash slots: at least 3 x (one slot's bytes), i.e. 3 x (one - reduction scratch)
-    assert four - one >= 3 * (one - scratch) > 0
 
 
 def test_stage_host_errors_without_device(zblib):
@@ -136,3 +139,44 @@ def test_op_argument_errors(zblib):
     assert lib.zb_op_backward_weight(fake, fake, fake, -1, 64, 64, None) == -2
     assert lib.zb_op_backward_input_attention(fake, fake, fake, 8, 6, 4, 64, None) == -2  # 4 does not divide 6
     assert lib.zb_op_rmsnorm_backward_gamma(fake, fake, fake, fake, 64, 256, fake, 10, None) == -10
+
+
+def test_causal_attention_host_checks(zblib):
+    """Shape rules of the causal attention core, decided on the host before any device call."""
+    assert zb.zb_op_attention_stat_stride(0) == 128
+    assert zb.zb_op_attention_stat_stride(129) == 256
+    fake = 1 << 20  # never dereferenced: the calls below fail their shape checks first
+    for nh, nkv, d, seq_len in [(4, 2, 96, 0), (4, 2, 64, 100), (4, 3, 64, 0), (4, 2, 64, -128)]:
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_op_attention_causal_forward(fake, fake, fake, 256, nh, nkv, d, seq_len, stream=0)
+        assert e.value.name == "ZB_ERR_SHAPE"
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_op_attention_causal_backward(fake, fake, fake, fake, fake, fake, 256, nh, nkv, d, seq_len,
+                                               stream=0)
+        assert e.value.name == "ZB_ERR_SHAPE"
+    tf = dict(kind="transformer", n_layers=2, hidden=256, ffn=512, n_heads=4, n_kv_heads=2, head_dim=64,
+              max_tokens=256, max_inflight=2)
+    standin = zb.zb_stage_workspace_bytes(zb.make_config(**tf))
+    causal = zb.zb_stage_workspace_bytes(zb.make_config(**tf, attention="causal", seq_len=128))
+    # the causal stash adds qkv [T, 512] bf16 and lse [4, 256] float32 per layer and slot
+    assert causal - standin >= 2 * 2 * (256 * 512 * 2 + 4 * 256 * 4) - 256 * 512 * 2
+    assert zb.zb_stage_workspace_bytes(zb.make_config(**tf, attention="causal", seq_len=100)) == 0
+    assert zb.zb_stage_workspace_bytes(zb.make_config(**tf, seq_len=128)) == 0  # stand-in has no sequences
+    assert zb.zb_stage_workspace_bytes(zb.make_config("mlp", 2, 256, 512, max_tokens=128,
+                                                      attention="causal")) == 0
+
+
+def test_schedule_search_equals_oracle(zblib):
+    """The library's memory-limited search gives the oracle's order, ceiling and makespan."""
+    from oracle import schedule as OS
+
+    for p, m in [(1, 3), (2, 5), (4, 8), (4, 13), (8, 16)]:
+        for mem in (p, p + p // 2, 2 * p, 3 * p):
+            for tf, tb, tw in [(1, 1, 1), (10, 12, 9), (3, 7, 2), (5, 5, 11)]:
+                limit, span, orders = OS.search_limit(p, m, mem, tf, tb, tw)
+                for s in range(p):
+                    got = zb.zb_schedule_search(s, p, m, mem, tf, tb, tw)
+                    assert got == (orders[s], limit, span), (p, m, mem, tf, tb, tw, s)
+    with pytest.raises(zb.ZBError) as e:
+        zb.zb_schedule_search(0, 4, 8, 3, 1, 1, 1)  # a ceiling below p cannot hold the warm-up
+    assert e.value.name == "ZB_ERR_ARG"

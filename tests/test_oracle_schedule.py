@@ -163,3 +163,85 @@ def test_zb2p_invariants(p, m):
     for (k, s, i), t in start.items():
         for d in S._deps(k, s, i, p, True):
             assert start[d] + 1 <= t
+
+
+# ----------------------------------------------------------------------------
+# memory-limited orders with measured durations
+# ----------------------------------------------------------------------------
+
+DURATIONS = [(1, 1, 1), (10, 12, 9), (3, 7, 2), (5, 5, 11)]
+
+
+@pytest.mark.parametrize("p", [1, 2, 4, 8])
+@pytest.mark.parametrize("m", [1, 3, 8, 16, 21])
+def test_timed_run_with_unit_times_is_the_unit_policy(p, m):
+    """With t_F = t_B = t_W = 1 the timed run is the unit-time ZB-H1 (L = p) and ZB-2p (L = 2p)."""
+    orders, _, _ = S.simulate_timed(p, m, p, S.limited_warm(p, p), 1, 1, 1)
+    assert orders == S.simulate_zbh1(p, m)[0]
+    orders, _, _ = S.simulate_timed(p, m, 2 * p, S.limited_warm(p, 2 * p), 1, 1, 1)
+    assert orders == S.simulate_zb2p(p, m)[0]
+
+
+@pytest.mark.parametrize("t", [1, 3, 7])
+def test_timed_equal_durations_scale_the_closed_form(t):
+    """Equal durations t: ZB-H1 ends at t (3m + p - 1) for m >= p ("Mathematical Modeling")."""
+    for p in (2, 4, 8):
+        for m in (p, 2 * p + 1):
+            _, _, finish = S.simulate_timed(p, m, p, S.limited_warm(p, p), t, t, t)
+            assert max(finish.values()) == t * (3 * m + p - 1)
+
+
+@pytest.mark.parametrize("tf,tb,tw", DURATIONS)
+@pytest.mark.parametrize("p,m", [(2, 5), (4, 8), (4, 13), (8, 16)])
+def test_timed_invariants(tf, tb, tw, p, m):
+    dur = {S.F: tf, S.B: tb, S.W: tw}
+    for limit in range(p, 2 * p + 1):
+        orders, start, finish = S.simulate_timed(p, m, limit, S.limited_warm(p, limit), tf, tb, tw)
+        for s, order in enumerate(orders):
+            assert len(order) == 3 * m
+            assert S.peak_in_flight(order) <= limit
+            pos = {op: j for j, op in enumerate(order)}
+            for i in range(m):
+                assert pos[(S.F, i)] < pos[(S.B, i)] < pos[(S.W, i)]
+            # one op at a time per stage, in program order
+            ends = [start[(k, s, i)] + dur[k] for k, i in order]
+            starts = [start[(k, s, i)] for k, i in order]
+            assert all(ends[j] <= starts[j + 1] for j in range(len(order) - 1))
+        for (k, s, i), t0 in start.items():
+            assert finish[(k, s, i)] == t0 + dur[k]
+            for d in S._deps(k, s, i, p, True):
+                assert finish[d] <= t0
+        span = max(finish.values())
+        assert span >= m * (tf + tb + tw)        # every stage does all of its work
+        assert span >= p * (tf + tb) + tw        # microbatch 0 down and back, then a W
+
+
+@pytest.mark.parametrize("tf,tb,tw", DURATIONS)
+def test_search_takes_the_best_limit_within_memory(tf, tb, tw):
+    p, m = 4, 12
+    spans = {}
+    for limit in range(p, 2 * p + 1):
+        _, _, finish = S.simulate_timed(p, m, limit, S.limited_warm(p, limit), tf, tb, tw)
+        spans[limit] = max(finish.values())
+    prev = None
+    for mem in range(p, 2 * p + 3):
+        limit, span, orders = S.search_limit(p, m, mem, tf, tb, tw)
+        allowed = [l for l in spans if l <= mem]
+        assert limit <= mem and span == min(spans[l] for l in allowed)
+        assert limit == min(l for l in allowed if spans[l] == span)
+        assert max(S.peak_in_flight(o) for o in orders) <= limit
+        if prev is not None:
+            assert span <= prev  # more memory never makes the best order slower
+        prev = span
+
+
+def test_planted_ceiling_mistake_is_caught(monkeypatch):
+    """A run that ignores the ceiling must break the in-flight pin."""
+    real = S.simulate_timed
+
+    def no_ceiling(p, m, limit, warm, tf, tb, tw):
+        return real(p, m, 10 ** 9, warm, tf, tb, tw)
+
+    monkeypatch.setattr(S, "simulate_timed", no_ceiling)
+    with pytest.raises(AssertionError):
+        test_timed_invariants(10, 12, 9, 4, 8)
