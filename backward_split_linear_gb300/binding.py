@@ -79,6 +79,9 @@ _SIGS = {
     "zb_op_backward_input_attention": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                                  c_int32, c_void_p]),
     "zb_op_backward_weight": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]),
+    "zb_op_backward_weight_group": (c_int32, [c_int32, ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
+                                              ctypes.POINTER(c_void_p), c_int32, ctypes.POINTER(c_int32),
+                                              ctypes.POINTER(c_int32), c_void_p]),
     "zb_op_rmsnorm_backward_gamma_scratch_bytes": (c_size_t, [c_int32, c_int32]),
     "zb_op_rmsnorm_backward_gamma": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
                                                c_void_p, c_size_t, c_void_p]),
@@ -243,6 +246,14 @@ def zb_op_backward_input_attention(dh, w_o, dqkv, tokens, n_heads, n_kv_heads, h
 def zb_op_backward_weight(dy, x, dw, tokens, in_features, out_features, stream=None):
     _check(lib().zb_op_backward_weight(_ptr(dy), _ptr(x), _ptr(dw), tokens, in_features, out_features,
                                        _stream(stream)), "zb_op_backward_weight")
+
+
+def zb_op_backward_weight_group(dys, xs, dws, tokens, in_features, out_features, stream=None):
+    n = len(dys)
+    ptrs = lambda ts: (c_void_p * n)(*[_ptr(t) for t in ts])  # noqa: E731
+    ints = lambda vs: (c_int32 * n)(*vs)  # noqa: E731
+    _check(lib().zb_op_backward_weight_group(n, ptrs(dys), ptrs(xs), ptrs(dws), tokens, ints(in_features),
+                                             ints(out_features), _stream(stream)), "zb_op_backward_weight_group")
 
 
 def zb_op_rmsnorm_backward_gamma_scratch_bytes(tokens, hidden):

@@ -146,6 +146,22 @@ zb_status run_backward_input_attention(const void* dh, const void* w_o, void* dq
     return cuda_status(zbk::launch_attention_backward_kv(dqkv, t, nh, nkv, hd, s));
 }
 
+GemmArgs wgrad_args(const void* dy, const void* x, float* dw, int t, int in, int out) {
+    GemmArgs g{};
+    g.kind = GemmKind::BackwardWeight;
+    g.epi = Epilogue::AccumF32;
+    g.a = dy;
+    g.lda = out;
+    g.b = x;
+    g.ldb = in;
+    g.m = out;
+    g.n = in;
+    g.k = t;
+    g.out = dw;
+    g.ldo = in;
+    return g;
+}
+
 zb_status run_backward_weight(const void* dy, const void* x, float* dw, int t, int in, int out,
                               cudaStream_t s, const SplitWs* ws = nullptr) {
     GemmArgs g{};
@@ -303,6 +319,22 @@ extern "C" zb_status zb_op_backward_weight(const void* dy, const void* x, float*
     if (!rows_ok(dy, tokens) || !rows_ok(x, tokens) || !fixed_ok(dw)) return ZB_ERR_ARG;
     ZB_TRY(device_ok());
     return run_backward_weight(dy, x, dw, tokens, in_features, out_features, as_stream(stream));
+}
+
+extern "C" zb_status zb_op_backward_weight_group(int32_t n, const void* const* dy, const void* const* x,
+                                                 float* const* dw, int32_t tokens, const int32_t* in_features,
+                                                 const int32_t* out_features, void* stream) {
+    if (n < 1 || n > 16 || !dy || !x || !dw || !in_features || !out_features) return ZB_ERR_ARG;
+    if (!tokens_ok(tokens)) return ZB_ERR_SHAPE;
+    std::vector<GemmArgs> gs;
+    for (int i = 0; i < n; ++i) {
+        if (!feature_ok(in_features[i]) || !feature_ok(out_features[i])) return ZB_ERR_SHAPE;
+        if (!rows_ok(dy[i], tokens) || !rows_ok(x[i], tokens) || !fixed_ok(dw[i])) return ZB_ERR_ARG;
+        gs.push_back(wgrad_args(dy[i], x[i], dw[i], tokens, in_features[i], out_features[i]));
+    }
+    ZB_TRY(device_ok());
+    if (tokens == 0) return ZB_OK;
+    return cuda_status(zbk::launch_gemm_group(gs.data(), n, as_stream(stream)));
 }
 
 extern "C" size_t zb_op_rmsnorm_backward_gamma_scratch_bytes(int32_t tokens, int32_t hidden) {
@@ -800,14 +832,20 @@ zb_status stage_backward_weight_body(zb_stage* st, int slot, int t, cudaStream_t
     const double T = t;
     SplitWs ws;
     ZB_TRY(stage_split_ws(st, s, &ws));
-    auto wgrad = [&](const void* dyv, const void* xv, float* dw, int in, int out) {
-        return traced(st, ZB_KCLASS_GEMM_BACKWARD_WEIGHT, 1, gemm_flops(out, in, T), wgrad_bytes(out, in, T), s,
-                      [&] { return run_backward_weight(dyv, xv, dw, t, in, out, s, &ws); });
-    };
     if (c.kind == ZB_LAYER_LINEAR) {
         const LayerSlot& L = st->lay.layers[0];
-        return wgrad(st->at(slot, L.dy), st->at(slot, L.x), st->prm[0].dw, H, F);
+        return traced(st, ZB_KCLASS_GEMM_BACKWARD_WEIGHT, 1, gemm_flops(F, H, T), wgrad_bytes(F, H, T), s, [&] {
+            return run_backward_weight(st->at(slot, L.dy), st->at(slot, L.x), st->prm[0].dw, t, H, F, s, &ws);
+        });
     }
+    // Every weight gradient of the call, run as grouped launches: the GEMMs are
+    // independent, and one stream of tiles fills the last waves of the small
+    // ones with tiles of the others.
+    std::vector<GemmArgs> wg;
+    auto wgrad = [&](const void* dyv, const void* xv, float* dw, int in, int out) {
+        wg.push_back(wgrad_args(dyv, xv, dw, t, in, out));
+        return ZB_OK;
+    };
     float* scratch = reinterpret_cast<float*>(st->ws + st->lay.gamma_scratch);
     // Every RMSNorm gamma reduction of the call runs in one launch pair.
     std::vector<zbk::GammaProblem> gammas;
@@ -822,6 +860,17 @@ zb_status stage_backward_weight_body(zb_stage* st, int slot, int t, cudaStream_t
             ZB_TRY(wgrad(st->at(slot, L.dqkv), st->at(slot, L.n1), p.dw_qkv, H, Q));
             gammas.push_back({st->at(slot, L.dn1), st->at(slot, L.x), st->at<float>(slot, L.r1), p.dgamma1});
         }
+    }
+    for (size_t g0 = 0; g0 < wg.size(); g0 += zbk::kMaxGroup) {
+        const int n = static_cast<int>(std::min<size_t>(zbk::kMaxGroup, wg.size() - g0));
+        double fl = 0.0, by = 0.0;
+        for (int i = 0; i < n; ++i) {
+            const GemmArgs& g = wg[g0 + i];
+            fl += gemm_flops(g.m, g.n, g.k);
+            by += wgrad_bytes(g.m, g.n, g.k);
+        }
+        ZB_TRY(traced(st, ZB_KCLASS_GEMM_BACKWARD_WEIGHT, 1, fl, by, s,
+                      [&] { return cuda_status(zbk::launch_gemm_group(wg.data() + g0, n, s)); }));
     }
     for (size_t g0 = 0; g0 < gammas.size(); g0 += zbk::kMaxGammaProblems) {
         const int n = static_cast<int>(std::min<size_t>(zbk::kMaxGammaProblems, gammas.size() - g0));

@@ -29,7 +29,8 @@
 // blocks of 128 rows x 128 bytes (16 KiB each), as TMA writes them.  A tile
 // serves as a K-major operand (contraction over d) or, through another
 // descriptor, as an MN-major one (contraction over its 128 rows).  P and dS
-// are written from registers in the same layout.
+// stay in tensor memory: each row thread packs them to bf16 over the score
+// columns it has read, and the next product takes them as its A operand.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -43,7 +44,10 @@ namespace {
 
 constexpr int kAttnThreads = 192;
 constexpr int kRows = 128;             // query and key block
-constexpr uint32_t kPTile = 128 * 256;  // 128 x 128 bf16
+// Every attention CTA allocates all 512 tensor-memory columns; asking for at
+// least this much shared memory keeps two CTAs off one SM (the second would
+// wait in its allocation until the first ends).
+constexpr size_t kMinSmem = 120 * 1024;
 
 struct AttnParams {
     int tokens;
@@ -83,13 +87,6 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) {
     return smem_desc_sw128(tile + static_cast<uint32_t>(kk) * 2048u, 16384, 1024);
 }
 
-// Byte offset of element (row, col) in a swizzled tile (col 8-aligned: one 16 B chunk).
-__device__ __forceinline__ uint32_t swz_chunk(int row, int col) {
-    const int block = col >> 6;
-    const int chunk = ((col & 63) >> 3) ^ (row & 7);
-    return static_cast<uint32_t>(block * 16384 + row * 128 + chunk * 16);
-}
-
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -100,11 +97,6 @@ __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
 }
 
 // A wait taken by every lane of a warp, with one verdict for the warp (the
@@ -123,33 +115,37 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
 
 // ------------------------------------------------------------------------ forward
 
+// P is written, as packed bf16 pairs, over the tensor-memory columns of the
+// scores it came from, and O += P V takes it from there as its A operand; the
+// shared memory this frees holds a third K / V stage.
 template <int D>
 struct FwdSmem {
+    static constexpr int kStages = 3;
     static constexpr uint32_t kTile = D * 256;
     static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kKV = kTile;                 // stage s: K at kKV + 2 s kTile, V after it
-    static constexpr uint32_t kP = kKV + 4 * kTile;
-    static constexpr uint32_t kBars = kP + kPTile;
-    static constexpr size_t kBytes = 1024 + kBars + 16 * 8;
+    static constexpr uint32_t kKV = kTile;  // stage s: K at kKV + 2 s kTile, V after it
+    static constexpr uint32_t kBars = kKV + 2 * kStages * kTile;
+    static constexpr size_t kBytes = 1024 + kBars + 16 * 8 > kMinSmem ? 1024 + kBars + 16 * 8 : kMinSmem;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_causal_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const AttnParams p) {
     using L = FwdSmem<D>;
+    constexpr int NS = L::kStages;
     constexpr uint32_t kTile = L::kTile;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t s_q = base + L::kQ, s_kv = base + L::kKV, s_p = base + L::kP;
+    const uint32_t s_q = base + L::kQ, s_kv = base + L::kKV;
     const uint32_t bars = base + L::kBars;
     const uint32_t q_full = bars;
     auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto kv_empty = [&](int s) { return bars + 8u * (3 + s); };
-    auto s_full = [&](int s) { return bars + 8u * (5 + s); };
-    auto s_free = [&](int s) { return bars + 8u * (7 + s); };
-    const uint32_t p_full = bars + 8u * 9, p_free = bars + 8u * 10, drain = bars + 8u * 11;
-    const uint32_t tmem_slot = bars + 8u * 12;
+    auto kv_empty = [&](int s) { return bars + 8u * (1 + NS + s); };
+    auto s_full = [&](int s) { return bars + 8u * (1 + 2 * NS + s); };
+    const uint32_t p_full = bars + 8u * (3 + 2 * NS), p_free = bars + 8u * (4 + 2 * NS),
+                   drain = bars + 8u * (5 + 2 * NS);
+    const uint32_t tmem_slot = bars + 8u * (6 + 2 * NS);
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -165,12 +161,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
-            mbar_init(s_full(s), 1);
-            mbar_init(s_free(s), 128);
         }
+        for (int s = 0; s < 2; ++s) mbar_init(s_full(s), 1);
         mbar_init(p_full, 128);
         mbar_init(p_free, 1);
         mbar_init(drain, 1);
@@ -182,16 +177,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot_ptr;
-    const uint32_t t_o = tmem_base + 256;  // columns 0-255: two score buffers; 256..: O
+    // columns 0-255: two score buffers (P packed into the first 64 columns of
+    // its buffer once read); 256..: O
+    const uint32_t t_o = tmem_base + 256;
 
     if (warp == 0) {
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, kTile);
             load_tile<D>(s_q, &map_qkv, q_full, qcol, q0);
-            int issued[2] = {0, 0};
+            int issued[NS] = {};
             for (int j = 0; j < nk; ++j) {
-                const int st = j & 1;
-                if (!mbar_wait(kv_empty(st), ((j >> 1) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                const int st = j % NS;
+                if (!mbar_wait(kv_empty(st), ((j / NS) & 1) ^ 1u, p.status, kSiteAttn)) break;
                 mbar_arrive_expect_tx(kv_full(st), 2 * kTile);
                 const int k0 = (kb0 + j) * kRows;
                 load_tile<D>(s_kv + 2 * st * kTile, &map_qkv, kv_full(st), kcol, k0);
@@ -199,7 +196,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 ++issued[st];
             }
             mbar_wait(q_full, 0, p.status, kSiteDrain);
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < NS; ++s)
                 if (issued[s] > 0) mbar_wait(kv_full(s), (issued[s] - 1) & 1, p.status, kSiteDrain);
         }
     } else if (warp == 1) {
@@ -209,9 +206,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             bool ok = mbar_wait(q_full, 0, p.status, kSiteAttn);
             for (int j = 0; ok && j <= nk; ++j) {
                 if (j < nk) {
-                    const int st = j & 1;
-                    if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.status, kSiteAttn) ||
-                        !mbar_wait(s_free(st), ((j >> 1) & 1) ^ 1u, p.status, kSiteAttn)) {
+                    // S_j reuses the buffer of S_{j-2}, whose P feeds O += P V of
+                    // step j - 2: that product was issued before and runs first
+                    const int st = j % NS;
+                    if (!mbar_wait(kv_full(st), (j / NS) & 1, p.status, kSiteAttn)) {
                         ok = false;
                         break;
                     }
@@ -219,20 +217,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t k_tile = s_kv + 2 * st * kTile;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(tmem_base + st * 128, kdesc(s_q, kk), kdesc(k_tile, kk), idesc_s, kk > 0);
-                    umma_commit(s_full(st));
+                        umma_bf16(tmem_base + (j & 1) * 128, kdesc(s_q, kk), kdesc(k_tile, kk), idesc_s, kk > 0);
+                    umma_commit(s_full(j & 1));
                 }
                 if (j > 0) {
-                    const int jj = j - 1, st = jj & 1;
+                    const int jj = j - 1, st = jj % NS;
                     if (!mbar_wait(p_full, jj & 1, p.status, kSiteAttn)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t v_tile = s_kv + (2 * st + 1) * kTile;
+                    const uint32_t t_p = tmem_base + (jj & 1) * 128;
 #pragma unroll
                     for (int kk = 0; kk < kRows / 16; ++kk)
-                        umma_bf16(t_o, kdesc(s_p, kk), mndesc(v_tile, kk), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ts(t_o, t_p + 8 * kk, mndesc(v_tile, kk), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(kv_empty(st));
                     umma_commit(p_free);
                 }
@@ -264,8 +263,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(r[e]);
             }
-            tc_fence_before();
-            mbar_arrive(s_free(sb));
             const int k0 = (kb0 + j) * kRows;
             const int lim = min(q - k0, s1 - 1 - k0);  // last visible key column of this row
             float mx = -INFINITY;
@@ -298,24 +295,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
                     tmem_store_32(t_o + t_row + 32 * c, r);
                 }
-                tmem_wait_store();
                 m = m_new;
             }
             float sum = 0.f;
 #pragma unroll
-            for (int c8 = 0; c8 < 16; ++c8) {
-                uint32_t w[4];
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = ex2(s[8 * c8 + 2 * e] - m);
-                    const float b = ex2(s[8 * c8 + 2 * e + 1] - m);
+                for (int e = 0; e < 16; ++e) {
+                    const float a = ex2(s[32 * c + 2 * e] - m);
+                    const float b = ex2(s[32 * c + 2 * e + 1] - m);
                     sum += a + b;
                     w[e] = pack_bf16x2(a, b);
                 }
-                st_shared_v4(s_p + swz_chunk(row, 8 * c8), w[0], w[1], w[2], w[3]);
+                tmem_store_16(tmem_base + t_row + sb * 128 + 16 * c, w);
             }
             l += sum;
-            fence_proxy_async_smem();
+            tmem_wait_store();
             tc_fence_before();
             mbar_arrive(p_full);
         }
@@ -353,34 +349,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // ------------------------------------------------------------------------ backward: dq
 
+// Work runs in sub-blocks of 64 keys (two per loaded key tile), with two
+// tensor-memory buffers each for S and dP, so the row threads' pass over one
+// sub-block overlaps the tensor cores' work on its neighbours.  dS goes, as
+// packed bf16 pairs, over the buffer columns of S it came from; dQ += dS K
+// takes it from there as its A operand.
 template <int D>
 struct DqSmem {
     static constexpr uint32_t kTile = D * 256;
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kDO = kTile;
-    static constexpr uint32_t kKV = 2 * kTile;     // stage s: K at kKV + 2 s kTile, V after it
-    static constexpr uint32_t kDS = kKV + 4 * kTile;
-    static constexpr uint32_t kBars = kDS + kPTile;
-    static constexpr size_t kBytes = 1024 + kBars + 16 * 8;
+    static constexpr uint32_t kKV = 2 * kTile;  // stage s: K at kKV + 2 s kTile, V after it
+    static constexpr uint32_t kBars = kKV + 4 * kTile;
+    static constexpr size_t kBytes = 1024 + kBars + 16 * 8 > kMinSmem ? 1024 + kBars + 16 * 8 : kMinSmem;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_causal_dq_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
-                   const AttnParams p) {
+                          const AttnParams p) {
     using L = DqSmem<D>;
     constexpr uint32_t kTile = L::kTile;
+    constexpr uint32_t kHalfRows = 64 * 128;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t s_q = base + L::kQ, s_do = base + L::kDO, s_kv = base + L::kKV, s_ds = base + L::kDS;
+    const uint32_t s_q = base + L::kQ, s_do = base + L::kDO, s_kv = base + L::kKV;
     const uint32_t bars = base + L::kBars;
     const uint32_t q_full = bars;
     auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
     auto kv_empty = [&](int s) { return bars + 8u * (3 + s); };
-    const uint32_t sp_full = bars + 8u * 5, sp_free = bars + 8u * 6, ds_full = bars + 8u * 7,
-                   ds_free = bars + 8u * 8, drain = bars + 8u * 9;
-    const uint32_t tmem_slot = bars + 8u * 10;
+    auto sp_full = [&](int b) { return bars + 8u * (5 + b); };
+    auto ds_full = [&](int b) { return bars + 8u * (7 + b); };
+    const uint32_t done = bars + 8u * 9, drain = bars + 8u * 10;
+    const uint32_t tmem_slot = bars + 8u * 11;
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -392,6 +394,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     seq_bounds(p, q0, s0, s1);
     const int kb0 = s0 / kRows;
     const int nk = qb - kb0 + 1;
+    const int n_sub = 2 * nk;
     const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
 
     if (threadIdx.x == 0) {
@@ -399,11 +402,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
+            mbar_init(sp_full(s), 1);
+            mbar_init(ds_full(s), 128);
         }
-        mbar_init(sp_full, 1);
-        mbar_init(sp_free, 128);
-        mbar_init(ds_full, 128);
-        mbar_init(ds_free, 1);
+        mbar_init(done, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
         tma_prefetch_map(&map_qkv);
@@ -414,6 +416,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot_ptr;
+    // columns: S buffers 0-63 and 64-127 (dS packed into the first 32 of a
+    // buffer once read), dP buffers 128-191 and 192-255, dQ 256..
     const uint32_t t_s = tmem_base, t_dp = tmem_base + 128, t_dq = tmem_base + 256;
 
     if (warp == 0) {
@@ -437,31 +441,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 64, false, false);
             constexpr uint32_t idesc_q = mma_idesc_bf16(128, D, false, true);
             bool ok = mbar_wait(q_full, 0, p.status, kSiteAttn);
-            for (int j = 0; ok && j < nk; ++j) {
-                const int st = j & 1;
-                if (!mbar_wait(kv_full(st), (j >> 1) & 1, p.status, kSiteAttn) ||
-                    !mbar_wait(sp_free, (j & 1) ^ 1u, p.status, kSiteAttn))
-                    break;
-                tc_fence_after();
-                const uint32_t k_tile = s_kv + 2 * st * kTile, v_tile = k_tile + kTile;
+            for (int it = 0; ok && it <= n_sub; ++it) {
+                if (it < n_sub) {
+                    // S / dP of sub-block it reuse the buffers of it - 2, whose dS
+                    // feeds a product issued earlier, which runs first
+                    const int j = it >> 1, half = it & 1, st = j & 1;
+                    if (half == 0 && !mbar_wait(kv_full(st), (j >> 1) & 1, p.status, kSiteAttn)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t k_rows = s_kv + 2 * st * kTile + half * kHalfRows;
+                    const uint32_t v_rows = k_rows + kTile;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(t_s, kdesc(s_q, kk), kdesc(k_tile, kk), idesc_s, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_bf16(t_s + 64 * half, kdesc(s_q, kk), kdesc(k_rows, kk), idesc_s, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(t_dp, kdesc(s_do, kk), kdesc(v_tile, kk), idesc_s, kk > 0);
-                umma_commit(sp_full);
-                if (!mbar_wait(ds_full, j & 1, p.status, kSiteAttn)) break;
-                tc_fence_after();
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_bf16(t_dp + 64 * half, kdesc(s_do, kk), kdesc(v_rows, kk), idesc_s, kk > 0);
+                    umma_commit(sp_full(half));
+                }
+                if (it > 0) {
+                    const int pi = it - 1, j = pi >> 1, half = pi & 1, st = j & 1;
+                    if (!mbar_wait(ds_full(half), (pi >> 1) & 1, p.status, kSiteAttn)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t k_rows = s_kv + 2 * st * kTile + half * kHalfRows;
 #pragma unroll
-                for (int kk = 0; kk < kRows / 16; ++kk)
-                    umma_bf16(t_dq, kdesc(s_ds, kk), mndesc(k_tile, kk), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(kv_empty(st));
-                umma_commit(ds_free);
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16_ts(t_dq, t_s + 64 * half + 8 * kk, mndesc(k_rows, kk), idesc_q,
+                                     (pi > 0 || kk > 0) ? 1u : 0u);
+                    if (half == 1) umma_commit(kv_empty(st));
+                }
             }
+            umma_commit(done);
             umma_commit(drain);
             mbar_wait(drain, 0, p.status, kSiteDrain);
         }
@@ -474,47 +492,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float lse = valid ? p.lse[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
         const float dv = valid ? p.dvec[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
         bool ok = true;
-        for (int j = 0; j < nk; ++j) {
-            if (!warp_wait(sp_full, j & 1, p.status) || !warp_wait(ds_free, (j & 1) ^ 1u, p.status)) {
+        for (int it = 0; it < n_sub; ++it) {
+            const int half = it & 1;
+            if (!warp_wait(sp_full(half), (it >> 1) & 1, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int k0 = (kb0 + j) * kRows;
+            const int k0 = (kb0 + (it >> 1)) * kRows + 64 * half;
             const int lim = valid ? min(q - k0, s1 - 1 - k0) : -1;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t rs[32], rp[32];
-                tmem_load_32(t_s + t_row + 32 * c, rs);
-                tmem_load_32(t_dp + t_row + 32 * c, rp);
+                tmem_load_32(t_s + t_row + 64 * half + 32 * c, rs);
+                tmem_load_32(t_dp + t_row + 64 * half + 32 * c, rp);
                 tmem_wait_load();
-                if (c == 3) {
-                    tc_fence_before();
-                    mbar_arrive(sp_free);
-                }
+                uint32_t w[16];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint32_t w[4];
+                for (int e = 0; e < 16; ++e) {
+                    float ds2[2];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float ds2[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int i = 8 * c8 + 2 * e + u;
-                            const int col = 32 * c + i;
-                            const float pr = col <= lim ? ex2(__uint_as_float(rs[i]) * p.scale_log2 - lse) : 0.f;
-                            ds2[u] = pr * (__uint_as_float(rp[i]) - dv);
-                        }
-                        w[e] = pack_bf16x2(ds2[0], ds2[1]);
+                    for (int u = 0; u < 2; ++u) {
+                        const int i = 2 * e + u;
+                        const int col = 32 * c + i;
+                        const float pr = col <= lim ? ex2(__uint_as_float(rs[i]) * p.scale_log2 - lse) : 0.f;
+                        ds2[u] = pr * (__uint_as_float(rp[i]) - dv);
                     }
-                    st_shared_v4(s_ds + swz_chunk(row, 32 * c + 8 * c8), w[0], w[1], w[2], w[3]);
+                    w[e] = pack_bf16x2(ds2[0], ds2[1]);
                 }
+                // packed columns 16 c .. 16 c + 15 of the buffer lie in columns already read
+                tmem_store_16(t_s + t_row + 64 * half + 16 * c, w);
             }
-            fence_proxy_async_smem();
+            tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(ds_full);
+            mbar_arrive(ds_full(half));
         }
-        if (ok && warp_wait(ds_free, (nk - 1) & 1, p.status)) {
+        if (ok && warp_wait(done, 0, p.status)) {
             tc_fence_after();
             uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(q) * p.ld_out + h * D;
 #pragma unroll 1
@@ -546,37 +559,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // ------------------------------------------------------------------------ backward: dk, dv
 
+// Work runs in sub-blocks of 64 queries (two per loaded 128-query tile), with
+// two tensor-memory buffers each for S^T and dP^T: while the row threads turn
+// sub-block i into P^T and dS^T, the tensor cores compute S^T and dP^T of
+// sub-block i + 1 and the dV / dK updates of sub-block i - 1.  P^T and dS^T
+// never touch shared memory: each thread writes its key row of them, as packed
+// bf16 pairs, over the buffer columns it has just read, and the dV and dK
+// products take them as their A operand from tensor memory.  Shared memory
+// holds K, V and two query-side stages.
 template <int D>
 struct DkvSmem {
     static constexpr uint32_t kTile = D * 256;
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = kTile;
-    static constexpr uint32_t kQ = 2 * kTile;
-    static constexpr uint32_t kDO = 3 * kTile;
-    static constexpr uint32_t kPT = 4 * kTile;      // P^T
-    static constexpr uint32_t kDST = kPT + kPTile;  // dS^T
-    static constexpr uint32_t kStat = kDST + kPTile;  // lse and dvec of the 128 queries (1 KiB)
-    static constexpr uint32_t kBars = kStat + 1024;
-    static constexpr size_t kBytes = 1024 + kBars + 16 * 8;
+    static constexpr uint32_t kQD = 2 * kTile;          // stage s: Q at kQD + 2 s kTile, dO after it
+    static constexpr uint32_t kStat = kQD + 4 * kTile;  // stage s: lse then dvec of its 128 queries (1 KiB)
+    static constexpr uint32_t kBars = kStat + 2048;
+    static constexpr size_t kBytes = 1024 + kBars + 16 * 8 > kMinSmem ? 1024 + kBars + 16 * 8 : kMinSmem;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_causal_dkdv_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
-                     const AttnParams p) {
+                            const AttnParams p) {
     using L = DkvSmem<D>;
     constexpr uint32_t kTile = L::kTile;
+    constexpr uint32_t kHalfRows = 64 * 128;  // bytes of 64 rows inside a 64-column block of a tile
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t s_k = base + L::kK, s_v = base + L::kV, s_q = base + L::kQ, s_do = base + L::kDO;
-    const uint32_t s_pt = base + L::kPT, s_dst = base + L::kDST, s_stat = base + L::kStat;
-    const float* stat_lse = reinterpret_cast<const float*>(smem_raw + (s_stat - raw));
-    const float* stat_dv = stat_lse + 128;
+    const uint32_t s_k = base + L::kK, s_v = base + L::kV, s_qd = base + L::kQD, s_stat = base + L::kStat;
     const uint32_t bars = base + L::kBars;
-    const uint32_t kv_full = bars, qd_full = bars + 8, qd_empty = bars + 16, sp_full = bars + 24,
-                   sp_free = bars + 32, pd_full = bars + 40, pd_free = bars + 48, drain = bars + 56;
-    const uint32_t tmem_slot = bars + 64;
+    const uint32_t kv_full = bars;
+    auto qd_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto qd_empty = [&](int s) { return bars + 8u * (3 + s); };
+    auto sp_full = [&](int b) { return bars + 8u * (5 + b); };
+    auto pd_full = [&](int b) { return bars + 8u * (7 + b); };
+    const uint32_t done = bars + 8u * 9, drain = bars + 8u * 10;
+    const uint32_t tmem_slot = bars + 8u * 11;
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -587,17 +607,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     int s0, s1;
     seq_bounds(p, k0, s0, s1);
     const int qb_last = (s1 - 1) / kRows;
-    const int n_it = group * (qb_last - kb + 1);  // (query block, head of the group) pairs
+    const int n_tiles = group * (qb_last - kb + 1);  // (query block, head of the group) pairs
+    const int n_sub = 2 * n_tiles;
     const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        mbar_init(qd_full, 1);
-        mbar_init(qd_empty, 1);
-        mbar_init(sp_full, 1);
-        mbar_init(sp_free, 128);
-        mbar_init(pd_full, 128);
-        mbar_init(pd_free, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(qd_full(s), 1);
+            mbar_init(qd_empty(s), 1);
+            mbar_init(sp_full(s), 1);
+            mbar_init(pd_full(s), 128);
+        }
+        mbar_init(done, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
         tma_prefetch_map(&map_qkv);
@@ -608,6 +630,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot_ptr;
+    // columns: S^T buffers 0-63 and 64-127 (P^T packed into the first 32 of a
+    // buffer once read), dP^T buffers 128-191 and 192-255 (dS^T likewise),
+    // dV 256.., dK 256 + D..
     const uint32_t t_s = tmem_base, t_dp = tmem_base + 128, t_dv = tmem_base + 256, t_dk = tmem_base + 256 + D;
 
     if (warp == 0) {
@@ -615,49 +640,71 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_arrive_expect_tx(kv_full, 2 * kTile);
             load_tile<D>(s_k, &map_qkv, kv_full, kcol, k0);
             load_tile<D>(s_v, &map_qkv, kv_full, vcol, k0);
-            int issued = 0;
-            for (int it = 0; it < n_it; ++it) {
+            int issued[2] = {0, 0};
+            for (int it = 0; it < n_tiles; ++it) {
+                const int st = it & 1;
                 const int qb = kb + it / group;
                 const int h = g * group + it % group;
-                if (!mbar_wait(qd_empty, (it & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(qd_full, 2 * kTile + 1024);
-                load_tile<D>(s_q, &map_qkv, qd_full, h * D, qb * kRows);
-                load_tile<D>(s_do, &map_do, qd_full, h * D, qb * kRows);
-                bulk_load_1d(s_stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + qb * kRows, 512, qd_full);
-                bulk_load_1d(s_stat + 512, p.dvec + static_cast<int64_t>(h) * p.ld_stat + qb * kRows, 512, qd_full);
-                ++issued;
+                if (!mbar_wait(qd_empty(st), ((it >> 1) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(qd_full(st), 2 * kTile + 1024);
+                const uint32_t q_tile = s_qd + 2 * st * kTile;
+                load_tile<D>(q_tile, &map_qkv, qd_full(st), h * D, qb * kRows);
+                load_tile<D>(q_tile + kTile, &map_do, qd_full(st), h * D, qb * kRows);
+                const uint32_t stat = s_stat + 1024u * st;
+                bulk_load_1d(stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + qb * kRows, 512, qd_full(st));
+                bulk_load_1d(stat + 512, p.dvec + static_cast<int64_t>(h) * p.ld_stat + qb * kRows, 512, qd_full(st));
+                ++issued[st];
             }
             mbar_wait(kv_full, 0, p.status, kSiteDrain);
-            if (issued > 0) mbar_wait(qd_full, (issued - 1) & 1, p.status, kSiteDrain);
+            for (int s = 0; s < 2; ++s)
+                if (issued[s] > 0) mbar_wait(qd_full(s), (issued[s] - 1) & 1, p.status, kSiteDrain);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 64, false, false);
             constexpr uint32_t idesc_g = mma_idesc_bf16(128, D, false, true);
             bool ok = mbar_wait(kv_full, 0, p.status, kSiteAttn);
-            for (int it = 0; ok && it < n_it; ++it) {
-                if (!mbar_wait(qd_full, it & 1, p.status, kSiteAttn) ||
-                    !mbar_wait(sp_free, (it & 1) ^ 1u, p.status, kSiteAttn))
-                    break;
-                tc_fence_after();
+            for (int it = 0; ok && it <= n_sub; ++it) {
+                if (it < n_sub) {
+                    // S^T / dP^T of sub-block it reuse the buffers of it - 2, whose
+                    // P^T / dS^T feed products issued earlier, which run first
+                    const int tile = it >> 1, half = it & 1, st = tile & 1;
+                    if (half == 0 && !mbar_wait(qd_full(st), (tile >> 1) & 1, p.status, kSiteAttn)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t q_rows = s_qd + 2 * st * kTile + half * kHalfRows;
+                    const uint32_t do_rows = q_rows + kTile;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(t_s, kdesc(s_k, kk), kdesc(s_q, kk), idesc_s, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_bf16(t_s + 64 * half, kdesc(s_k, kk), kdesc(q_rows, kk), idesc_s, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(t_dp, kdesc(s_v, kk), kdesc(s_do, kk), idesc_s, kk > 0);
-                umma_commit(sp_full);
-                if (!mbar_wait(pd_full, it & 1, p.status, kSiteAttn)) break;
-                tc_fence_after();
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_bf16(t_dp + 64 * half, kdesc(s_v, kk), kdesc(do_rows, kk), idesc_s, kk > 0);
+                    umma_commit(sp_full(half));
+                }
+                if (it > 0) {
+                    const int pi = it - 1, tile = pi >> 1, half = pi & 1, st = tile & 1;
+                    if (!mbar_wait(pd_full(half), (pi >> 1) & 1, p.status, kSiteAttn)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t q_rows = s_qd + 2 * st * kTile + half * kHalfRows;
+                    const uint32_t do_rows = q_rows + kTile;
 #pragma unroll
-                for (int kk = 0; kk < kRows / 16; ++kk)
-                    umma_bf16(t_dv, kdesc(s_pt, kk), mndesc(s_do, kk), idesc_g, (it > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16_ts(t_dv, t_s + 64 * half + 8 * kk, mndesc(do_rows, kk), idesc_g,
+                                     (pi > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < kRows / 16; ++kk)
-                    umma_bf16(t_dk, kdesc(s_dst, kk), mndesc(s_q, kk), idesc_g, (it > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(qd_empty);
-                umma_commit(pd_free);
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16_ts(t_dk, t_dp + 64 * half + 8 * kk, mndesc(q_rows, kk), idesc_g,
+                                     (pi > 0 || kk > 0) ? 1u : 0u);
+                    if (half == 1) umma_commit(qd_empty(st));
+                }
             }
+            umma_commit(done);
             umma_commit(drain);
             mbar_wait(drain, 0, p.status, kSiteDrain);
         }
@@ -668,56 +715,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int k = k0 + row;
         const uint32_t t_row = static_cast<uint32_t>(qw * 32) << 16;
         bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int q0 = (kb + it / group) * kRows;
-            if (!warp_wait(qd_full, it & 1, p.status) || !warp_wait(sp_full, it & 1, p.status) ||
-                !warp_wait(pd_free, (it & 1) ^ 1u, p.status)) {
+        for (int it = 0; it < n_sub; ++it) {
+            const int tile = it >> 1, half = it & 1, st = tile & 1;
+            const int q0 = (kb + tile / group) * kRows + 64 * half;
+            if ((half == 0 && !warp_wait(qd_full(st), (tile >> 1) & 1, p.status)) ||
+                !warp_wait(sp_full(half), (it >> 1) & 1, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const float* stat_lse = reinterpret_cast<const float*>(smem_raw + (s_stat + 1024u * st - raw)) + 64 * half;
+            const float* stat_dv = stat_lse + 128;
             // query column c is visible to this key when k <= q0 + c < s1
             const int first = k - q0;
             const int last = s1 - 1 - q0;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t rs[32], rp[32];
-                tmem_load_32(t_s + t_row + 32 * c, rs);
-                tmem_load_32(t_dp + t_row + 32 * c, rp);
+                tmem_load_32(t_s + t_row + 64 * half + 32 * c, rs);
+                tmem_load_32(t_dp + t_row + 64 * half + 32 * c, rp);
                 tmem_wait_load();
-                if (c == 3) {
-                    tc_fence_before();
-                    mbar_arrive(sp_free);
-                }
+                uint32_t wp[16], wd[16];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint32_t wp[4], wd[4];
+                for (int e = 0; e < 16; ++e) {
+                    float pv[2], dsv[2];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float pv[2], dsv[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int i = 8 * c8 + 2 * e + u;
-                            const int col = 32 * c + i;
-                            const bool vis = col >= first && col <= last;
-                            // statistics past the sequence end are not written: never read them into a value
-                            const float pr = vis ? ex2(__uint_as_float(rs[i]) * p.scale_log2 - stat_lse[col]) : 0.f;
-                            pv[u] = pr;
-                            dsv[u] = vis ? pr * (__uint_as_float(rp[i]) - stat_dv[col]) : 0.f;
-                        }
-                        wp[e] = pack_bf16x2(pv[0], pv[1]);
-                        wd[e] = pack_bf16x2(dsv[0], dsv[1]);
+                    for (int u = 0; u < 2; ++u) {
+                        const int i = 2 * e + u;
+                        const int col = 32 * c + i;
+                        const bool vis = col >= first && col <= last;
+                        // statistics past the sequence end are not written: never read them into a value
+                        const float pr = vis ? ex2(__uint_as_float(rs[i]) * p.scale_log2 - stat_lse[col]) : 0.f;
+                        pv[u] = pr;
+                        dsv[u] = vis ? pr * (__uint_as_float(rp[i]) - stat_dv[col]) : 0.f;
                     }
-                    const uint32_t off = swz_chunk(row, 32 * c + 8 * c8);
-                    st_shared_v4(s_pt + off, wp[0], wp[1], wp[2], wp[3]);
-                    st_shared_v4(s_dst + off, wd[0], wd[1], wd[2], wd[3]);
+                    wp[e] = pack_bf16x2(pv[0], pv[1]);
+                    wd[e] = pack_bf16x2(dsv[0], dsv[1]);
                 }
+                // packed columns 16 c .. 16 c + 15 of the buffer lie in columns already read
+                tmem_store_16(t_s + t_row + 64 * half + 16 * c, wp);
+                tmem_store_16(t_dp + t_row + 64 * half + 16 * c, wd);
             }
-            fence_proxy_async_smem();
+            tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(pd_full);
+            mbar_arrive(pd_full(half));
         }
-        if (ok && n_it > 0 && warp_wait(pd_free, (n_it - 1) & 1, p.status)) {
+        if (ok && warp_wait(done, 0, p.status)) {
             tc_fence_after();
             const bool valid = k < s1;
             uint16_t* dk_dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(k) * p.ld_out + kcol;

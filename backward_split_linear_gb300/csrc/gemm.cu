@@ -109,6 +109,23 @@ __device__ __forceinline__ Unit unit_of(const KParams& p, int u) {
     return w;
 }
 
+// A CTA-pair launch: up to kMaxGroup independent GEMMs of the same operand
+// layouts and epilogue, run as one stream of work units (problem after
+// problem), so that the last wave of one fills with the first tiles of the
+// next.  A single GEMM is a group of one.
+struct PairGroup {
+    CUtensorMap map[2 * kMaxGroup];  // A and B of each problem
+    KParams kp[kMaxGroup];
+    int unit_begin[kMaxGroup + 1];   // first work unit of each problem; the last entry is the total
+    int n_probs;
+};
+
+__device__ __forceinline__ int problem_of(const PairGroup& G, int u) {
+    int pi = 0;
+    while (pi + 1 < G.n_probs && u >= G.unit_begin[pi + 1]) ++pi;
+    return pi;
+}
+
 // Tile index -> (tile row, tile column) under the grouped raster.
 __device__ __forceinline__ void tile_coords(const KParams& p, int tile, int& tm, int& tn) {
     if (p.group_m) {
@@ -418,8 +435,10 @@ static_assert(kPairSmemBytes <= 232448, "shared memory");
 
 template <bool A_MN, bool B_MN, int EPI, int NACC, bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                     const KParams p) {
+    gemm_pair_kernel(const __grid_constant__ PairGroup G) {
+    int* const status = G.kp[0].status;
+    const uint32_t mn_lbo = G.kp[0].mn_lbo, mn_sbo = G.kp[0].mn_sbo;
+    const int num_units = G.unit_begin[G.n_probs];
     constexpr uint32_t kTmemCols = NACC * kPairN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -453,8 +472,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(drain_bar, 1);
         mbar_fence_init();
-        tma_prefetch_map(&map_a);
-        tma_prefetch_map(&map_b);
+        for (int i = 0; i < 2 * G.n_probs; ++i) tma_prefetch_map(&G.map[i]);
     }
     if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -464,7 +482,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Both CTAs must hold the accumulator at the same columns.
     const uint32_t peer_base = ld_shared_cluster_u32(map_to_cta(tmem_slot, rank ^ 1u));
     const bool usable = peer_base == tmem_base;
-    if (!usable && threadIdx.x == 0) atomicCAS(p.status, 0, kSitePairTmem);
+    if (!usable && threadIdx.x == 0) atomicCAS(status, 0, kSitePairTmem);
 
     if (usable && warp == 0) {
         if (lane == 0) {
@@ -474,14 +492,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int u = pair; ok && u < p.num_units; u += npairs) {
-                const Unit w = unit_of<SPLIT>(p, u);
+            for (int u = pair; ok && u < num_units; u += npairs) {
+                const int pi = problem_of(G, u);
+                const KParams& p = G.kp[pi];
+                const Unit w = unit_of<SPLIT>(p, u - G.unit_begin[pi]);
                 int tm, tn;
                 tile_coords(p, w.tile, tm, tn);
                 const int m0 = tm * kPairM + static_cast<int>(rank) * kHalf;
                 const int n0 = tn * kPairN + static_cast<int>(rank) * kHalf;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, p.status, kSiteProducerEmpty)) {
+                    if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, status, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
@@ -494,16 +514,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if constexpr (A_MN) {
 #pragma unroll
                         for (int j = 0; j < kHalf / 64; ++j)
-                            tma_load_2d_pair(a_dst + j * kMnBlockBytes, &map_a, fb, m0 + 64 * j, k0);
+                            tma_load_2d_pair(a_dst + j * kMnBlockBytes, &G.map[2 * pi], fb, m0 + 64 * j, k0);
                     } else {
-                        tma_load_2d_pair(a_dst, &map_a, fb, k0, m0);
+                        tma_load_2d_pair(a_dst, &G.map[2 * pi], fb, k0, m0);
                     }
                     if constexpr (B_MN) {
 #pragma unroll
                         for (int j = 0; j < kHalf / 64; ++j)
-                            tma_load_2d_pair(b_dst + j * kMnBlockBytes, &map_b, fb, n0 + 64 * j, k0);
+                            tma_load_2d_pair(b_dst + j * kMnBlockBytes, &G.map[2 * pi + 1], fb, n0 + 64 * j, k0);
                     } else {
-                        tma_load_2d_pair(b_dst, &map_b, fb, k0, n0);
+                        tma_load_2d_pair(b_dst, &G.map[2 * pi + 1], fb, k0, n0);
                     }
                     ++issued[stage];
                     if (++stage == kPairStages) {
@@ -517,9 +537,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kPairStages; ++s)
                 if (issued[s] > 0) {
                     if (leader)
-                        mbar_wait_cluster(full_bar(s), (issued[s] - 1u) & 1u, p.status, kSiteDrain, kWaitLimitNs);
+                        mbar_wait_cluster(full_bar(s), (issued[s] - 1u) & 1u, status, kSiteDrain, kWaitLimitNs);
                     else
-                        mbar_wait_cluster(empty_bar(s), (issued[s] - 1u) & 1u, p.status, kSiteDrain, kWaitLimitNs);
+                        mbar_wait_cluster(empty_bar(s), (issued[s] - 1u) & 1u, status, kSiteDrain, kWaitLimitNs);
                 }
         }
     } else if (usable && warp == 1) {
@@ -530,15 +550,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int u = pair; ok && u < p.num_units; u += npairs, ++it) {
-                const Unit w = unit_of<SPLIT>(p, u);
+            for (int u = pair; ok && u < num_units; u += npairs, ++it) {
+                const int pi = problem_of(G, u);
+                const KParams& p = G.kp[pi];
+                const Unit w = unit_of<SPLIT>(p, u - G.unit_begin[pi]);
                 const int acc = it % NACC;
                 const uint32_t aph = static_cast<uint32_t>(it / NACC) & 1u;
-                if (!mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, p.status, kSiteMmaTmemEmpty)) break;
+                if (!mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, status, kSiteMmaTmemEmpty)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait_cluster(full_bar(stage), phase, p.status, kSiteMmaFull)) {
+                    if (!mbar_wait_cluster(full_bar(stage), phase, status, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
@@ -547,9 +569,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t b0 = s_b + stage * kPairBStage;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, p.mn_lbo, p.mn_sbo)
+                        const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, mn_lbo, mn_sbo)
                                                  : smem_desc_sw128(a0 + k * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, p.mn_lbo, p.mn_sbo)
+                        const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, mn_lbo, mn_sbo)
                                                  : smem_desc_sw128(b0 + k * 32, 16, 1024);
                         umma_bf16_pair(d, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
                     }
@@ -563,19 +585,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 umma_commit_pair(tfull_bar(acc), 0x3);
             }
             umma_commit_pair(drain_bar, 0x1);
-            mbar_wait(drain_bar, 0, p.status, kSiteDrain, kWaitLimitNs);
+            mbar_wait(drain_bar, 0, status, kSiteDrain, kWaitLimitNs);
         }
     } else if (usable && warp >= 2) {
         // ---------------- epilogue (both CTAs): warp w reads lanes 32 (w % 4) .. +31
         const int q = warp & 3;
         const int row = q * 32 + lane;
         int it = 0;
-        for (int u = pair; u < p.num_units; u += npairs, ++it) {
-            const Unit w = unit_of<SPLIT>(p, u);
+        for (int u = pair; u < num_units; u += npairs, ++it) {
+            const int pi = problem_of(G, u);
+                const KParams& p = G.kp[pi];
+                const Unit w = unit_of<SPLIT>(p, u - G.unit_begin[pi]);
             const int acc = it % NACC;
             const uint32_t aph = static_cast<uint32_t>(it / NACC) & 1u;
             // one verdict per warp: the tensor-memory loads below are warp-wide
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(tfull_bar(acc), aph, p.status, kSiteEpiTmemFull)))
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(tfull_bar(acc), aph, status, kSiteEpiTmemFull)))
                 break;
             tc_fence_after();
             int tm, tn;
@@ -609,7 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 store_partial = old != claimed && old != claimed + 1u;
                 if (old == claimed) {
                     int ready = 1;
-                    if (lane == 0) ready = wait_value(flag, claimed + 1u, p.status, kSiteSplitFlag) ? 1 : 0;
+                    if (lane == 0) ready = wait_value(flag, claimed + 1u, status, kSiteSplitFlag) ? 1 : 0;
                     give_up = __shfl_sync(0xffffffffu, ready, 0) == 0;
                 }
                 __syncwarp();  // the partial rows read below come after lane 0's acquire
@@ -736,9 +760,10 @@ cudaError_t launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const K
 // kernel checks this and reports kSitePairTmem otherwise).
 constexpr int kPairAccums = 2;
 
+static_assert(sizeof(PairGroup) <= 32000, "kernel parameter space");
+
 template <bool A_MN, bool B_MN, int EPI, bool SPLIT>
-cudaError_t launch_pair_split_variant(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& p,
-                                      cudaStream_t stream) {
+cudaError_t launch_pair_split_variant(const PairGroup& G, cudaStream_t stream) {
     auto kern = gemm_pair_kernel<A_MN, B_MN, EPI, kPairAccums, SPLIT>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -755,16 +780,16 @@ cudaError_t launch_pair_split_variant(const CUtensorMap& ma, const CUtensorMap& 
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-    const int pairs = p.num_units < max_clusters ? p.num_units : max_clusters;
-    kern<<<2 * pairs, kThreads, kPairSmemBytes, stream>>>(ma, mb, p);
+    const int units = G.unit_begin[G.n_probs];
+    const int pairs = units < max_clusters ? units : max_clusters;
+    kern<<<2 * pairs, kThreads, kPairSmemBytes, stream>>>(G);
     return cudaGetLastError();
 }
 
 template <bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_pair_variant(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& p,
-                                cudaStream_t stream) {
-    return p.split == 2 ? launch_pair_split_variant<A_MN, B_MN, EPI, true>(ma, mb, p, stream)
-                        : launch_pair_split_variant<A_MN, B_MN, EPI, false>(ma, mb, p, stream);
+cudaError_t launch_pair_variant(const PairGroup& G, cudaStream_t stream) {
+    return G.kp[0].split == 2 ? launch_pair_split_variant<A_MN, B_MN, EPI, true>(G, stream)
+                              : launch_pair_split_variant<A_MN, B_MN, EPI, false>(G, stream);
 }
 
 // DRAM bytes a raster fetches, modelled wave by wave: a wave reads the A
@@ -871,23 +896,22 @@ cudaError_t dispatch(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMap
     return cudaErrorInvalidValue;
 }
 
-cudaError_t dispatch_pair(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMap& mb, KParams& p,
-                          cudaStream_t stream) {
+cudaError_t dispatch_pair(const GemmArgs& g, const PairGroup& G, cudaStream_t stream) {
     constexpr int kStore = static_cast<int>(Epilogue::StoreBf16);
     constexpr int kResid = static_cast<int>(Epilogue::AddResidual);
     constexpr int kSwiglu = static_cast<int>(Epilogue::SwigluBwd);
     constexpr int kAccum = static_cast<int>(Epilogue::AccumF32);
     switch (g.kind) {
         case GemmKind::Forward:
-            if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, false, kStore>(ma, mb, p, stream);
-            if (g.epi == Epilogue::AddResidual) return launch_pair_variant<false, false, kResid>(ma, mb, p, stream);
+            if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, false, kStore>(G, stream);
+            if (g.epi == Epilogue::AddResidual) return launch_pair_variant<false, false, kResid>(G, stream);
             break;
         case GemmKind::BackwardInput:
-            if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, true, kStore>(ma, mb, p, stream);
-            if (g.epi == Epilogue::SwigluBwd) return launch_pair_variant<false, true, kSwiglu>(ma, mb, p, stream);
+            if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, true, kStore>(G, stream);
+            if (g.epi == Epilogue::SwigluBwd) return launch_pair_variant<false, true, kSwiglu>(G, stream);
             break;
         case GemmKind::BackwardWeight:
-            if (g.epi == Epilogue::AccumF32) return launch_pair_variant<true, true, kAccum>(ma, mb, p, stream);
+            if (g.epi == Epilogue::AccumF32) return launch_pair_variant<true, true, kAccum>(G, stream);
             break;
     }
     return cudaErrorInvalidValue;
@@ -929,15 +953,18 @@ std::atomic<uint32_t> g_split_epoch{0};
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
-    if (g.m <= 0 || g.n <= 0 || g.k <= 0) return cudaSuccess;
+namespace {
+
+// Tensor maps and kernel parameters of one GEMM; `pair` says which kernel
+// takes it.  A K split is considered only when `allow_split`.
+cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtensorMap& mb, KParams& p,
+                    bool& pair) {
     const int sms = sm_count();
     // A CTA pair takes 256 x 256 tiles; small outputs keep the one-CTA kernel.
-    const bool pair = g.m >= kPairM && g.n >= kPairN;
+    pair = g.m >= kPairM && g.n >= kPairN;
     const int tile_m = pair ? kPairM : BM;
     const int tile_n = pair ? kPairN : kBN;
     const uint32_t b_rows = pair ? kHalf : kBN;  // rows of a K-major B box
-    CUtensorMap ma, mb;
     bool ok = true;
     switch (g.kind) {
         case GemmKind::Forward:
@@ -951,7 +978,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
             break;
     }
     if (!ok) return cudaErrorInvalidValue;
-    KParams p{};
+    p = KParams{};
     p.m = g.m;
     p.n = g.n;
     p.k = g.k;
@@ -968,8 +995,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     // the extra partial-tile traffic and the shorter pipelines than the fuller
     // last wave won: 4096 x 4096 outputs with K = 4096 ran at 1071 TFLOP/s
     // split against 1279 unsplit, while K = 28672 went from 1477 to 1587.
-    if (pair && g.split_flags && g.split_partial && p.k_blocks >= 256 && p.num_tiles <= g.split_tiles &&
-        p.num_tiles <= kSplitMaxTiles) {
+    if (allow_split && pair && g.split_flags && g.split_partial && p.k_blocks >= 256 &&
+        p.num_tiles <= g.split_tiles && p.num_tiles <= kSplitMaxTiles) {
         const int pairs = pair_max_clusters();
         if (pairs > 0 && fill(2 * p.num_tiles, pairs) > 1.08 * fill(p.num_tiles, pairs)) {
             p.split = 2;
@@ -993,7 +1020,53 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     p.mn_lbo = kMnBlockBytes;
     p.mn_sbo = 1024;
     if (!p.status) return cudaErrorInvalidDevice;
-    return pair ? dispatch_pair(g, ma, mb, p, stream) : dispatch<kBN>(g, ma, mb, p, stream);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
+    if (g.m <= 0 || g.n <= 0 || g.k <= 0) return cudaSuccess;
+    CUtensorMap ma, mb;
+    KParams p;
+    bool pair = false;
+    const cudaError_t e = prepare(g, true, ma, mb, p, pair);
+    if (e != cudaSuccess) return e;
+    if (!pair) return dispatch<kBN>(g, ma, mb, p, stream);
+    PairGroup G;
+    G.map[0] = ma;
+    G.map[1] = mb;
+    G.kp[0] = p;
+    G.unit_begin[0] = 0;
+    G.unit_begin[1] = p.num_units;
+    G.n_probs = 1;
+    return dispatch_pair(g, G, stream);
+}
+
+cudaError_t launch_gemm_group(const GemmArgs* gs, int n, cudaStream_t stream) {
+    // One grouped launch when every GEMM takes the CTA-pair kernel with the
+    // same layouts and epilogue; otherwise one launch each.
+    bool grouped = n > 1 && n <= kMaxGroup;
+    for (int i = 0; grouped && i < n; ++i)
+        grouped = gs[i].m >= kPairM && gs[i].n >= kPairN && gs[i].k > 0 && gs[i].kind == gs[0].kind &&
+                  gs[i].epi == gs[0].epi;
+    if (!grouped) {
+        for (int i = 0; i < n; ++i) {
+            const cudaError_t e = launch_gemm(gs[i], stream);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    PairGroup G;
+    G.unit_begin[0] = 0;
+    for (int i = 0; i < n; ++i) {
+        bool pair = false;
+        const cudaError_t e = prepare(gs[i], false, G.map[2 * i], G.map[2 * i + 1], G.kp[i], pair);
+        if (e != cudaSuccess) return e;
+        G.unit_begin[i + 1] = G.unit_begin[i] + G.kp[i].num_units;
+    }
+    G.n_probs = n;
+    return dispatch_pair(gs[0], G, stream);
 }
 
 }  // namespace zbk

@@ -57,6 +57,12 @@ constexpr int kSplitMaxTiles = 512;
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
 
+// Up to kMaxGroup independent GEMMs in one launch when they all take the
+// CTA-pair kernel with the same layouts and epilogue (else one launch each).
+// Their outputs must not overlap.  Grouped GEMMs never split K.
+constexpr int kMaxGroup = 16;
+cudaError_t launch_gemm_group(const GemmArgs* gs, int n, cudaStream_t stream);
+
 cudaError_t launch_rmsnorm_forward(const void* x, const float* gamma, float eps, void* n,
                                    float* rstd, int tokens, int hidden, cudaStream_t stream);
 cudaError_t launch_rmsnorm_backward_input(const void* dn, const void* x, const float* rstd,

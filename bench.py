@@ -127,12 +127,13 @@ def read_ncu_csv(paths):
     return [launches[k] for k in sorted(launches)]
 
 
-def summarize_ncu(path, command, title):
+def summarize_ncu(path, command, title, bw_flops=None):
     """Markdown summary of an ncu CSV: launches, time and share per kernel; DRAM bytes if captured.
 
-    When DRAM bytes are present, a closing line gives the mean DRAM bytes per launch of the
-    B and W GEMMs with the sha256 of the GEMM sources; bench.py reports it as the roofline's
-    traffic while the sources are unchanged."""
+    When DRAM bytes are present and `bw_flops` (the algorithmic FLOPs of the captured B and W
+    GEMM launches) is given, closing lines give the B/W GEMMs' DRAM bytes per FLOP with the
+    sha256 of the GEMM sources; bench.py scales it by its own FLOPs per launch to report the
+    roofline's traffic while the sources are unchanged."""
     rows = {}
     for name, met in read_ncu_csv(path):
         r = rows.setdefault(kernel_label(name), {"n": 0, "s": 0.0, "rd": 0.0, "wr": 0.0})
@@ -154,18 +155,18 @@ def summarize_ncu(path, command, title):
         out.append(line)
     out.append(f"| **total** | {sum(r['n'] for r in rows.values())} | {1e3 * total:.2f} | 100 % |" +
                (" | |" if dram else ""))
-    if dram:
+    if dram and bw_flops:
         bw = [r for label, r in rows.items() if label.startswith("gemm") and (" B (" in label or " W (" in label)]
-        n = sum(r["n"] for r in bw)
-        if n:
-            per = sum(r["rd"] + r["wr"] for r in bw) / n
-            out += ["", f"gemm_bw_dram_bytes_per_launch: {per:.0f}", f"gemm_source_sha256: {gemm_source_sha()}"]
+        total = sum(r["rd"] + r["wr"] for r in bw)
+        if total:
+            out += ["", f"gemm_bw_dram_bytes_per_flop: {total / bw_flops:.6e}",
+                    f"gemm_source_sha256: {gemm_source_sha()}"]
     return "\n".join(out) + "\n"
 
 
 def profiled_gemm_traffic(workload, w_mode):
-    """DRAM bytes per B/W GEMM launch from the committed ncu summary of this workload, or None
-    when there is none or the GEMM sources changed since it was taken."""
+    """DRAM bytes per algorithmic FLOP of the B/W GEMMs from the committed ncu summary of this
+    workload, or None when there is none or the GEMM sources changed since it was taken."""
     if w_mode != "per-microbatch":
         return None, "no capture for this W mode"
     path = os.path.join(ROOT, "profiles", f"gemm_traffic_{workload}.md")
@@ -176,12 +177,12 @@ def profiled_gemm_traffic(workload, w_mode):
         return None, "no capture"
     vals = {}
     for line in text.splitlines():
-        if ":" in line and line.split(":")[0] in ("gemm_bw_dram_bytes_per_launch", "gemm_source_sha256"):
+        if ":" in line and line.split(":")[0] in ("gemm_bw_dram_bytes_per_flop", "gemm_source_sha256"):
             k, v = line.split(":", 1)
             vals[k] = v.strip()
-    if vals.get("gemm_source_sha256") != gemm_source_sha() or "gemm_bw_dram_bytes_per_launch" not in vals:
+    if vals.get("gemm_source_sha256") != gemm_source_sha() or "gemm_bw_dram_bytes_per_flop" not in vals:
         return None, "GEMM sources changed since the capture"
-    return float(vals["gemm_bw_dram_bytes_per_launch"]), f"profiles/gemm_traffic_{workload}.md"
+    return float(vals["gemm_bw_dram_bytes_per_flop"]), f"profiles/gemm_traffic_{workload}.md"
 
 
 def measured_peaks():
@@ -492,13 +493,15 @@ def run_ours(args, w):
                "note": "B+W GEMM FLOPs over the whole step: H2D of x and dy, F, B, W, D2H of dx"}
 
     peaks = measured_peaks()
-    traffic, traffic_src = profiled_gemm_traffic(args.workload, args.w_mode) if not args.overridden else (
+    bytes_per_flop, traffic_src = profiled_gemm_traffic(args.workload, args.w_mode) if not args.overridden else (
         None, "workload overridden")
     gemm = {k: trace[k] for k in ("gemm_backward_input", "gemm_backward_weight")}
     g_ms = sum(c["ms"] for c in gemm.values())
     g_launch = sum(c["launches"] for c in gemm.values())
     g_flops = sum(c["flops"] for c in gemm.values())
     g_ach = g_flops / (g_ms * 1e-3) / 1e12
+    # DRAM bytes of an average B/W GEMM launch: the captured bytes per FLOP times this run's FLOPs per launch
+    traffic = bytes_per_flop * g_flops / max(1, g_launch) if bytes_per_flop else None
     rows = {k: trace[k] for k in ("row_backward_input", "row_backward_weight")}
     r_ms = sum(c["ms"] for c in rows.values())
     r_bytes = sum(c["bytes"] for c in rows.values())
@@ -679,9 +682,10 @@ def main():
     ap.add_argument("--summarize-ncu", metavar="CSV[,CSV...]", help="print a markdown summary of ncu --csv logs")
     ap.add_argument("--ncu-command", default="", help="the command that wrote the CSV (for the summary)")
     ap.add_argument("--title", default="ncu launch list")
+    ap.add_argument("--bw-flops", type=float, help="algorithmic FLOPs of the B/W GEMM launches in the CSV")
     args = ap.parse_args()
     if args.summarize_ncu:
-        sys.stdout.write(summarize_ncu(args.summarize_ncu, args.ncu_command, args.title))
+        sys.stdout.write(summarize_ncu(args.summarize_ncu, args.ncu_command, args.title, args.bw_flops))
         return 0
     if args.op:
         return run_op(args)

@@ -193,6 +193,17 @@ zb_status zb_op_backward_weight(const void* dy, const void* x, float* dw,
                                 int32_t tokens, int32_t in_features,
                                 int32_t out_features, void* stream);
 
+/* W of n (1..16) linears over the same tokens in one launch, [G1]: for each i,
+ * dw[i][out_i, in_i] (float32) += dy[i][T, out_i]^T x[i][T, in_i].  The arrays
+ * are host arrays of device pointers and sizes.  The products are independent
+ * (outputs must not overlap), so one stream of output tiles serves them all and
+ * the last wave of each fills with tiles of the others.  Each dw element gets
+ * one float32 add per call, in the same order as from zb_op_backward_weight, so
+ * the results are the same bits as n separate calls. */
+zb_status zb_op_backward_weight_group(int32_t n, const void* const* dy, const void* const* x,
+                                      float* const* dw, int32_t tokens, const int32_t* in_features,
+                                      const int32_t* out_features, void* stream);
+
 /* W of an RMSNorm weight: dgamma[H] (float32) += sum_t dn[t,:] * x[t,:] * rstd[t].
  * Two passes in a fixed order (per-block partial sums in `scratch`, then one
  * ordered sum), so results are bitwise reproducible.  `scratch` is device

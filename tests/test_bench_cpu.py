@@ -33,12 +33,12 @@ def test_summary_shares_and_gemm_traffic(tmp_path):
         lines.append(row(i, name, "dram__bytes_read.sum", "Mbyte", rd_mb))
         lines.append(row(i, name, "dram__bytes_write.sum", "byte", int(wr_mb * 1e6)))
     csv.write_text("".join(lines))
-    text = bench.summarize_ncu(str(csv), "ncu ... python bench.py", "t")
+    text = bench.summarize_ncu(str(csv), "ncu ... python bench.py", "t", bw_flops=4.6e9)
     assert "| gemm_pair_kernel W (float32 red.add epilogue) | 1 | 0.60 | 60.0 % | 30.0 | 40.0 |" in text
     assert "| rmsnorm_bwd_kernel<2> | 1 | 0.10 | 10.0 % |" in text
     assert "| **total** | 4 | 1.00 | 100 % |" in text
-    # B and W GEMM launches only: (20 + 2 + 30 + 40) MB over 2 launches
-    assert "gemm_bw_dram_bytes_per_launch: 46000000" in text
+    # B and W GEMM launches only: (20 + 2 + 30 + 40) MB over 4.6 GFLOP
+    assert "gemm_bw_dram_bytes_per_flop: 2.000000e-02" in text
     assert f"gemm_source_sha256: {bench.gemm_source_sha()}" in text
 
 
@@ -48,10 +48,10 @@ def test_traffic_lookup_needs_matching_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "gemm_source_sha", lambda: "abc")
     assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] is None
-    (prof / "gemm_traffic_w.md").write_text("x\ngemm_bw_dram_bytes_per_launch: 123\ngemm_source_sha256: abc\n")
-    assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] == 123.0
+    (prof / "gemm_traffic_w.md").write_text("x\ngemm_bw_dram_bytes_per_flop: 1.5e-4\ngemm_source_sha256: abc\n")
+    assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] == 1.5e-4
     assert bench.profiled_gemm_traffic("w", "flush")[0] is None
-    (prof / "gemm_traffic_w.md").write_text("gemm_bw_dram_bytes_per_launch: 123\ngemm_source_sha256: old\n")
+    (prof / "gemm_traffic_w.md").write_text("gemm_bw_dram_bytes_per_flop: 1.5e-4\ngemm_source_sha256: old\n")
     assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] is None
 
 
@@ -64,6 +64,6 @@ def test_summary_of_several_logs(tmp_path):
                        row(0, W, "dram__bytes_read.sum", "byte", "2000000") +
                        row(0, W, "dram__bytes_write.sum", "byte", "0"))
         paths.append(str(csv))
-    text = bench.summarize_ncu(",".join(paths), "cmd", "t")
+    text = bench.summarize_ncu(",".join(paths), "cmd", "t", bw_flops=1e9)
     assert "| gemm_pair_kernel W (float32 red.add epilogue) | 2 | 0.00 | 100.0 % | 2.0 | 0.0 |" in text
-    assert "gemm_bw_dram_bytes_per_launch: 2000000" in text
+    assert "gemm_bw_dram_bytes_per_flop: 4.000000e-03" in text

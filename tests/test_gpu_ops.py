@@ -79,6 +79,29 @@ def test_backward_weight_accumulates(t_list, n_in, n_out):
     assert_close(dw.cpu().numpy(), ref["w"], "backward weight")
 
 
+@pytest.mark.parametrize("shapes", [[(512, 768), (320, 1024), (1024, 256), (640, 640)],
+                                    [(256, 512), (64, 128), (512, 256)]])
+def test_backward_weight_group_equals_separate_calls(shapes):
+    """One grouped W launch gives the same bits as one call per linear (onto non-zero
+    accumulators); the second case has an output too small for the CTA-pair kernel, so the
+    group runs as separate launches."""
+    t = 700
+    rng = np.random.default_rng(77)
+    dys, xs, acc0 = [], [], []
+    for n_in, n_out in shapes:
+        dys.append(bf16_from_bits(draw_bf16(rng, (t, n_out))[0]))
+        xs.append(bf16_from_bits(draw_bf16(rng, (t, n_in))[0]))
+        acc0.append(f32(rng.standard_normal((n_out, n_in))))
+    grouped = [a.clone() for a in acc0]
+    zb.zb_op_backward_weight_group(dys, xs, grouped, t, [s[0] for s in shapes], [s[1] for s in shapes])
+    for i, (n_in, n_out) in enumerate(shapes):
+        single = acc0[i].clone()
+        zb.zb_op_backward_weight(dys[i], xs[i], single, t, n_in, n_out)
+        assert torch.equal(grouped[i], single), shapes[i]
+        ref = acc0[i].double().cpu().numpy() + (f64_from_bf16(dys[i]).T @ f64_from_bf16(xs[i]))
+        assert_close(grouped[i].cpu().numpy(), ref, f"grouped dW {shapes[i]}")
+
+
 def test_backward_weight_bitwise_reproducible():
     rng = np.random.default_rng(5)
     xb, _ = draw_bf16(rng, (777, 384))
