@@ -76,15 +76,18 @@ __device__ __forceinline__ void seq_bounds(const AttnParams& p, int t0, int& s0,
 
 // K-major operand from a tile whose rows are the M (or N) index and whose
 // columns are the contraction: step kk covers columns 16 kk .. 16 kk + 15.
-__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) {
-    return smem_desc_sw128(tile + static_cast<uint32_t>(kk >> 2) * 16384u + static_cast<uint32_t>(kk & 3) * 32u,
-                           16, 1024);
+// The descriptor of step kk is the tile's descriptor plus the step's byte
+// offset / 16 in its start-address field, so callers build the base once.
+__device__ __forceinline__ uint64_t kdesc_base(uint32_t tile) { return smem_desc_sw128(tile, 16, 1024); }
+__device__ __forceinline__ uint64_t kdesc_at(uint64_t base, int kk) {
+    return base + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
 }
 
 // MN-major operand from the same kind of tile: the contraction runs over its
 // 128 rows (step kk = rows 16 kk .. +15), the MN index over its columns.
-__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) {
-    return smem_desc_sw128(tile + static_cast<uint32_t>(kk) * 2048u, 16384, 1024);
+__device__ __forceinline__ uint64_t mndesc_base(uint32_t tile) { return smem_desc_sw128(tile, 16384, 1024); }
+__device__ __forceinline__ uint64_t mndesc_at(uint64_t base, int kk) {
+    return base + static_cast<uint64_t>((kk * 2048) >> 4);
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -214,10 +217,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t k_tile = s_kv + 2 * st * kTile;
+                    const uint64_t a_desc = kdesc_base(s_q), b_desc = kdesc_base(s_kv + 2 * st * kTile);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(tmem_base + (j & 1) * 128, kdesc(s_q, kk), kdesc(k_tile, kk), idesc_s, kk > 0);
+                        umma_bf16(tmem_base + (j & 1) * 128, kdesc_at(a_desc, kk), kdesc_at(b_desc, kk), idesc_s,
+                                  kk > 0);
                     umma_commit(s_full(j & 1));
                 }
                 if (j > 0) {
@@ -227,11 +231,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t v_tile = s_kv + (2 * st + 1) * kTile;
+                    const uint64_t v_desc = mndesc_base(s_kv + (2 * st + 1) * kTile);
                     const uint32_t t_p = tmem_base + (jj & 1) * 128;
 #pragma unroll
                     for (int kk = 0; kk < kRows / 16; ++kk)
-                        umma_bf16_ts(t_o, t_p + 8 * kk, mndesc(v_tile, kk), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ts(t_o, t_p + 8 * kk, mndesc_at(v_desc, kk), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(kv_empty(st));
                     umma_commit(p_free);
                 }
@@ -455,13 +459,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t k_rows = s_kv + 2 * st * kTile + half * kHalfRows;
-                    const uint32_t v_rows = k_rows + kTile;
+                    const uint64_t q_desc = kdesc_base(s_q), do_desc = kdesc_base(s_do);
+                    const uint64_t k_desc = kdesc_base(k_rows), v_desc = kdesc_base(k_rows + kTile);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_s + 64 * half, kdesc(s_q, kk), kdesc(k_rows, kk), idesc_s, kk > 0);
+                        umma_bf16(t_s + 64 * half, kdesc_at(q_desc, kk), kdesc_at(k_desc, kk), idesc_s, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_dp + 64 * half, kdesc(s_do, kk), kdesc(v_rows, kk), idesc_s, kk > 0);
+                        umma_bf16(t_dp + 64 * half, kdesc_at(do_desc, kk), kdesc_at(v_desc, kk), idesc_s, kk > 0);
                     umma_commit(sp_full(half));
                 }
                 if (it > 0) {
@@ -471,10 +476,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t k_rows = s_kv + 2 * st * kTile + half * kHalfRows;
+                    const uint64_t k_desc = mndesc_base(s_kv + 2 * st * kTile + half * kHalfRows);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ts(t_dq, t_s + 64 * half + 8 * kk, mndesc(k_rows, kk), idesc_q,
+                        umma_bf16_ts(t_dq, t_s + 64 * half + 8 * kk, mndesc_at(k_desc, kk), idesc_q,
                                      (pi > 0 || kk > 0) ? 1u : 0u);
                     if (half == 1) umma_commit(kv_empty(st));
                 }
@@ -675,13 +680,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t q_rows = s_qd + 2 * st * kTile + half * kHalfRows;
-                    const uint32_t do_rows = q_rows + kTile;
+                    const uint64_t k_desc = kdesc_base(s_k), v_desc = kdesc_base(s_v);
+                    const uint64_t q_desc = kdesc_base(q_rows), do_desc = kdesc_base(q_rows + kTile);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_s + 64 * half, kdesc(s_k, kk), kdesc(q_rows, kk), idesc_s, kk > 0);
+                        umma_bf16(t_s + 64 * half, kdesc_at(k_desc, kk), kdesc_at(q_desc, kk), idesc_s, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_dp + 64 * half, kdesc(s_v, kk), kdesc(do_rows, kk), idesc_s, kk > 0);
+                        umma_bf16(t_dp + 64 * half, kdesc_at(v_desc, kk), kdesc_at(do_desc, kk), idesc_s, kk > 0);
                     umma_commit(sp_full(half));
                 }
                 if (it > 0) {
@@ -692,14 +698,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t q_rows = s_qd + 2 * st * kTile + half * kHalfRows;
-                    const uint32_t do_rows = q_rows + kTile;
+                    const uint64_t q_desc = mndesc_base(q_rows), do_desc = mndesc_base(q_rows + kTile);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ts(t_dv, t_s + 64 * half + 8 * kk, mndesc(do_rows, kk), idesc_g,
+                        umma_bf16_ts(t_dv, t_s + 64 * half + 8 * kk, mndesc_at(do_desc, kk), idesc_g,
                                      (pi > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ts(t_dk, t_dp + 64 * half + 8 * kk, mndesc(q_rows, kk), idesc_g,
+                        umma_bf16_ts(t_dk, t_dp + 64 * half + 8 * kk, mndesc_at(q_desc, kk), idesc_g,
                                      (pi > 0 || kk > 0) ? 1u : 0u);
                     if (half == 1) umma_commit(qd_empty(st));
                 }
