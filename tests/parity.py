@@ -11,6 +11,15 @@ path and four on the backward path, so errors grow like the square root of
 the number of chained steps.  Whole-stage comparisons against the exact
 float64 oracle therefore use Frobenius <= 5e-3 * sqrt(4 L) for L layers
 (1e-2 for one layer, 2e-2 for four), and keep max-abs <= 2e-2 * max|ref|.
+
+A layer with the causal softmax core adds roundings on both paths (P for the
+P V and dV products, the bf16 output a, dS) and the exponential amplifies the
+rounding of q and k.  tests/bf16_emulation.py replays the causal 8B-shaped
+two-layer stage with every stored tensor rounded: Frobenius up to 1.61e-2
+(top layer's dW_qkv) and max-abs up to 1.94e-2 (its dgamma1); the GPU gives
+1.59e-2 and 1.70e-2 there.  Causal stages therefore count eight roundings a
+layer: Frobenius <= 5e-3 * sqrt(8 L) (2e-2 for two layers) and max-abs
+<= 3e-2 * max|ref|.
 """
 import numpy as np
 
@@ -18,8 +27,15 @@ FRO_TOL = 5e-3
 MAX_TOL = 2e-2
 
 
+CAUSAL_MAX_TOL = 3e-2
+
+
 def stage_fro_tol(n_layers):
     return FRO_TOL * float(np.sqrt(4 * n_layers))
+
+
+def causal_stage_fro_tol(n_layers):
+    return FRO_TOL * float(np.sqrt(8 * n_layers))
 
 
 def errors(got, ref):

@@ -15,7 +15,7 @@ from backward_split_linear_gb300 import binding as zb
 from backward_split_linear_gb300 import synth
 from backward_split_linear_gb300.runtime import Stage, bf16_from_bits, f64_from_bf16
 from oracle import stage as S
-from parity import MAX_TOL, assert_close, draw_bf16, stage_fro_tol
+from parity import CAUSAL_MAX_TOL, assert_close, causal_stage_fro_tol, draw_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -157,7 +157,7 @@ CAUSAL_TF = dict(kind="transformer", n_layers=2, hidden=256, ffn=512, n_heads=4,
 @pytest.mark.parametrize("seq_len,tokens", [(0, [300, 128]), (128, [384, 200])])
 def test_causal_stage_against_oracle(seq_len, tokens):
     """A two-layer stage with the causal attention core: F -> B -> W per microbatch,
-    dx and every weight gradient against the oracle at the two-layer stage tolerance."""
+    dx and every weight gradient against the oracle at the causal two-layer stage tolerance."""
     c = CAUSAL_TF
     inp = synth.stage_inputs(c["kind"], 2, 256, 512, 4, 2, 64, n_mb=len(tokens), seed=21, tokens_per_mb=tokens)
     st = Stage.from_synth(c["kind"], 2, 256, 512, 4, 2, 64, 1e-5, max(tokens), len(tokens), inp["params"],
@@ -176,9 +176,40 @@ def test_causal_stage_against_oracle(seq_len, tokens):
         orc.forward(i, synth.bf16_to_f64(xb))
         ref_dx = orc.backward_input(i, synth.bf16_to_f64(dyb))
         orc.backward_weight(i)
-        assert_close(f64_from_bf16(dx), ref_dx, f"dx[{i}]", fro_tol=stage_fro_tol(2), max_tol=MAX_TOL)
+        assert_close(f64_from_bf16(dx), ref_dx, f"dx[{i}]", fro_tol=causal_stage_fro_tol(2), max_tol=CAUSAL_MAX_TOL)
     st.sync()
     for li in range(2):
         for k, ref in orc.grads[li].items():
-            assert_close(st.grads[li][k].cpu().numpy(), ref, f"layer {li} d{k}", fro_tol=stage_fro_tol(2))
+            assert_close(st.grads[li][k].cpu().numpy(), ref, f"layer {li} d{k}", fro_tol=causal_stage_fro_tol(2),
+                         max_tol=CAUSAL_MAX_TOL)
+    st.close()
+
+
+def test_causal_stage_8b_shaped():
+    """Two 8B-shaped layers (hidden 4096, ffn 14336, 32 heads on 8 kv heads, d = 128) with the
+    causal core: two microbatches of 256 tokens in sequences of 128, F -> B -> W each, against
+    the oracle at the causal two-layer stage tolerance (the oracle follows every token)."""
+    c = dict(kind="transformer", n_layers=2, hidden=4096, ffn=14336, n_heads=32, n_kv_heads=8, head_dim=128)
+    tokens = [256, 256]
+    inp = synth.stage_inputs(c["kind"], 2, 4096, 14336, 32, 8, 128, n_mb=2, seed=23, tokens_per_mb=tokens)
+    st = Stage.from_synth(c["kind"], 2, 4096, 14336, 32, 8, 128, 1e-5, 256, 2, inp["params"],
+                          attention="causal", seq_len=128)
+    orc = S.StageOracle(synth.params_f64(inp["params"]), dict(c, eps=1e-5, attention="causal", seq_len=128))
+    for i, (xb, dyb) in enumerate(zip(inp["x"], inp["dy"])):
+        x, dy = bf16_from_bits(xb), bf16_from_bits(dyb)
+        y = torch.empty(256, 4096, dtype=torch.bfloat16, device="cuda")
+        dx = torch.empty_like(y)
+        st.forward(i, x, y)
+        st.backward_input(i, dy, dx)
+        orc.forward(i, synth.bf16_to_f64(xb))
+        ref_dx = orc.backward_input(i, synth.bf16_to_f64(dyb))
+        assert_close(f64_from_bf16(dx), ref_dx, f"dx[{i}]", fro_tol=causal_stage_fro_tol(2), max_tol=CAUSAL_MAX_TOL)
+    st.flush()  # both W in one batched call
+    st.sync()
+    orc.backward_weight(0)
+    orc.backward_weight(1)
+    for li in range(2):
+        for k, ref in orc.grads[li].items():
+            assert_close(st.grads[li][k].cpu().numpy(), ref, f"layer {li} d{k}", fro_tol=causal_stage_fro_tol(2),
+                         max_tol=CAUSAL_MAX_TOL)
     st.close()
