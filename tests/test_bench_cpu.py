@@ -67,3 +67,23 @@ def test_summary_of_several_logs(tmp_path):
     text = bench.summarize_ncu(",".join(paths), "cmd", "t", bw_flops=1e9)
     assert "| gemm_pair_kernel W (float32 red.add epilogue) | 2 | 0.00 | 100.0 % | 2.0 | 0.0 |" in text
     assert "gemm_bw_dram_bytes_per_flop: 4.000000e-03" in text
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the float64 oracle on the host cores) prints one JSON line
+    with the contract's keys, on the same metric and unit as the GPU arm."""
+    import json
+    import subprocess
+    import sys
+
+    out = subprocess.run([sys.executable, bench.__file__, "--impl", "reference", "--workload", "tiny_stage",
+                          "--steps", "1", "--warmup", "0"], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["higher_is_better"] is True and d["value"] > 0 and d["steps"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "tiny_stage"
