@@ -678,11 +678,13 @@ zb_status check_layer_params(const zb_stage_config& c, const zb_layer_params& p)
     return ZB_ERR_ARG;
 }
 
-// Stash copy of a caller tensor (x at F, dy at B), booked with F's or B's row kernels.
+// Stash copy of a caller tensor (x at F, dy at B), booked with F's or B's row
+// kernels: its time and bytes count, but not as a launch (it is a copy, not one
+// of the library's kernels).
 zb_status stash_copy(zb_stage* st, zb_kernel_class cls, void* dst, const void* src, size_t bytes,
                      cudaStream_t s) {
     if (!bytes) return ZB_OK;
-    return traced(st, cls, 1, 0.0, 2.0 * bytes, s, [&] {
+    return traced(st, cls, 0, 0.0, 2.0 * bytes, s, [&] {
         return cuda_status(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s));
     });
 }

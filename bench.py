@@ -416,6 +416,13 @@ def run_ours(args, w):
         return spans
 
     st.set_tracing(True)
+    # stash bytes one microbatch holds between its F and its W
+    st.forward(0, xs[0], ys[0], stream)
+    stash_per_mb = st.stats()[2]
+    dys0 = torch.empty_like(dxs[0])
+    st.backward_input(0, dys[0], dys0, stream)
+    st.backward_weight(0, stream)
+    st.sync()
     for _ in range(args.warmup):
         step(False)
     st.sync()
@@ -566,6 +573,15 @@ def run_ours(args, w):
             search["by_memory_limit"][mem] = {"ceiling": limit, "makespan_ms": span / 1e3,
                                               "bubble_over_wall": (span - work) / span}
         line["schedule_search"] = search
+        if args.w_mode != "flush":
+            # the order the step ran: its held microbatches and the unit-time model of the whole pipeline
+            pipe = args.pipeline or m
+            inflight, peak, _ = st.stats()
+            span, over_compute, over_wall = zb.zb_schedule_bubble("zbh1", pipe, m)
+            line["order_stats"] = {"stage": args.stage, "p": pipe, "m": m, "peak_inflight": peak,
+                                   "stash_bytes_per_microbatch": stash_per_mb,
+                                   "unit_model": {"makespan": span, "bubble_over_compute": over_compute,
+                                                  "bubble_over_wall": over_wall}}
         if w.get("attention") == "causal":
             # the attention core's own work: not in the metric (which counts the linears), reported beside it
             af, ab = trace["attn_forward"], trace["attn_backward"]

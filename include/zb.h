@@ -418,7 +418,7 @@ typedef enum {
 } zb_kernel_class;
 
 typedef struct {
-    int32_t launches;  /* kernels (or copies) launched */
+    int32_t launches;  /* kernels of the library launched (stash copies count time and bytes, not launches) */
     int32_t pad;
     double ms;         /* summed event time */
     double flops;      /* algorithmic FLOPs */
