@@ -115,7 +115,7 @@ __device__ __forceinline__ Unit unit_of(const KParams& p, int u) {
 // next.  A single GEMM is a group of one.
 struct PairGroup {
     CUtensorMap map[2 * kMaxGroup];   // A and B of each problem
-    CUtensorMap omap[kMaxGroup];      // output of each problem (plain and residual bf16 epilogues)
+    CUtensorMap omap[kMaxGroup];      // output of each problem (all epilogues but the SwiGLU backward)
     KParams kp[kMaxGroup];
     int unit_begin[kMaxGroup + 1];   // first work unit of each problem; the last entry is the total
     int n_probs;
@@ -224,21 +224,35 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int m, int n, c
 }
 
 // Output staging of the CTA-pair kernel: each epilogue warp writes a chunk of
-// its 32 rows x 32 columns (64 bytes a row) into a shared-memory box laid out
-// as the 64-byte TMA swizzle expects (16-byte word j of row r sits at word
-// j ^ ((r >> 1) & 3)), so eight consecutive rows fill all banks; one lane then
-// stores the box with a TMA bulk-tensor copy.
-constexpr uint32_t kOutBoxBytes = 32 * 64;
+// its 32 rows x 32 columns into a shared-memory box and one lane hands the box
+// to a TMA bulk-tensor store (bf16) or reduce-add (float32).  A bf16 row is 64
+// bytes and takes the 64-byte TMA swizzle (16-byte word j of row r at word
+// j ^ ((r >> 1) & 3)); a float32 row is 128 bytes and takes the 128-byte
+// swizzle (word j of row r at word j ^ (r & 7)).  Either way eight
+// consecutive rows cover all banks.
+template <int EPI>
+__host__ __device__ constexpr uint32_t out_box_bytes() {
+    return EPI == static_cast<int>(Epilogue::AccumF32) ? 32 * 128 : 32 * 64;
+}
 
 template <int EPI>
 __device__ __forceinline__ void epilogue_chunk_to_smem(uint32_t box, int lane, const uint32_t (&r)[32],
                                                        const uint4 (&x0)[4]) {
-    uint4 o0[4], unused[4];
-    epilogue_pack<EPI>(r, x0, x0, o0, unused);
-    const uint32_t row = box + static_cast<uint32_t>(lane) * 64u;
-    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+    const uint32_t l = static_cast<uint32_t>(lane);
+    if constexpr (EPI == static_cast<int>(Epilogue::AccumF32)) {
+        const uint32_t row = box + l * 128u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) st_shared_v4(row + ((static_cast<uint32_t>(j) ^ sw) << 4), o0[j]);
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(row + ((static_cast<uint32_t>(j) ^ (l & 7u)) << 4),
+                         make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]));
+    } else {
+        uint4 o0[4], unused[4];
+        epilogue_pack<EPI>(r, x0, x0, o0, unused);
+        const uint32_t row = box + l * 64u;
+        const uint32_t sw = (l >> 1) & 3u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_shared_v4(row + ((static_cast<uint32_t>(j) ^ sw) << 4), o0[j]);
+    }
 }
 
 template <int BN, bool A_MN, bool B_MN, int EPI>
@@ -467,22 +481,24 @@ constexpr uint32_t kPairStage = kPairAStage + kPairBStage;
 constexpr int kPairNumBars = 2 * kPairStages + 5;
 // bf16 outputs of the plain and residual epilogues leave through staging boxes
 // and TMA stores (4.2 % faster for a 4096 x 14336 dgrad, 4.9 % for a
-// 4096 x 28672 forward on GB300).  The SwiGLU backward keeps direct stores:
-// its epilogue is bound by the latency of each chunk, and the extra fence and
-// warp synchronisation made it 2 % slower.  The float32 accumulation keeps
-// red.global.add, where the L2 does the read-modify-write.
+// 4096 x 28672 forward on GB300), and the float32 weight-gradient sums through
+// TMA reduce-adds, where the L2 does the read-modify-write.  The SwiGLU
+// backward keeps direct stores: its epilogue is bound by the latency of each
+// chunk, and the extra fence and warp synchronisation made it 2 % slower.
 template <int EPI>
 __host__ __device__ constexpr bool tma_out() {
-    return EPI == static_cast<int>(Epilogue::StoreBf16) || EPI == static_cast<int>(Epilogue::AddResidual);
+    return EPI != static_cast<int>(Epilogue::SwigluBwd);
 }
 // Output staging: per epilogue warp two boxes, used in turn.
-constexpr uint32_t kPairOutWarpBytes = 2 * kOutBoxBytes;
-constexpr uint32_t kPairOutBytes = 4 * kPairOutWarpBytes;  // 16 KiB
+template <int EPI>
+__host__ __device__ constexpr uint32_t pair_out_bytes() {
+    return tma_out<EPI>() ? 4 * 2 * out_box_bytes<EPI>() : 0;
+}
 template <int EPI>
 __host__ __device__ constexpr size_t pair_smem_bytes() {
-    return 1024 + kPairStages * kPairStage + (tma_out<EPI>() ? kPairOutBytes : 0) + kPairNumBars * 8 + 16;
+    return 1024 + kPairStages * kPairStage + pair_out_bytes<EPI>() + kPairNumBars * 8 + 16;
 }
-static_assert(pair_smem_bytes<static_cast<int>(Epilogue::StoreBf16)>() <= 232448, "shared memory");
+static_assert(pair_smem_bytes<static_cast<int>(Epilogue::AccumF32)>() <= 232448, "shared memory");
 
 template <bool A_MN, bool B_MN, int EPI, int NACC, bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -498,7 +514,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t s_b = base + kPairStages * kPairAStage;
     constexpr bool kTmaOut = tma_out<EPI>();
     const uint32_t s_out = s_b + kPairStages * kPairBStage;  // 2 KiB-aligned boxes
-    const uint32_t bars = s_out + (kTmaOut ? kPairOutBytes : 0u);
+    constexpr uint32_t kBoxBytes = out_box_bytes<EPI>();
+    const uint32_t bars = s_out + pair_out_bytes<EPI>();
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (kPairStages + s); };
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * kPairStages + a); };
@@ -646,7 +663,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---------------- epilogue (both CTAs): warp w reads lanes 32 (w % 4) .. +31
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        const uint32_t out_stage = s_out + static_cast<uint32_t>(q) * kPairOutWarpBytes;
+        const uint32_t out_stage = s_out + static_cast<uint32_t>(q) * 2u * kBoxBytes;
         uint32_t n_stored = 0;  // staged chunks this warp has handed to TMA stores
         int it = 0;
         for (int u = pair; u < num_units; u += npairs, ++it) {
@@ -752,14 +769,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // that read it, two chunks back, has finished reading.
                     const int row0 = tm * kPairM + static_cast<int>(rank) * kHalf + q * 32;
                     if (!give_up && row0 < p.m && n < p.n) {
-                        const uint32_t box = out_stage + (n_stored & 1u) * kOutBoxBytes;
+                        const uint32_t box = out_stage + (n_stored & 1u) * kBoxBytes;
                         if (lane == 0) bulk_wait_group_read<1>();
                         __syncwarp();
                         if (ok) epilogue_chunk_to_smem<EPI>(box, lane, r, x0);
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&G.omap[pi], box, n, row0);
+                            if constexpr (EPI == static_cast<int>(Epilogue::AccumF32))
+                                tma_reduce_add_2d(&G.omap[pi], box, n, row0);
+                            else
+                                tma_store_2d(&G.omap[pi], box, n, row0);
                             bulk_commit_group();
                         }
                         ++n_stored;
@@ -808,16 +828,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // descriptors; output boxes (32 x 32) the 64-byte swizzle of the staging boxes.
 bool encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
                 uint32_t box_cols, uint32_t box_rows,
-                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) return false;
+    const cuuint64_t esize = dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, bool A_MN, bool B_MN, int EPI>
@@ -1064,9 +1085,12 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
             ok = encode_map(&ma, g.a, g.k, g.m, g.lda, 64, BK) && encode_map(&mb, g.b, g.k, g.n, g.ldb, 64, BK);
             break;
     }
-    // Output of the CTA-pair kernel's TMA-store epilogues.
+    // Output of the CTA-pair kernel's TMA stores (bf16) and reduce-adds (float32).
     if (ok && pair && (g.epi == Epilogue::StoreBf16 || g.epi == Epilogue::AddResidual))
         ok = encode_map(&mo, g.out, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (ok && pair && g.epi == Epilogue::AccumF32)
+        ok = encode_map(&mo, g.out, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
     if (!ok) return cudaErrorInvalidValue;
     p = KParams{};
     p.m = g.m;
