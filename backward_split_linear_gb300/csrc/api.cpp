@@ -549,8 +549,8 @@ Layout make_layout(const zb_stage_config& c) {
         L.gamma_scratch = total;
         total += round_up(L.gamma_scratch_bytes);
     }
-    // K-split scratch for the largest GEMM output of the stage, up to the
-    // largest launch that may split.
+    // K-split scratch for the split tiles of one launch: no more than the
+    // tiles of the stage's largest GEMM output, nor than kSplitMaxTiles.
     {
         const int64_t Tt = static_cast<int64_t>(c.max_tokens);
         auto tiles = [](int64_t m, int64_t n) { return ((m + 255) / 256) * ((n + 255) / 256); };

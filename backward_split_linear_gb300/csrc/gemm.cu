@@ -77,34 +77,41 @@ struct KParams {
     // 64-element MN blocks, the stride-dimension offset between 8-row K groups.
     uint32_t mn_lbo;
     uint32_t mn_sbo;
-    // K split (CTA-pair kernel only): split == 2 makes two work units per tile,
-    // unit 2t + h covering k-blocks [0, kb_split) for h = 0 and
-    // [kb_split, k_blocks) for h = 1; split == 1 is one unit per tile.
+    // K split of the last wave (CTA-pair kernel only): tiles from split_from on
+    // are two work units each, unit split_from + 2 (t - split_from) + h
+    // covering k-blocks [0, kb_split) for h = 0 and [kb_split, k_blocks) for
+    // h = 1; earlier tiles are one unit each.  split == 1: no tile splits
+    // (split_from == num_tiles).
     int split;
+    int split_from;
     int kb_split;
     int num_units;
-    uint32_t* flags;   // one word per 32 rows of a tile: 2 epoch (claimed), 2 epoch + 1 (partial written)
-    float* partial;    // one float32 256 x 256 tile per output tile
+    uint32_t* flags;   // one word per 32 rows of a split tile: 2 epoch (claimed), 2 epoch + 1 (partial written)
+    float* partial;    // one float32 256 x 256 tile per split tile
     uint32_t epoch;
 };
 
 struct Unit {
     int tile, half, kb0, kb1;
+    bool split;  // one of the two K halves of a split tile
 };
 
 template <bool SPLIT>
 __device__ __forceinline__ Unit unit_of(const KParams& p, int u) {
     Unit w;
-    if (SPLIT) {
-        w.tile = u >> 1;
-        w.half = u & 1;
+    if (SPLIT && u >= p.split_from) {
+        const int v = u - p.split_from;
+        w.tile = p.split_from + (v >> 1);
+        w.half = v & 1;
         w.kb0 = w.half ? p.kb_split : 0;
         w.kb1 = w.half ? p.k_blocks : p.kb_split;
+        w.split = true;
     } else {
         w.tile = u;
         w.half = 0;
         w.kb0 = 0;
         w.kb1 = p.k_blocks;
+        w.split = false;
     }
     return w;
 }
@@ -695,11 +702,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool store_partial = false;
             bool give_up = false;
             uint32_t* flag = nullptr;
+            const size_t split_slot = SPLIT && w.split ? static_cast<size_t>(w.tile - p.split_from) : 0;
             const float* prow =
-                SPLIT ? p.partial + (static_cast<size_t>(w.tile) * kPairM + static_cast<size_t>(trow)) * kPairN
-                      : nullptr;
-            if constexpr (SPLIT) {
-                flag = p.flags + static_cast<size_t>(w.tile) * 8 + rank * 4 + static_cast<uint32_t>(q);
+                SPLIT && w.split ? p.partial + (split_slot * kPairM + static_cast<size_t>(trow)) * kPairN : nullptr;
+            if (SPLIT && w.split) {
+                flag = p.flags + split_slot * 8 + rank * 4 + static_cast<uint32_t>(q);
                 const uint32_t claimed = 2u * p.epoch;
                 uint32_t old = 0;
                 if (lane == 0) old = atom_exch_acq_rel(flag, claimed);
@@ -751,7 +758,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                     continue;
                 }
-                if (SPLIT && ok) {
+                if (SPLIT && w.split && ok) {
                     const float4* src = reinterpret_cast<const float4*>(prow + c * 32);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -1049,15 +1056,12 @@ int pair_max_clusters() {
     return counts[dev];
 }
 
-// Share of the launch's worker slots (waves x workers) that do work.
-double fill(int units, int workers) {
-    const int waves = (units + workers - 1) / workers;
-    return static_cast<double>(units) / (static_cast<double>(waves) * workers);
-}
-
 // Each K-split launch tags the flags it writes with a new epoch, so the flags
 // never need clearing between launches.
 std::atomic<uint32_t> g_split_epoch{0};
+
+// Shortest K half (in 64-element blocks) of a split tile.
+constexpr int kMinHalfKBlocks = 48;
 
 }  // namespace
 
@@ -1101,27 +1105,33 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_blocks = (g.k + BK - 1) / BK;
     p.split = 1;
+    p.split_from = p.num_tiles;
     p.kb_split = p.k_blocks;
     p.num_units = p.num_tiles;
-    // Split K in two when that fills the last wave markedly better and each
-    // half keeps at least 128 k-blocks (K >= 16384); only with caller scratch
-    // for the tiles.  On GB300 a split of shorter contractions lost more to
-    // the extra partial-tile traffic and the shorter pipelines than the fuller
-    // last wave won: 4096 x 4096 outputs with K = 4096 ran at 1071 TFLOP/s
-    // split against 1279 unsplit, while K = 28672 went from 1477 to 1587.
-    if (allow_split && pair && g.split_flags && g.split_partial && p.k_blocks >= 256 &&
-        p.num_tiles <= g.split_tiles && p.num_tiles <= kSplitMaxTiles) {
+    // K split of the last wave: when the tiles left over after the full waves
+    // of CTA pairs would keep at most half of the pairs busy, each of those
+    // tiles becomes two half-K units, so the last round costs half a tile
+    // instead of a whole one (a 4096 x 4096 output is 256 tiles: on 76 pairs
+    // three full waves and 28 split tiles, 3.5 tile times instead of 4).  Only
+    // the split tiles exchange float32 partials.  Halves keep at least 48 k-blocks: on GB300 (ncu) the split
+    // gained 3 % at K = 6144 (146 -> 141 us), 8 % at K = 14336 (320 -> 294 us)
+    // and 6 % at K = 28672 against splitting every tile (610 -> 575 us), while
+    // at K = 4096 the exchange of partials cost what the half tile saved.
+    // Only with caller scratch.
+    if (allow_split && pair && g.split_flags && g.split_partial && p.k_blocks >= 2 * kMinHalfKBlocks) {
         const int pairs = pair_max_clusters();
-        if (pairs > 0 && fill(2 * p.num_tiles, pairs) > 1.08 * fill(p.num_tiles, pairs)) {
+        const int rem = pairs > 0 ? p.num_tiles % pairs : 0;
+        if (rem > 0 && 2 * rem <= pairs && rem <= g.split_tiles && rem <= kSplitMaxTiles) {
             p.split = 2;
+            p.split_from = p.num_tiles - rem;
             p.kb_split = p.k_blocks / 2;
-            p.num_units = 2 * p.num_tiles;
+            p.num_units = p.split_from + 2 * rem;
             p.flags = g.split_flags;
             p.partial = g.split_partial;
             p.epoch = ++g_split_epoch;
         }
     }
-    const int waves_of = pair ? sms / 2 / p.split : sms;
+    const int waves_of = pair ? sms / 2 : sms;
     const Raster r = choose_raster(p.tiles_m, p.tiles_n, tile_m, tile_n, g.k, std::min(p.num_tiles, waves_of));
     p.group = r.group;
     p.group_m = r.group_m ? 1 : 0;

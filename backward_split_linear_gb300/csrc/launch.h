@@ -36,13 +36,15 @@ struct GemmArgs {
     int64_t ld_aux;
     int ffn;           // SwigluBwd: column offset of u in aux and of du in out
     // Optional K-split scratch.  A CTA-pair launch whose last wave of tiles
-    // would leave many SMs idle may cut K in two halves computed by different
-    // CTA pairs; the half that finishes second adds the other's float32
-    // partial tile.  `split_flags` holds kSplitTileFlagBytes per tile and must
-    // be zeroed once before its first use (it is never reset: each launch
-    // tags its flags with a new epoch); `split_partial` holds
-    // kSplitTilePartialBytes per tile.  Launches whose tiles do not fit in
-    // `split_tiles` do not split.  Launches sharing the scratch must not overlap.
+    // would leave at least half of the CTA pairs idle cuts the K of that
+    // wave's tiles in two halves computed by different CTA pairs; the half
+    // that finishes second adds the other's float32 partial tile.
+    // `split_flags` holds kSplitTileFlagBytes per split tile and must be
+    // zeroed once before its first use (it is never reset: each launch tags
+    // its flags with a new epoch); `split_partial` holds
+    // kSplitTilePartialBytes per split tile.  Launches whose last wave has
+    // more tiles than `split_tiles` do not split.  Launches sharing the
+    // scratch must not overlap.
     uint32_t* split_flags;
     float* split_partial;
     int split_tiles;
@@ -50,10 +52,9 @@ struct GemmArgs {
 
 constexpr size_t kSplitTileFlagBytes = 8 * 4;            // one word per 32 rows of a 256 x 256 tile
 constexpr size_t kSplitTilePartialBytes = 256 * 256 * 4;  // one float32 tile
-// Launches of more tiles never split: scratch for 512 tiles is 128 MiB, and at
-// 76 CTA pairs such launches run seven waves or more, so their last wave
-// costs little.
-constexpr int kSplitMaxTiles = 512;
+// At most this many tiles split in one launch (16 MiB of partials): a last
+// wave that splits holds at most half as many tiles as there are CTA pairs.
+constexpr int kSplitMaxTiles = 64;
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
 

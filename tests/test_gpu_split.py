@@ -1,15 +1,17 @@
 """GPU tests of the K-split GEMM path of the stage runtime.
 
-A stage launches its GEMMs with scratch for a K split: when a launch's tiles
-would leave the last wave of CTA pairs mostly idle and its contraction is long
-(at least 256 blocks of 64, K >= 16384), each tile's contraction is cut in two
-halves computed by different CTA pairs, and the half that finishes second adds
-the other's float32 partial.  The per-step ops never split, so they serve as
-the unsplit comparison on the same inputs.  The shapes below split, on 76 CTA
-pairs: B of a linear with 28672 outputs (K = 28672, 256 tiles), W of a
-4096 x 4096 weight over 16384 tokens (K = 16384, 256 tiles), and a ragged case
-(4000 tokens, 4032 inputs, 24640 outputs: K = 24640 in 385 blocks, split 192 /
-193).  `test_split_rule_applies` checks that on the host.
+A stage launches its GEMMs with scratch for a K split of the last wave: when
+the 256 x 256 tiles left over after the full waves of CTA pairs would keep at
+most half of the pairs busy (and K has at least 96 blocks of 64), each of those
+tiles is cut into two K halves computed by different CTA pairs, and the half
+that finishes second adds the other's float32 partial.  The per-step ops never
+split, so they serve as the unsplit comparison on the same inputs.  The shapes
+below split on 76 CTA pairs (256 tiles: 3 full waves and 28 split tiles): B of
+a linear with 28672 outputs (K = 28672), W of a 4096 x 4096 weight over 16384
+tokens (K = 16384), B of a linear with 6144 outputs (K = 6144, halves of 48
+blocks), and a ragged case (4000 tokens, 4032 inputs, 24640 outputs: K = 24640
+in 385 blocks, split 192 / 193).  `test_split_rule_applies` checks that on the
+host.
 """
 import math
 
@@ -48,16 +50,13 @@ def run_linear_stage(inp, t, n_in, n_out):
     return y, dx, dw
 
 
-SPLIT_SHAPES = [(4096, 4096, 28672), (16384, 4096, 4096), (4000, 4032, 24640)]
-
-
-def _fill(units, workers):
-    return units / (math.ceil(units / workers) * workers)
+SPLIT_SHAPES = [(4096, 4096, 28672), (16384, 4096, 4096), (4096, 4096, 6144), (4000, 4032, 24640)]
 
 
 def _splits(m, n, k, pairs=76):
     tiles = math.ceil(m / 256) * math.ceil(n / 256)
-    return math.ceil(k / 64) >= 256 and tiles <= 512 and _fill(2 * tiles, pairs) > 1.08 * _fill(tiles, pairs)
+    rem = tiles % pairs
+    return math.ceil(k / 64) >= 96 and 0 < rem and 2 * rem <= pairs
 
 
 def test_split_rule_applies():
