@@ -67,7 +67,7 @@ def gemm_flops_per_mb(w):
 # ---------------------------------------------------------------- ncu summaries
 
 GEMM_SOURCES = ("gemm.cu", "device_common.cuh", "launch.h")
-EPILOGUES = {0: "bf16 store", 1: "residual epilogue", 2: "SwiGLU backward epilogue", 3: "float32 red.add epilogue"}
+EPILOGUES = {0: "bf16 store", 1: "residual epilogue", 2: "SwiGLU backward epilogue", 3: "float32 TMA reduce-add epilogue"}
 
 
 def gemm_source_sha():

@@ -20,7 +20,7 @@ B_NCU = "void unnamed>::gemm_pair_kernel<0, 1, 2, 2>(CUtensorMap_st, CUtensorMap
 
 def test_labels_of_ncu_names():
     assert bench.kernel_label(B_NCU) == "gemm_pair_kernel B (SwiGLU backward epilogue)"
-    assert bench.kernel_label(W) == "gemm_pair_kernel W (float32 red.add epilogue)"
+    assert bench.kernel_label(W) == "gemm_pair_kernel W (float32 TMA reduce-add epilogue)"
     assert bench.kernel_label("void <unnamed>::dgamma_final_kernel(<unnamed>::GammaBatch)") == "dgamma_final_kernel"
 
 
@@ -34,7 +34,7 @@ def test_summary_shares_and_gemm_traffic(tmp_path):
         lines.append(row(i, name, "dram__bytes_write.sum", "byte", int(wr_mb * 1e6)))
     csv.write_text("".join(lines))
     text = bench.summarize_ncu(str(csv), "ncu ... python bench.py", "t", bw_flops=4.6e9)
-    assert "| gemm_pair_kernel W (float32 red.add epilogue) | 1 | 0.60 | 60.0 % | 30.0 | 40.0 |" in text
+    assert "| gemm_pair_kernel W (float32 TMA reduce-add epilogue) | 1 | 0.60 | 60.0 % | 30.0 | 40.0 |" in text
     assert "| rmsnorm_bwd_kernel<2> | 1 | 0.10 | 10.0 % |" in text
     assert "| **total** | 4 | 1.00 | 100 % |" in text
     # B and W GEMM launches only: (20 + 2 + 30 + 40) MB over 4.6 GFLOP
@@ -65,7 +65,7 @@ def test_summary_of_several_logs(tmp_path):
                        row(0, W, "dram__bytes_write.sum", "byte", "0"))
         paths.append(str(csv))
     text = bench.summarize_ncu(",".join(paths), "cmd", "t", bw_flops=1e9)
-    assert "| gemm_pair_kernel W (float32 red.add epilogue) | 2 | 0.00 | 100.0 % | 2.0 | 0.0 |" in text
+    assert "| gemm_pair_kernel W (float32 TMA reduce-add epilogue) | 2 | 0.00 | 100.0 % | 2.0 | 0.0 |" in text
     assert "gemm_bw_dram_bytes_per_flop: 4.000000e-03" in text
 
 
