@@ -25,6 +25,7 @@ enum WaitSite : int {
     kSiteSplitFlag = 7,      // K-split epilogue waiting for the other half's partial tile
     kSiteAttn = 8,           // attention kernels (any of their pipeline waits)
     kSiteSelftest = 9,       // zb_selftest_wait_timeout
+    kSiteEpiSideInput = 10,  // epilogue waiting for side-input boxes (g and u) loaded by TMA
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -87,6 +88,16 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int
             return false;
         }
     }
+}
+
+// Teardown wait: until the phase completes or `limit_ns` passes, whatever the
+// status word says, so that copies still in flight land before the CTA's
+// shared memory goes away.
+static __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    return true;
 }
 
 // Same as mbar_wait, with cluster-scope acquire: for barriers that CTAs of the
@@ -243,6 +254,13 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 
 // Waits until every bulk group this thread committed has completed.
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)

@@ -123,6 +123,7 @@ __device__ __forceinline__ Unit unit_of(const KParams& p, int u) {
 struct PairGroup {
     CUtensorMap map[2 * kMaxGroup];   // A and B of each problem
     CUtensorMap omap[kMaxGroup];      // output of each problem (all epilogues but the SwiGLU backward)
+    CUtensorMap xmap[4];              // SwiGLU backward (never grouped): g, u, dg, du
     KParams kp[kMaxGroup];
     int unit_begin[kMaxGroup + 1];   // first work unit of each problem; the last entry is the total
     int n_probs;
@@ -237,9 +238,34 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int m, int n, c
 // j ^ ((r >> 1) & 3)); a float32 row is 128 bytes and takes the 128-byte
 // swizzle (word j of row r at word j ^ (r & 7)).  Either way eight
 // consecutive rows cover all banks.
+constexpr uint32_t kBf16BoxBytes = 32 * 64;  // 32 rows x 32 bf16 columns
+
 template <int EPI>
 __host__ __device__ constexpr uint32_t out_box_bytes() {
-    return EPI == static_cast<int>(Epilogue::AccumF32) ? 32 * 128 : 32 * 64;
+    return EPI == static_cast<int>(Epilogue::AccumF32) ? 32 * 128 : kBf16BoxBytes;
+}
+
+// SwiGLU backward of one 32-column chunk in place in a side-input ring slot:
+// the g box (64-byte swizzle, as TMA loaded it) becomes dg and the u box du,
+// ready for the TMA stores.
+__device__ __forceinline__ void swiglu_chunk_in_smem(uint32_t slot, int lane, const uint32_t (&r)[32]) {
+    const uint32_t l = static_cast<uint32_t>(lane);
+    const uint32_t sw = (l >> 1) & 3u;
+    const uint32_t grow = slot + l * 64u, urow = slot + kBf16BoxBytes + l * 64u;
+    uint4 x0[4], x1[4], o0[4], o1[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t off = (static_cast<uint32_t>(j) ^ sw) << 4;
+        x0[j] = ld_shared_v4(grow + off);
+        x1[j] = ld_shared_v4(urow + off);
+    }
+    epilogue_pack<static_cast<int>(Epilogue::SwigluBwd)>(r, x0, x1, o0, o1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t off = (static_cast<uint32_t>(j) ^ sw) << 4;
+        st_shared_v4(grow + off, o0[j]);
+        st_shared_v4(urow + off, o1[j]);
+    }
 }
 
 template <int EPI>
@@ -481,31 +507,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kPairM = 256;
 constexpr int kPairN = 256;
 constexpr int kHalf = 128;
-constexpr int kPairStages = 6;
 constexpr uint32_t kPairAStage = kHalf * BK * 2;  // 16 KiB
 constexpr uint32_t kPairBStage = kHalf * BK * 2;  // 16 KiB
 constexpr uint32_t kPairStage = kPairAStage + kPairBStage;
-constexpr int kPairNumBars = 2 * kPairStages + 5;
+// Side-input ring of the SwiGLU backward: per epilogue warp four slots, each
+// the g and u boxes of one 32-column chunk; the operand ring gives up a stage
+// to make room.
+constexpr int kSideSlots = 4;
+constexpr uint32_t kSideSlotBytes = 2 * kBf16BoxBytes;
+template <int EPI>
+__host__ __device__ constexpr int pair_stages() {
+    return EPI == static_cast<int>(Epilogue::SwigluBwd) ? 5 : 6;
+}
+template <int EPI>
+__host__ __device__ constexpr int pair_num_bars() {
+    return 2 * pair_stages<EPI>() + 5 + (EPI == static_cast<int>(Epilogue::SwigluBwd) ? 4 * kSideSlots : 0);
+}
 // bf16 outputs of the plain and residual epilogues leave through staging boxes
 // and TMA stores (4.2 % faster for a 4096 x 14336 dgrad, 4.9 % for a
 // 4096 x 28672 forward on GB300), and the float32 weight-gradient sums through
 // TMA reduce-adds, where the L2 does the read-modify-write.  The SwiGLU
-// backward keeps direct stores: its epilogue is bound by the latency of each
-// chunk, and the extra fence and warp synchronisation made it 2 % slower.
+// backward has its side inputs g and u brought in by TMA as well, into a ring
+// that runs three chunks ahead, computes dg and du in place there and stores
+// them by TMA: its epilogue warps touch no global memory with per-row accesses.
 template <int EPI>
 __host__ __device__ constexpr bool tma_out() {
     return EPI != static_cast<int>(Epilogue::SwigluBwd);
 }
-// Output staging: per epilogue warp two boxes, used in turn.
+// Output staging (two boxes per epilogue warp, used in turn) or the side-input ring.
 template <int EPI>
 __host__ __device__ constexpr uint32_t pair_out_bytes() {
-    return tma_out<EPI>() ? 4 * 2 * out_box_bytes<EPI>() : 0;
+    return tma_out<EPI>() ? 4 * 2 * out_box_bytes<EPI>() : 4 * kSideSlots * kSideSlotBytes;
 }
 template <int EPI>
 __host__ __device__ constexpr size_t pair_smem_bytes() {
-    return 1024 + kPairStages * kPairStage + pair_out_bytes<EPI>() + kPairNumBars * 8 + 16;
+    return 1024 + pair_stages<EPI>() * kPairStage + pair_out_bytes<EPI>() + pair_num_bars<EPI>() * 8 + 16;
 }
 static_assert(pair_smem_bytes<static_cast<int>(Epilogue::AccumF32)>() <= 232448, "shared memory");
+static_assert(pair_smem_bytes<static_cast<int>(Epilogue::SwigluBwd)>() <= 232448, "shared memory");
 
 template <bool A_MN, bool B_MN, int EPI, int NACC, bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -518,17 +557,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t s_a = base;
-    const uint32_t s_b = base + kPairStages * kPairAStage;
+    constexpr int kStages = pair_stages<EPI>();
+    constexpr int kNumBars = pair_num_bars<EPI>();
+    const uint32_t s_b = base + kStages * kPairAStage;
     constexpr bool kTmaOut = tma_out<EPI>();
-    const uint32_t s_out = s_b + kPairStages * kPairBStage;  // 2 KiB-aligned boxes
+    const uint32_t s_out = s_b + kStages * kPairBStage;  // 2 KiB-aligned boxes
     constexpr uint32_t kBoxBytes = out_box_bytes<EPI>();
     const uint32_t bars = s_out + pair_out_bytes<EPI>();
     auto full_bar = [&](int s) { return bars + 8u * s; };
-    auto empty_bar = [&](int s) { return bars + 8u * (kPairStages + s); };
-    auto tfull_bar = [&](int a) { return bars + 8u * (2 * kPairStages + a); };
-    auto tempty_bar = [&](int a) { return bars + 8u * (2 * kPairStages + 2 + a); };
-    const uint32_t drain_bar = bars + 8u * (2 * kPairStages + 4);
-    const uint32_t tmem_slot = bars + 8u * kPairNumBars;
+    auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+    auto tfull_bar = [&](int a) { return bars + 8u * (2 * kStages + a); };
+    auto tempty_bar = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
+    const uint32_t side_bars = bars + 8u * (2 * kStages + 5);  // SwiGLU backward: 4 warps x kSideSlots
+    const uint32_t tmem_slot = bars + 8u * kNumBars;
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5;
@@ -539,10 +581,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int npairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kPairStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
+        if constexpr (!kTmaOut)
+            for (int s = 0; s < 4 * kSideSlots; ++s) mbar_init(side_bars + 8u * s, 1);
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), 2 * 128);
@@ -552,6 +596,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2 * G.n_probs; ++i) tma_prefetch_map(&G.map[i]);
         if constexpr (kTmaOut)
             for (int i = 0; i < G.n_probs; ++i) tma_prefetch_map(&G.omap[i]);
+        else
+            for (int i = 0; i < 4; ++i) tma_prefetch_map(&G.xmap[i]);
     }
     if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -566,8 +612,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (usable && warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer (both CTAs)
-            uint32_t issued[kPairStages];
-            for (int s = 0; s < kPairStages; ++s) issued[s] = 0;
+            uint32_t issued[kStages];
+            for (int s = 0; s < kStages; ++s) issued[s] = 0;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -605,7 +651,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tma_load_2d_pair(b_dst, &G.map[2 * pi + 1], fb, k0, n0);
                     }
                     ++issued[stage];
-                    if (++stage == kPairStages) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -613,7 +659,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             // Loads must land before shared memory goes away: rank 0 sees its
             // full barriers complete; rank 1 sees the MMA release each stage.
-            for (int s = 0; s < kPairStages; ++s)
+            for (int s = 0; s < kStages; ++s)
                 if (issued[s] > 0) {
                     if (leader)
                         mbar_wait_cluster(full_bar(s), (issued[s] - 1u) & 1u, status, kSiteDrain, kWaitLimitNs);
@@ -655,7 +701,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         umma_bf16_pair(d, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
                     }
                     umma_commit_pair(empty_bar(stage), 0x3);
-                    if (++stage == kPairStages) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -668,15 +714,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else if (usable && warp >= 2) {
         // ---------------- epilogue (both CTAs): warp w reads lanes 32 (w % 4) .. +31
+        constexpr bool kSide = !kTmaOut;  // SwiGLU backward: side inputs by TMA into a ring
+        constexpr int kChunks = kPairN / 32;
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const uint32_t out_stage = s_out + static_cast<uint32_t>(q) * 2u * kBoxBytes;
         uint32_t n_stored = 0;  // staged chunks this warp has handed to TMA stores
-        int it = 0;
-        for (int u = pair; u < num_units; u += npairs, ++it) {
+        // Side-input ring (SwiGLU backward): chunk k of this warp is column
+        // chunk k % 8 of its (k / 8)-th work unit; lane 0 requests the g and u
+        // boxes of its 32 rows into slot k % kSideSlots, kSideSlots - 1 chunks
+        // ahead (across units: side inputs do not depend on the accumulator).
+        const uint32_t ring = s_out + static_cast<uint32_t>(q) * (kSideSlots * kSideSlotBytes);
+        auto side_bar = [&](int slot) { return side_bars + 8u * static_cast<uint32_t>(q * kSideSlots + slot); };
+        const int my_units = pair < num_units ? (num_units - 1 - pair) / npairs + 1 : 0;
+        const int n_chunks = kSide ? my_units * kChunks : 0;
+        auto issue_side = [&](int k) {
+            const int u = pair + (k / kChunks) * npairs;
             const int pi = problem_of(G, u);
-                const KParams& p = G.kp[pi];
-                const Unit w = unit_of<SPLIT>(p, u - G.unit_begin[pi]);
+            const KParams& p = G.kp[pi];
+            const Unit w = unit_of<SPLIT>(p, u - G.unit_begin[pi]);
+            int tm, tn;
+            tile_coords(p, w.tile, tm, tn);
+            const int n = tn * kPairN + (k % kChunks) * 32;
+            const int row0 = tm * kPairM + static_cast<int>(rank) * kHalf + q * 32;
+            const uint32_t slot = ring + static_cast<uint32_t>(k % kSideSlots) * kSideSlotBytes;
+            const uint32_t bar = side_bar(k % kSideSlots);
+            mbar_arrive_expect_tx(bar, kSideSlotBytes);
+            tma_load_2d(slot, &G.xmap[0], bar, n, row0);
+            tma_load_2d(slot + kBf16BoxBytes, &G.xmap[1], bar, n, row0);
+        };
+        int issued = 0;  // chunks whose side inputs lane 0 has requested
+        int k = 0;       // chunks this warp has consumed
+        if (kSide && lane == 0)
+            for (; issued < kSideSlots - 1 && issued < n_chunks; ++issued) issue_side(issued);
+        bool alive = true;
+        int it = 0;
+        for (int u = pair; alive && u < num_units; u += npairs, ++it) {
+            const int pi = problem_of(G, u);
+            const KParams& p = G.kp[pi];
+            const Unit w = unit_of<SPLIT>(p, u - G.unit_begin[pi]);
             const int acc = it % NACC;
             const uint32_t aph = static_cast<uint32_t>(it / NACC) & 1u;
             // one verdict per warp: the tensor-memory loads below are warp-wide
@@ -687,6 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tile_coords(p, w.tile, tm, tn);
             const int trow = static_cast<int>(rank) * kHalf + row;  // row inside the 256-row tile
             const int m = tm * kPairM + trow;
+            const int row0 = m - lane;  // first row of this warp's 32
             const int n_base = tn * kPairN;
             const bool row_ok = m < p.m;
             const uint32_t tbase =
@@ -721,81 +798,105 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const bool run_epi = row_ok && !store_partial && !give_up;
 #pragma unroll 1
-            for (int c = 0; c < kPairN / 32; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
                 const int n = n_base + c * 32;
                 const bool ok = run_epi && n < p.n;
-                uint4 x0[4], x1[4];
-                if constexpr (EPI == static_cast<int>(Epilogue::AddResidual) ||
-                              EPI == static_cast<int>(Epilogue::SwigluBwd)) {
+                uint4 x0[4];
+                if constexpr (EPI == static_cast<int>(Epilogue::AddResidual)) {
                     if (ok) {
-                        const uint16_t* rowp =
-                            static_cast<const uint16_t*>(p.aux) + static_cast<int64_t>(m) * p.ld_aux;
-                        const uint4* s0 = reinterpret_cast<const uint4*>(rowp + n);
+                        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.aux) +
+                                                                          static_cast<int64_t>(m) * p.ld_aux + n);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) x0[j] = s0[j];
-                        if constexpr (EPI == static_cast<int>(Epilogue::SwigluBwd)) {
-                            const uint4* s1 = reinterpret_cast<const uint4*>(rowp + p.ffn + n);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) x1[j] = s1[j];
-                        }
+                        for (int j = 0; j < 4; ++j) x0[j] = src[j];
+                    }
+                }
+                if constexpr (kSide) {
+                    const uint32_t sb = side_bar(k % kSideSlots);
+                    const uint32_t sph = static_cast<uint32_t>(k / kSideSlots) & 1u;
+                    if (!__all_sync(0xffffffffu, mbar_wait(sb, sph, status, kSiteEpiSideInput))) {
+                        alive = false;
+                        break;
                     }
                 }
                 uint32_t r[32];
                 tmem_load_32(tbase + static_cast<uint32_t>(c * 32), r);
                 tmem_wait_load();
-                if (c == kPairN / 32 - 1) {
+                if (c == kChunks - 1) {
                     tc_fence_before();
                     if (leader)
                         mbar_arrive(tempty_bar(acc));
                     else
                         mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
                 }
+                bool stored = false;
                 if (SPLIT && store_partial) {
                     float4* dst = reinterpret_cast<float4*>(const_cast<float*>(prow) + c * 32);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                    continue;
-                }
-                if (SPLIT && w.split && ok) {
-                    const float4* src = reinterpret_cast<const float4*>(prow + c * 32);
+                } else {
+                    if (SPLIT && w.split && ok) {
+                        const float4* src = reinterpret_cast<const float4*>(prow + c * 32);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float4 v = src[j];
-                        r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
-                        r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
-                        r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
-                        r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 v = src[j];
+                            r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
+                            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
+                            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
+                            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                        }
+                    }
+                    // The box is stored when any of the warp's rows lies inside
+                    // M (the TMA drops rows >= M and columns >= N); the
+                    // decision is warp-uniform.
+                    stored = !give_up && row0 < p.m && n < p.n;
+                    if (stored) {
+                        if constexpr (kSide) {
+                            const uint32_t slot = ring + static_cast<uint32_t>(k % kSideSlots) * kSideSlotBytes;
+                            if (ok) swiglu_chunk_in_smem(slot, lane, r);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&G.xmap[2], slot, n, row0);
+                                tma_store_2d(&G.xmap[3], slot + kBf16BoxBytes, n, row0);
+                                bulk_commit_group();
+                            }
+                        } else {
+                            // a box is rewritten only after the store that read
+                            // it, two chunks back, has finished reading
+                            const uint32_t box = out_stage + (n_stored & 1u) * kBoxBytes;
+                            if (lane == 0) bulk_wait_group_read<1>();
+                            __syncwarp();
+                            if (ok) epilogue_chunk_to_smem<EPI>(box, lane, r, x0);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if constexpr (EPI == static_cast<int>(Epilogue::AccumF32))
+                                    tma_reduce_add_2d(&G.omap[pi], box, n, row0);
+                                else
+                                    tma_store_2d(&G.omap[pi], box, n, row0);
+                                bulk_commit_group();
+                            }
+                            ++n_stored;
+                        }
                     }
                 }
-                if constexpr (kTmaOut) {
-                    // The box is stored when any of the warp's rows lies inside M
-                    // (the TMA drops rows >= M and columns >= N); the decision is
-                    // warp-uniform.  A buffer is rewritten only after the store
-                    // that read it, two chunks back, has finished reading.
-                    const int row0 = tm * kPairM + static_cast<int>(rank) * kHalf + q * 32;
-                    if (!give_up && row0 < p.m && n < p.n) {
-                        const uint32_t box = out_stage + (n_stored & 1u) * kBoxBytes;
-                        if (lane == 0) bulk_wait_group_read<1>();
-                        __syncwarp();
-                        if (ok) epilogue_chunk_to_smem<EPI>(box, lane, r, x0);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            if constexpr (EPI == static_cast<int>(Epilogue::AccumF32))
-                                tma_reduce_add_2d(&G.omap[pi], box, n, row0);
-                            else
-                                tma_store_2d(&G.omap[pi], box, n, row0);
-                            bulk_commit_group();
-                        }
-                        ++n_stored;
+                if constexpr (kSide) {
+                    // Refill the slot chunk k - 1 used, once the stores that
+                    // read it are done (all but this chunk's own group).
+                    if (lane == 0 && issued < n_chunks) {
+                        if (stored)
+                            bulk_wait_group_read<1>();
+                        else
+                            bulk_wait_group_read<0>();
+                        issue_side(issued);
+                        ++issued;
                     }
-                } else if (ok) {
-                    epilogue_chunk<EPI>(p, m, n, r, x0, x1);
+                    ++k;
                 }
             }
-            if (SPLIT && store_partial) {
+            if (SPLIT && store_partial && alive) {
                 __syncwarp();  // every lane's partial rows before lane 0's release
                 if (lane == 0) {
                     __threadfence();
@@ -803,8 +904,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        // the staging boxes must stay until the last stores have read them
-        if (kTmaOut && lane == 0) bulk_wait_group_all();
+        // The staging boxes and the ring must stay until the last stores have
+        // read them, and side inputs still in flight (after a wait gave up)
+        // must land before the CTA leaves.
+        if (lane == 0) {
+            bulk_wait_group_all();
+            for (; k < issued; ++k)
+                mbar_drain(side_bar(k % kSideSlots), static_cast<uint32_t>(k / kSideSlots) & 1u, kWaitLimitNs);
+        }
     }
 
     tc_fence_before();
@@ -1070,7 +1177,7 @@ namespace {
 // Tensor maps and kernel parameters of one GEMM; `pair` says which kernel
 // takes it.  A K split is considered only when `allow_split`.
 cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtensorMap& mb, CUtensorMap& mo,
-                    KParams& p, bool& pair) {
+                    CUtensorMap* mx, KParams& p, bool& pair) {
     const int sms = sm_count();
     // A CTA pair takes 256 x 256 tiles; small outputs keep the one-CTA kernel.
     pair = g.m >= kPairM && g.n >= kPairN;
@@ -1095,6 +1202,17 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
     if (ok && pair && g.epi == Epilogue::AccumF32)
         ok = encode_map(&mo, g.out, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+    // SwiGLU backward of the CTA-pair kernel: g and u (loaded) and dg and du
+    // (stored), each [M, ffn] inside a row of 2 ffn, 32 x 32 boxes.
+    if (ok && pair && g.epi == Epilogue::SwigluBwd) {
+        if (!mx) return cudaErrorInvalidValue;
+        const uint16_t* aux = static_cast<const uint16_t*>(g.aux);
+        uint16_t* out = static_cast<uint16_t*>(g.out);
+        ok = encode_map(&mx[0], aux, g.m, g.n, g.ld_aux, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+             encode_map(&mx[1], aux + g.ffn, g.m, g.n, g.ld_aux, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+             encode_map(&mx[2], out, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+             encode_map(&mx[3], out + g.ffn, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    }
     if (!ok) return cudaErrorInvalidValue;
     p = KParams{};
     p.m = g.m;
@@ -1151,16 +1269,17 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     if (g.m <= 0 || g.n <= 0 || g.k <= 0) return cudaSuccess;
-    CUtensorMap ma, mb, mo = {};
+    CUtensorMap ma, mb, mo = {}, mx[4] = {};
     KParams p;
     bool pair = false;
-    const cudaError_t e = prepare(g, true, ma, mb, mo, p, pair);
+    const cudaError_t e = prepare(g, true, ma, mb, mo, mx, p, pair);
     if (e != cudaSuccess) return e;
     if (!pair) return dispatch<kBN>(g, ma, mb, p, stream);
     PairGroup G;
     G.map[0] = ma;
     G.map[1] = mb;
     G.omap[0] = mo;
+    for (int i = 0; i < 4; ++i) G.xmap[i] = mx[i];
     G.kp[0] = p;
     G.unit_begin[0] = 0;
     G.unit_begin[1] = p.num_units;
@@ -1170,11 +1289,12 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
 
 cudaError_t launch_gemm_group(const GemmArgs* gs, int n, cudaStream_t stream) {
     // One grouped launch when every GEMM takes the CTA-pair kernel with the
-    // same layouts and epilogue; otherwise one launch each.
+    // same layouts and epilogue; otherwise one launch each.  The SwiGLU
+    // backward (side-input maps for one problem per launch) is never grouped.
     bool grouped = n > 1 && n <= kMaxGroup;
     for (int i = 0; grouped && i < n; ++i)
         grouped = gs[i].m >= kPairM && gs[i].n >= kPairN && gs[i].k > 0 && gs[i].kind == gs[0].kind &&
-                  gs[i].epi == gs[0].epi;
+                  gs[i].epi == gs[0].epi && gs[i].epi != Epilogue::SwigluBwd;
     if (!grouped) {
         for (int i = 0; i < n; ++i) {
             const cudaError_t e = launch_gemm(gs[i], stream);
@@ -1186,7 +1306,7 @@ cudaError_t launch_gemm_group(const GemmArgs* gs, int n, cudaStream_t stream) {
     G.unit_begin[0] = 0;
     for (int i = 0; i < n; ++i) {
         bool pair = false;
-        const cudaError_t e = prepare(gs[i], false, G.map[2 * i], G.map[2 * i + 1], G.omap[i], G.kp[i], pair);
+        const cudaError_t e = prepare(gs[i], false, G.map[2 * i], G.map[2 * i + 1], G.omap[i], nullptr, G.kp[i], pair);
         if (e != cudaSuccess) return e;
         G.unit_begin[i + 1] = G.unit_begin[i] + G.kp[i].num_units;
     }
