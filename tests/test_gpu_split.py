@@ -22,7 +22,8 @@ import torch
 from backward_split_linear_gb300 import binding as zb
 from backward_split_linear_gb300 import synth
 from backward_split_linear_gb300.runtime import Stage, bf16_from_bits, f64_from_bf16
-from parity import assert_close, errors
+from oracle import stage as S
+from parity import MAX_TOL, assert_close, errors, stage_fro_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -112,3 +113,32 @@ def test_split_is_bitwise_reproducible():
         again = run_linear_stage(inp, t, n_in, n_out)
         for a, b in zip(first, again):
             assert torch.equal(a, b)
+
+
+def test_swiglu_dgrad_split_in_mlp_stage():
+    """A SwiGLU-MLP layer whose down-projection dgrad (M = 4096 tokens, N = ffn 4096, K = hidden
+    6144) and gate|up dgrad (N = 6144, K = 8192) split their last wave, so the SwiGLU epilogue's
+    side-input ring also serves the half that only stores a partial.  dx and every gradient against
+    the float64 oracle over all tokens, at the one-layer stage tolerance."""
+    t, hidden, ffn = 4096, 6144, 4096
+    assert _splits(t, ffn, hidden) and _splits(t, hidden, 2 * ffn)
+    inp = synth.stage_inputs("mlp", 1, hidden, ffn, tokens=t, n_mb=1, seed=13)
+    st = Stage.from_synth("mlp", 1, hidden, ffn, max_tokens=t, max_inflight=1, params_bits=inp["params"])
+    x = bf16_from_bits(inp["x"][0])
+    dy = bf16_from_bits(inp["dy"][0])
+    y = torch.empty(t, hidden, dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty(t, hidden, dtype=torch.bfloat16, device="cuda")
+    st.forward(0, x, y)
+    st.backward_input(0, dy, dx)
+    st.backward_weight(0)
+    st.sync()
+    orc = S.StageOracle(synth.params_f64(inp["params"]), dict(kind="mlp", hidden=hidden, ffn=ffn, eps=1e-5))
+    orc.forward(0, synth.bf16_to_f64(inp["x"][0]))
+    ref_dx = orc.backward_input(0, synth.bf16_to_f64(inp["dy"][0]))
+    orc.backward_weight(0)
+    tol = stage_fro_tol(1)
+    assert_close(f64_from_bf16(dx), ref_dx, "dx", fro_tol=tol, max_tol=MAX_TOL)
+    for k, ref in orc.grads[0].items():
+        assert_close(st.grads[0][k].cpu().numpy(), ref, f"d{k}", fro_tol=tol, max_tol=MAX_TOL)
+    st.close()
+
