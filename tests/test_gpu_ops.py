@@ -228,7 +228,8 @@ def test_wait_timeout_is_reported_and_cleared():
 
 @pytest.mark.parametrize("t,n_in,n_out", [(4096, 4096, 512), (4000, 4032, 320)])
 def test_backward_input_many_tiles(t, n_in, n_out):
-    """256 CTA-pair tiles: the last wave runs as half tiles (ragged in the second case)."""
+    """256 CTA-pair tiles, 3.4 waves of 76 pairs, with the TMA-store epilogue (ragged M and N in the
+    second case); per-step ops never split K."""
     rng = np.random.default_rng(21)
     dyb, dy = draw_bf16(rng, (t, n_out))
     wb, w = draw_bf16(rng, (n_out, n_in), 0.05)
