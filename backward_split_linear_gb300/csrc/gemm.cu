@@ -940,10 +940,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // boxes of box_cols x box_rows, zero fill out of range (loads) and no writes
 // out of range (stores).  Operand boxes take the 128-byte swizzle of the MMA
 // descriptors; output boxes (32 x 32) the 64-byte swizzle of the staging boxes.
+// Loads promote to 256-byte L2 fills, except the SwiGLU side inputs (64-byte
+// box rows): 128-byte fills made that dgrad 3 % faster on GB300 (325.4 ->
+// 315.6 us) for the same DRAM bytes.
 bool encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
                 uint32_t box_cols, uint32_t box_rows,
                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
-                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t esize = dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
@@ -952,7 +956,7 @@ bool encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, i
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, bool A_MN, bool B_MN, int EPI>
@@ -1208,8 +1212,11 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
         if (!mx) return cudaErrorInvalidValue;
         const uint16_t* aux = static_cast<const uint16_t*>(g.aux);
         uint16_t* out = static_cast<uint16_t*>(g.out);
-        ok = encode_map(&mx[0], aux, g.m, g.n, g.ld_aux, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
-             encode_map(&mx[1], aux + g.ffn, g.m, g.n, g.ld_aux, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+        constexpr auto kBf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        constexpr auto kFill128 = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+        ok = encode_map(&mx[0], aux, g.m, g.n, g.ld_aux, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, kBf16, kFill128) &&
+             encode_map(&mx[1], aux + g.ffn, g.m, g.n, g.ld_aux, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, kBf16,
+                        kFill128) &&
              encode_map(&mx[2], out, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
              encode_map(&mx[3], out + g.ffn, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     }
