@@ -281,9 +281,19 @@ zb_status zb_op_attention_causal_backward(const void* qkv, const void* a, const 
                                           int32_t head_dim, int32_t seq_len, void* stream);
 
 /* Device status word shared by all kernels of the library on the current
- * device: 0 = fine, else the code of the first wait that ran out.  Reading
- * synchronises `stream`; `reset` != 0 clears the word afterwards.  Returns
- * ZB_ERR_DEVICE_TIMEOUT when the word was set, ZB_OK otherwise. */
+ * device: 0 = fine, else the code of the first wait that ran out:
+ *   1  GEMM TMA producer waiting for a free shared-memory stage
+ *   2  GEMM MMA issuer waiting for a loaded stage
+ *   3  GEMM MMA issuer waiting for the epilogue to free an accumulator
+ *   4  GEMM epilogue waiting for a finished accumulator
+ *   5  teardown waiting for copies or MMAs in flight
+ *   6  the two CTAs of a GEMM pair got different tensor-memory columns
+ *   7  K-split epilogue waiting for the other half's partial tile
+ *   8  attention kernels (any of their pipeline waits)
+ *   9  zb_selftest_wait_timeout
+ *   10 GEMM epilogue waiting for SwiGLU side inputs loaded by TMA
+ * Reading synchronises `stream`; `reset` != 0 clears the word afterwards.
+ * Returns ZB_ERR_DEVICE_TIMEOUT when the word was set, ZB_OK otherwise. */
 zb_status zb_device_status(void* stream, int32_t reset, int32_t* code);
 
 /* Runs one bounded wait on an mbarrier that nothing arrives on, with a limit
