@@ -25,6 +25,20 @@ def test_exports_every_declared_function(zblib):
     assert sorted(zb.declared_symbols()) == names
 
 
+def test_device_status_codes_documented():
+    """The device status codes that zb.h lists are the kernels' wait sites, code for code."""
+    src = open(os.path.join(os.path.dirname(HEADER), "..", "backward_split_linear_gb300", "csrc",
+                            "device_common.cuh")).read()
+    enum = src[src.index("enum WaitSite"):src.index("};", src.index("enum WaitSite"))]
+    sites = {int(v) for v in re.findall(r"kSite\w+\s*=\s*(\d+)", enum)}
+    text = open(HEADER).read()
+    start = text.index("Device status word")
+    block = text[start:text.index("zb_device_status(", start)]
+    listed = {int(v) for v in re.findall(r"^\s*\*\s+(\d+)\s+\S", block, flags=re.M)}
+    assert sites == set(range(1, max(sites) + 1))
+    assert listed == sites
+
+
 def test_version_and_status_strings(zblib):
     assert zb.zb_version() == 100
     for code in zb.STATUS_NAMES:
