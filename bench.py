@@ -337,7 +337,10 @@ def run_reference(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * (tb + tw) / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "tokens_per_step": sample, "wall_s": wall},
+            "config": {"workload": args.workload, **{k: v for k, v in w.items()},
+                       "timed": f"each step: B and W of one {sample}-token microbatch of this workload "
+                                f"(a bounded sample), float64 on the host cores",
+                       "sample_tokens_per_step": sample, "wall_s": wall},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "blas_threads": blas_threads(),
                              "sample": f"each step: B and W of one {sample}-token microbatch of the stage"},

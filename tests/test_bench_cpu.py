@@ -87,3 +87,7 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "tiny_stage"
+    # the same workload description as the GPU arm's line, plus how it was sampled
+    for key, val in bench.WORKLOADS["tiny_stage"].items():
+        assert d["config"][key] == val, key
+    assert d["config"]["sample_tokens_per_step"] > 0
