@@ -808,21 +808,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // One warp per (token, head): dvec[h][t] = sum_c da[t, h d + c] * a[t, h d + c].
 __global__ void attn_causal_rowsum_kernel(const uint16_t* __restrict__ da, const uint16_t* __restrict__ a, float* dvec,
                                  int tokens, int n_heads, int head_dim, int ld_stat) {
-    const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (wid >= static_cast<int64_t>(tokens) * n_heads) return;
-    const int t = static_cast<int>(wid / n_heads), h = static_cast<int>(wid % n_heads);
-    const int64_t off = static_cast<int64_t>(t) * n_heads * head_dim + static_cast<int64_t>(h) * head_dim;
-    float acc = 0.f;
-    for (int c = 4 * lane; c < head_dim; c += 128) {
-        const uint2 x = *reinterpret_cast<const uint2*>(da + off + c);
-        const uint2 y = *reinterpret_cast<const uint2*>(a + off + c);
-        acc += bf16_lo(x.x) * bf16_lo(y.x) + bf16_hi(x.x) * bf16_hi(y.x) + bf16_lo(x.y) * bf16_lo(y.y) +
-               bf16_hi(x.y) * bf16_hi(y.y);
-    }
+    // Row r = t n_heads + h of da and a starts at element r head_dim (rows are
+    // contiguous).  A warp takes kRowsPerWarp consecutive rows, two at a time:
+    // each half-warp reads one row in 16-byte pieces (pointers and head_dim
+    // keep them 16-byte aligned), so every load instruction covers 512
+    // contiguous bytes of each tensor.
+    constexpr int kRowsPerWarp = 8;
+    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+    const int64_t n_rows = static_cast<int64_t>(tokens) * n_heads;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) dvec[static_cast<int64_t>(h) * ld_stat + t] = acc;
+    for (int i = 0; i < kRowsPerWarp; i += 2) {
+        const int64_t r = warp_id * kRowsPerWarp + i + half;
+        float acc = 0.f;
+        if (r < n_rows) {
+            const uint16_t* x = da + r * head_dim;
+            const uint16_t* y = a + r * head_dim;
+            for (int c = 8 * hl; c < head_dim; c += 128) {
+                const uint4 u = *reinterpret_cast<const uint4*>(x + c);
+                const uint4 v = *reinterpret_cast<const uint4*>(y + c);
+                acc += bf16_lo(u.x) * bf16_lo(v.x) + bf16_hi(u.x) * bf16_hi(v.x) + bf16_lo(u.y) * bf16_lo(v.y) +
+                       bf16_hi(u.y) * bf16_hi(v.y) + bf16_lo(u.z) * bf16_lo(v.z) + bf16_hi(u.z) * bf16_hi(v.z) +
+                       bf16_lo(u.w) * bf16_lo(v.w) + bf16_hi(u.w) * bf16_hi(v.w);
+            }
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);  // within each half-warp
+        if (hl == 0 && r < n_rows) {
+            const int t = static_cast<int>(r / n_heads), h = static_cast<int>(r % n_heads);
+            dvec[static_cast<int64_t>(h) * ld_stat + t] = acc;
+        }
+    }
 }
 
 // ------------------------------------------------------------------------ host side
@@ -912,7 +928,7 @@ cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const
     p.ld_out = qkv_w;
     p.lse = const_cast<float*>(lse);
     p.dvec = dvec;
-    const int64_t warps = static_cast<int64_t>(s.tokens) * s.n_heads;
+    const int64_t warps = (static_cast<int64_t>(s.tokens) * s.n_heads + 7) / 8;  // 8 rows per warp
     attn_causal_rowsum_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
         static_cast<const uint16_t*>(da), static_cast<const uint16_t*>(a), dvec, s.tokens, s.n_heads, D, s.ld_stat);
     cudaError_t e = cudaGetLastError();
