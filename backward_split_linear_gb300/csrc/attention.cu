@@ -805,7 +805,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // ------------------------------------------------------------------------ D = rowsum(dO * O)
 
-// One warp per (token, head): dvec[h][t] = sum_c da[t, h d + c] * a[t, h d + c].
+// dvec[h][t] = sum_c da[t, h d + c] * a[t, h d + c]: each half-warp reduces
+// one (token, head) row, and each warp covers 8 consecutive rows.
 __global__ void attn_causal_rowsum_kernel(const uint16_t* __restrict__ da, const uint16_t* __restrict__ a, float* dvec,
                                  int tokens, int n_heads, int head_dim, int ld_stat) {
     // Row r = t n_heads + h of da and a starts at element r head_dim (rows are

@@ -78,7 +78,10 @@ struct GammaProblem {
 };
 constexpr int kMaxGammaProblems = 16;
 
-// Scratch bytes of one reduction; a batch of n needs n times as much.
+// Scratch bytes of one reduction; a batch of n needs n times as much.  For
+// hidden <= kGammaMaxPartialFloats it is at most 4 * kGammaMaxPartialFloats
+// bytes, whatever the token count.
+constexpr int kGammaMaxPartialFloats = 1 << 17;
 size_t rmsnorm_gamma_scratch_bytes(int tokens, int hidden);
 // Up to kMaxGammaProblems reductions of the same [tokens, hidden] shape in one
 // launch pair; each problem's result is the same bits as when run alone.

@@ -19,12 +19,17 @@
 
 namespace {
 
-constexpr size_t kStaticScratchFloats = size_t(1) << 17;  // 512 KiB of float32 partial sums
+// 512 KiB of float32 partial sums: the most the reduction's partition takes
+// for any hidden <= 131072, at any token count.
+constexpr size_t kStaticScratchFloats = static_cast<size_t>(zbk::kGammaMaxPartialFloats);
 
 __device__ __align__(256) float g_gamma_scratch[kStaticScratchFloats];
 
 // Device address of g_gamma_scratch on the current device, looked up on the
-// first call for that device (with that device current).  nullptr on failure.
+// first call for that device (with that device current) and kept for the
+// process.  cudaDeviceReset() on a device invalidates the kept address, so the
+// library must not be used on that device again afterwards.  nullptr on
+// failure.
 float* static_scratch() {
     static float* ptrs[64] = {};
     static std::mutex mu;
@@ -55,7 +60,9 @@ extern "C" zb_status zb_op_rmsnorm_backward_gamma_noalloc(const void* dn, const 
     if (!rows_ok(dn) || !rows_ok(x) || !rows_ok(rstd) || !dgamma ||
         (reinterpret_cast<uintptr_t>(dgamma) & 15u) != 0)
         return ZB_ERR_ARG;
-    // The partial sums must fit the fixed array: ceil(T / 32) * H floats.
+    // The partial sums must fit the fixed array: they take exactly the bytes
+    // zb_op_rmsnorm_backward_gamma_scratch_bytes(T, H) reports (the partition's
+    // parts * H floats), which fit for every T when H <= 131072.
     if (zbk::rmsnorm_gamma_scratch_bytes(tokens, hidden) > kStaticScratchFloats * sizeof(float))
         return ZB_ERR_SHAPE;
     if (zbk::device_arch() != 103) return zbk::device_arch() < 0 ? ZB_ERR_CUDA : ZB_ERR_DEVICE;

@@ -174,11 +174,17 @@ constexpr int kGammaGroups = kRowThreads / kGammaChunks;  // 8 row groups
 constexpr int kGammaTargetBlocks = 320;
 constexpr int kGammaUnroll = 4;
 
+// parts = min(ceil(320 / column blocks), ceil(T / 8), 2^17 / H), at least 1.
+// The last bound keeps the partial sums (parts * H floats) within 2^17 floats
+// for every H <= 2^17, whatever T: a fixed 512 KiB buffer then serves every
+// token count of those widths.  At H <= 16384 it never binds (the first bound
+// is smaller), so the partition of the stage's widths is unaffected.
 int gamma_parts(int tokens, int hidden) {
     const int col_blocks = (hidden + kGammaCols - 1) / kGammaCols;
     const int want = (kGammaTargetBlocks + col_blocks - 1) / col_blocks;
     const int most = (tokens + kGammaGroups - 1) / kGammaGroups;  // at least 8 tokens per part
-    return std::max(1, std::min(want, most));
+    const int fit = kGammaMaxPartialFloats / hidden;
+    return std::max(1, std::min({want, most, fit}));
 }
 
 // Several reductions of the same shape in one launch: problem blockIdx.z.

@@ -43,6 +43,10 @@
  *    or zb_stage_sync() reports ZB_ERR_DEVICE_TIMEOUT.
  *  - Not thread-safe: calls on one zb_stage_t must come from one host thread
  *    and one stream (or be ordered by the caller).
+ *  - The library keeps, per device, the addresses of its own device variables
+ *    (the status word, the array of the _noalloc call).  cudaDeviceReset() on
+ *    a device invalidates them: do not use the library on that device again in
+ *    the same process afterwards.
  */
 #ifndef ZB_H_
 #define ZB_H_
@@ -225,8 +229,9 @@ zb_status zb_op_rmsnorm_backward_gamma(const void* dn, const void* x, const floa
  *  - Every GPU that loads the library holds that array until the process exits.
  *  - Size limit: zb_op_rmsnorm_backward_gamma_scratch_bytes(tokens, hidden)
  *    must not exceed 4 * zb_op_rmsnorm_backward_gamma_noalloc_max_floats()
- *    bytes (512 KiB); that admits every token count for hidden <= 131072.
- *    Larger sizes return ZB_ERR_SHAPE and enqueue nothing.
+ *    bytes (512 KiB).  The reduction's partition takes at most 131072 / hidden
+ *    partial rows, so every token count fits for hidden <= 131072 (multiples
+ *    of 64); wider rows return ZB_ERR_SHAPE and enqueue nothing.
  *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *    routine.
  *  - The first call on a device looks up the array's device address (with that

@@ -194,3 +194,19 @@ def test_schedule_search_equals_oracle(zblib):
     with pytest.raises(zb.ZBError) as e:
         zb.zb_schedule_search(0, 4, 8, 3, 1, 1, 1)  # a ceiling below p cannot hold the warm-up
     assert e.value.name == "ZB_ERR_ARG"
+
+
+def test_noalloc_size_rule_holds_for_every_width(zblib):
+    """zb.h promises that the allocation-free gamma reduction takes every token count for
+    hidden <= 131072: its partial sums (zb_op_rmsnorm_backward_gamma_scratch_bytes) must
+    fit the library's fixed array for each multiple of 64 up to there, at any T."""
+    from backward_split_linear_gb300 import binding as zb
+
+    cap = 4 * zb.zb_op_rmsnorm_backward_gamma_noalloc_max_floats()
+    assert cap == 512 * 1024
+    for hidden in range(64, 131072 + 1, 64):
+        for t in (1, 8, 9, 63, 1000, 4096, 1 << 20, 1 << 24):
+            nbytes = zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(t, hidden)
+            assert 0 < nbytes <= cap, (t, hidden, nbytes)
+    # past the promise the partition needs more than the array for long inputs
+    assert zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(1 << 20, 131072 + 64) > cap
