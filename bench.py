@@ -159,30 +159,41 @@ def summarize_ncu(path, command, title, bw_flops=None):
         bw = [r for label, r in rows.items() if label.startswith("gemm") and (" B (" in label or " W (" in label)]
         total = sum(r["rd"] + r["wr"] for r in bw)
         if total:
-            out += ["", f"gemm_bw_dram_bytes_per_flop: {total / bw_flops:.6e}",
-                    f"gemm_source_sha256: {gemm_source_sha()}"]
+            out += ["", f"B/W GEMM DRAM bytes per algorithmic FLOP: {total / bw_flops:.6e} "
+                        f"(GEMM sources sha256 {gemm_source_sha()[:16]}...)"]
     return "\n".join(out) + "\n"
 
 
-def profiled_gemm_traffic(workload, w_mode):
-    """DRAM bytes per algorithmic FLOP of the B/W GEMMs from the committed ncu summary of this
-    workload, or None when there is none or the GEMM sources changed since it was taken."""
-    if w_mode != "per-microbatch":
-        return None, "no capture for this W mode"
-    path = os.path.join(ROOT, "profiles", f"gemm_traffic_{workload}.md")
+def gemm_traffic_record(path, command, bw_flops):
+    """The data file bench.py reads for roofline.traffic: B/W GEMM DRAM bytes per algorithmic FLOP."""
+    rows = [(kernel_label(n), m) for n, m in read_ncu_csv(path)]
+    bw = [m for label, m in rows if label.startswith("gemm") and (" B (" in label or " W (" in label)]
+    total = sum(m.get("dram__bytes_read.sum", 0.0) + m.get("dram__bytes_write.sum", 0.0) for m in bw)
+    return {"what": "DRAM bytes (read + write) of the captured B and W GEMM launches per algorithmic FLOP",
+            "dram_bytes_per_unit": total / bw_flops, "unit": "byte per FLOP", "launches": len(bw),
+            "algorithmic_flops": bw_flops, "command": command, "source_sha256": gemm_source_sha()}
+
+
+def profiled_traffic(name, workload, sources_sha):
+    """DRAM bytes per algorithmic unit from the committed data file profiles/<name>_<workload>.json
+    (written with --summarize-ncu --write-json from an ncu capture), or None when there is none or
+    the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{name}_{workload}.json")
     try:
         with open(path) as fh:
-            text = fh.read()
-    except OSError:
+            d = json.load(fh)
+    except (OSError, ValueError):
         return None, "no capture"
-    vals = {}
-    for line in text.splitlines():
-        if ":" in line and line.split(":")[0] in ("gemm_bw_dram_bytes_per_flop", "gemm_source_sha256"):
-            k, v = line.split(":", 1)
-            vals[k] = v.strip()
-    if vals.get("gemm_source_sha256") != gemm_source_sha() or "gemm_bw_dram_bytes_per_flop" not in vals:
-        return None, "GEMM sources changed since the capture"
-    return float(vals["gemm_bw_dram_bytes_per_flop"]), f"profiles/gemm_traffic_{workload}.md"
+    if d.get("source_sha256") != sources_sha or "dram_bytes_per_unit" not in d:
+        return None, "kernel sources changed since the capture"
+    return float(d["dram_bytes_per_unit"]), f"profiles/{name}_{workload}.json"
+
+
+def profiled_gemm_traffic(workload, w_mode):
+    """DRAM bytes per algorithmic FLOP of the B/W GEMMs (see profiled_traffic)."""
+    if w_mode != "per-microbatch":
+        return None, "no capture for this W mode"
+    return profiled_traffic("gemm_traffic", workload, gemm_source_sha())
 
 
 def measured_peaks():
@@ -734,9 +745,15 @@ def main():
     ap.add_argument("--ncu-command", default="", help="the command that wrote the CSV (for the summary)")
     ap.add_argument("--title", default="ncu launch list")
     ap.add_argument("--bw-flops", type=float, help="algorithmic FLOPs of the B/W GEMM launches in the CSV")
+    ap.add_argument("--write-json", metavar="PATH", help="with --summarize-ncu and --bw-flops: write the "
+                                                         "bytes-per-FLOP data file that roofline.traffic reads")
     args = ap.parse_args()
     if args.summarize_ncu:
         sys.stdout.write(summarize_ncu(args.summarize_ncu, args.ncu_command, args.title, args.bw_flops))
+        if args.write_json and args.bw_flops:
+            with open(args.write_json, "w") as fh:
+                json.dump(gemm_traffic_record(args.summarize_ncu, args.ncu_command, args.bw_flops), fh, indent=1)
+                fh.write("\n")
         return 0
     if args.op:
         return run_op(args)

@@ -38,8 +38,10 @@ def test_summary_shares_and_gemm_traffic(tmp_path):
     assert "| rmsnorm_bwd_kernel<2> | 1 | 0.10 | 10.0 % |" in text
     assert "| **total** | 4 | 1.00 | 100 % |" in text
     # B and W GEMM launches only: (20 + 2 + 30 + 40) MB over 4.6 GFLOP
-    assert "gemm_bw_dram_bytes_per_flop: 2.000000e-02" in text
-    assert f"gemm_source_sha256: {bench.gemm_source_sha()}" in text
+    assert "B/W GEMM DRAM bytes per algorithmic FLOP: 2.000000e-02" in text
+    rec = bench.gemm_traffic_record(str(csv), "ncu ... python bench.py", 4.6e9)
+    assert abs(rec["dram_bytes_per_unit"] - 2e-2) < 1e-12 and rec["launches"] == 2
+    assert rec["source_sha256"] == bench.gemm_source_sha()
 
 
 def test_traffic_lookup_needs_matching_sources(tmp_path, monkeypatch):
@@ -48,10 +50,10 @@ def test_traffic_lookup_needs_matching_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "gemm_source_sha", lambda: "abc")
     assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] is None
-    (prof / "gemm_traffic_w.md").write_text("x\ngemm_bw_dram_bytes_per_flop: 1.5e-4\ngemm_source_sha256: abc\n")
+    (prof / "gemm_traffic_w.json").write_text('{"dram_bytes_per_unit": 1.5e-4, "source_sha256": "abc"}')
     assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] == 1.5e-4
     assert bench.profiled_gemm_traffic("w", "flush")[0] is None
-    (prof / "gemm_traffic_w.md").write_text("gemm_bw_dram_bytes_per_flop: 1.5e-4\ngemm_source_sha256: old\n")
+    (prof / "gemm_traffic_w.json").write_text('{"dram_bytes_per_unit": 1.5e-4, "source_sha256": "old"}')
     assert bench.profiled_gemm_traffic("w", "per-microbatch")[0] is None
 
 
@@ -66,7 +68,7 @@ def test_summary_of_several_logs(tmp_path):
         paths.append(str(csv))
     text = bench.summarize_ncu(",".join(paths), "cmd", "t", bw_flops=1e9)
     assert "| gemm_pair_kernel W (float32 TMA reduce-add epilogue) | 2 | 0.00 | 100.0 % | 2.0 | 0.0 |" in text
-    assert "gemm_bw_dram_bytes_per_flop: 4.000000e-03" in text
+    assert "B/W GEMM DRAM bytes per algorithmic FLOP: 4.000000e-03" in text
 
 
 def test_reference_arm_json_line():
