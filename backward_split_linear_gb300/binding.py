@@ -108,6 +108,9 @@ _SIGS = {
     "zb_stage_sync": (c_int32, [c_void_p, c_void_p]),
     "zb_stage_stats": (c_int32, [c_void_p, ctypes.POINTER(c_int32), ctypes.POINTER(c_int32),
                                  ctypes.POINTER(c_size_t)]),
+    "zb_stage_stash_view": (c_int32, [c_void_p, c_int32, c_int32, c_int32, ctypes.POINTER(c_void_p),
+                                      ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                      ctypes.POINTER(c_int32)]),
     "zb_stage_set_tracing": (c_int32, [c_void_p, c_int32]),
     "zb_stage_read_tracing": (c_int32, [c_void_p, ctypes.POINTER(zb_kernel_stats), c_int32]),
 }
@@ -373,6 +376,20 @@ def zb_stage_stats(st):
     a, b, c = c_int32(0), c_int32(0), c_size_t(0)
     _check(lib().zb_stage_stats(st, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "zb_stage_stats")
     return a.value, b.value, c.value
+
+
+STASH_TENSORS = ["x", "rstd1", "n1", "a", "h", "rstd2", "n2", "gu", "s", "dy", "dn2", "dh", "dqkv", "dn1", "qkv",
+                 "lse"]
+
+
+def zb_stage_stash_view(st, mb, layer, tensor):
+    """(device address, rows, cols, element bytes) of one stashed tensor; `tensor` is a name of
+    STASH_TENSORS or its index."""
+    idx = STASH_TENSORS.index(tensor) if isinstance(tensor, str) else int(tensor)
+    ptr, rows, cols, eb = c_void_p(0), ctypes.c_int64(0), ctypes.c_int64(0), c_int32(0)
+    _check(lib().zb_stage_stash_view(st, mb, layer, idx, ctypes.byref(ptr), ctypes.byref(rows), ctypes.byref(cols),
+                                     ctypes.byref(eb)), "zb_stage_stash_view")
+    return ptr.value or 0, rows.value, cols.value, eb.value
 
 
 def zb_stage_set_tracing(st, enable):

@@ -1013,6 +1013,46 @@ extern "C" zb_status zb_stage_stats(zb_stage_t st, int32_t* inflight, int32_t* p
     return ZB_OK;
 }
 
+extern "C" zb_status zb_stage_stash_view(zb_stage_t st, int32_t mb, int32_t layer, int32_t tensor,
+                                        const void** ptr, int64_t* rows, int64_t* cols, int32_t* elem_bytes) {
+    if (!st || !ptr || !rows || !cols || !elem_bytes || mb < 0) return ZB_ERR_ARG;
+    const zb_stage_config& c = st->cfg;
+    if (layer < 0 || layer >= c.n_layers || tensor < 0 || tensor >= ZB_STASH_COUNT) return ZB_ERR_ARG;
+    auto it = st->mbs.find(mb);
+    if (it == st->mbs.end()) return ZB_ERR_NO_MB;
+    const LayerSlot& L = st->lay.layers[layer];
+    const int64_t t = it->second.tokens;
+    const int64_t H = c.hidden, F = c.ffn, Q = c.kind == ZB_LAYER_TRANSFORMER ? qkv_width(c) : 0;
+    const Region* r = nullptr;
+    int64_t nr = t, nc = H;
+    int32_t eb = 2;
+    switch (tensor) {
+        case ZB_STASH_X: r = &L.x; break;
+        case ZB_STASH_RSTD1: r = &L.r1; nc = 1; eb = 4; break;
+        case ZB_STASH_N1: r = &L.n1; break;
+        case ZB_STASH_A: r = &L.a; break;
+        case ZB_STASH_H: r = &L.h; break;
+        case ZB_STASH_RSTD2: r = &L.r2; nc = 1; eb = 4; break;
+        case ZB_STASH_N2: r = &L.n2; break;
+        case ZB_STASH_GU: r = &L.gu; nc = 2 * F; break;
+        case ZB_STASH_S: r = &L.s; nc = F; break;
+        case ZB_STASH_DY: r = &L.dy; nc = c.kind == ZB_LAYER_LINEAR ? F : H; break;
+        case ZB_STASH_DN2: r = &L.dn2; break;
+        case ZB_STASH_DH: r = &L.dh; break;
+        case ZB_STASH_DQKV: r = &L.dqkv; nc = Q; break;
+        case ZB_STASH_DN1: r = &L.dn1; break;
+        case ZB_STASH_QKV: r = &L.qkv; nc = Q; break;
+        case ZB_STASH_LSE: r = &L.lse; nr = c.n_heads; nc = st->lay.ld_stat; eb = 4; break;
+        default: return ZB_ERR_ARG;
+    }
+    if (!r || r->off == kNone) return ZB_ERR_ARG;  // not stashed for this layer kind
+    *ptr = st->ws + r->off + r->stride * static_cast<size_t>(it->second.slot);
+    *rows = nr;
+    *cols = nc;
+    *elem_bytes = eb;
+    return ZB_OK;
+}
+
 extern "C" zb_status zb_stage_set_tracing(zb_stage_t st, int32_t enable) {
     if (!st) return ZB_ERR_ARG;
     st->tr.on = enable != 0;

@@ -93,6 +93,17 @@ class Stage:
     def stats(self):
         return zb.zb_stage_stats(self.handle)
 
+    def stash(self, mb, layer, name):
+        """A view (no copy) of one stashed tensor of microbatch `mb`, layer `layer`, inside the
+        workspace: bf16 [rows, cols] or float32 [rows, cols].  Valid until the microbatch's W."""
+        ptr, rows, cols, eb = zb.zb_stage_stash_view(self.handle, mb, layer, name)
+        off = ptr - self.workspace.data_ptr()
+        nbytes = rows * cols * eb
+        if off < 0 or off + nbytes > self.workspace.numel():
+            raise zb.ZBError(-1, "zb_stage_stash_view (address outside the workspace)")
+        raw = self.workspace[off:off + nbytes]
+        return raw.view(torch.bfloat16 if eb == 2 else torch.float32).view(rows, cols)
+
     def set_tracing(self, enable):
         zb.zb_stage_set_tracing(self.handle, enable)
 

@@ -412,6 +412,46 @@ zb_status zb_stage_stats(zb_stage_t st, int32_t* inflight, int32_t* peak_infligh
                          size_t* stash_bytes);
 
 /* ------------------------------------------------------------------------
+ * Read-only view of the activation stash, for tests and diagnostics.  An
+ * oracle that takes a layer's inputs from here consumes exactly the bf16
+ * values the kernels consumed, so each step of every layer can be checked
+ * against the plain definition on its own (the guide's section "2.
+ * Convergence and Numerical Stability": B and W are the plain backward's
+ * arithmetic, split), apart from the roundings of the steps before it.
+ * ---------------------------------------------------------------------- */
+typedef enum {
+    ZB_STASH_X = 0,    /* layer input x [T, H] (LINEAR: [T, hidden]); MLP: also h */
+    ZB_STASH_RSTD1,    /* float32 [T], TRANSFORMER */
+    ZB_STASH_N1,       /* RMSNorm(x; gamma1) [T, H], TRANSFORMER */
+    ZB_STASH_A,        /* attention output [T, H], TRANSFORMER */
+    ZB_STASH_H,        /* x + a W_o^T [T, H] (MLP: the same region as x) */
+    ZB_STASH_RSTD2,    /* float32 [T] */
+    ZB_STASH_N2,       /* RMSNorm(h; gamma2) [T, H] */
+    ZB_STASH_GU,       /* [T, 2F]: [g | u] after F; [dg | du] once B ran (written in place) */
+    ZB_STASH_S,        /* silu(g) * u [T, F] */
+    ZB_STASH_DY,       /* the layer's output gradient [T, H] (LINEAR: [T, ffn]); written by B */
+    ZB_STASH_DN2,      /* dgu W_gu [T, H]; written by B */
+    ZB_STASH_DH,       /* gradient of h [T, H], TRANSFORMER; written by B */
+    ZB_STASH_DQKV,     /* [T, (nh + 2 nkv) hd], TRANSFORMER; written by B */
+    ZB_STASH_DN1,      /* dqkv W_qkv [T, H], TRANSFORMER; written by B */
+    ZB_STASH_QKV,      /* attention input [T, (nh + 2 nkv) hd], ZB_ATTN_CAUSAL only */
+    ZB_STASH_LSE,      /* float32 [nh, zb_op_attention_stat_stride(max_tokens)], ZB_ATTN_CAUSAL only */
+    ZB_STASH_COUNT
+} zb_stash_tensor;
+
+/* Device address, shape and element size (2: bf16, 4: float32) of one stashed
+ * tensor of layer `layer` of microbatch `mb` (rows are the microbatch's T
+ * tokens, or the heads for ZB_STASH_LSE; rows are dense, `cols` elements
+ * apart).  The address points into the caller's workspace and holds the
+ * tensor from the call that writes it (F, or B for the gradients) until the
+ * microbatch's W; read it only after `stream` has passed that call.  Nothing
+ * is enqueued.  Errors: ZB_ERR_NO_MB (mb not between F and W), ZB_ERR_ARG
+ * (layer outside [0, n_layers), a tensor this layer kind does not stash, a
+ * NULL output pointer). */
+zb_status zb_stage_stash_view(zb_stage_t st, int32_t mb, int32_t layer, int32_t tensor, const void** ptr,
+                              int64_t* rows, int64_t* cols, int32_t* elem_bytes);
+
+/* ------------------------------------------------------------------------
  * Per-launch tracing (the guide's section "Operational Checklist" asks for
  * per-stage telemetry; this is its per-kernel form).  When enabled, the stage
  * records a CUDA event pair on the call's stream around every launch and

@@ -14,12 +14,17 @@ float64 oracle therefore use Frobenius <= 5e-3 * sqrt(4 L) for L layers
 
 A layer with the causal softmax core adds roundings on both paths (P for the
 P V and dV products, the bf16 output a, dS) and the exponential amplifies the
-rounding of q and k.  tests/bf16_emulation.py replays the causal 8B-shaped
+rounding of q and k.  tests/bf16_replay.py replays the causal 8B-shaped
 two-layer stage with every stored tensor rounded: Frobenius up to 1.61e-2
 (top layer's dW_qkv) and max-abs up to 1.94e-2 (its dgamma1); the GPU gives
 1.59e-2 and 1.70e-2 there.  Causal stages therefore count eight roundings a
 layer: Frobenius <= 5e-3 * sqrt(8 L) (2e-2 for two layers) and max-abs
 <= 3e-2 * max|ref|.
+
+tests/test_bf16_replay.py holds every whole-stage bound between the replay's
+error and a small multiple of it.  Kernel errors are checked apart from the
+roundings of earlier steps by tests/test_gpu_stash_fed.py, at the single-step
+bar, on the stashed bf16 inputs of each step.
 """
 import numpy as np
 

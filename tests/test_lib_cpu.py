@@ -140,6 +140,14 @@ def test_stage_host_errors_without_device(zblib):
         assert e.value.name == "ZB_ERR_SHAPE"  # tokens > max_tokens
         assert zb.zb_stage_stats(st) == (0, 0, 0)
         zb.zb_wgrad_flush(st, 0)  # nothing pending: no device call
+        # the stash view of a microbatch that is not in flight, or of a bad layer or tensor
+        with pytest.raises(zb.ZBError) as e:
+            zb.zb_stage_stash_view(st, 0, 0, "x")
+        assert e.value.name == "ZB_ERR_NO_MB"
+        for layer, tensor in ((1, "x"), (-1, "x"), (0, len(zb.STASH_TENSORS))):
+            with pytest.raises(zb.ZBError) as e:
+                zb.zb_stage_stash_view(st, 0, layer, tensor)
+            assert e.value.name == "ZB_ERR_ARG"
     finally:
         zb.zb_stage_destroy(st)
 
@@ -210,3 +218,15 @@ def test_noalloc_size_rule_holds_for_every_width(zblib):
             assert 0 < nbytes <= cap, (t, hidden, nbytes)
     # past the promise the partition needs more than the array for long inputs
     assert zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(1 << 20, 131072 + 64) > cap
+
+
+def test_stash_tensor_names_follow_the_header():
+    """binding.STASH_TENSORS is the zb_stash_tensor enum of include/zb.h, in order."""
+    import re
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "include", "zb.h")) as fh:
+        text = fh.read()
+    body = text[text.index("typedef enum {\n    ZB_STASH_X"):text.index("} zb_stash_tensor;")]
+    names = [n.lower() for n in re.findall(r"ZB_STASH_([A-Z0-9]+)", body) if n != "COUNT"]
+    assert names == zb.STASH_TENSORS
