@@ -50,7 +50,7 @@ class zb_kernel_stats(ctypes.Structure):
 
 
 KERNEL_CLASSES = ["gemm_forward", "gemm_backward_input", "gemm_backward_weight", "row_backward_input",
-                  "row_backward_weight", "row_forward", "attn_forward", "attn_backward"]
+                  "row_backward_weight", "row_forward", "attn_forward", "attn_backward", "stash_copy"]
 ATTENTION_KINDS = {"standin": 0, "causal": 1}
 
 

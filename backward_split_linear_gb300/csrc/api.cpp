@@ -678,13 +678,12 @@ zb_status check_layer_params(const zb_stage_config& c, const zb_layer_params& p)
     return ZB_ERR_ARG;
 }
 
-// Stash copy of a caller tensor (x at F, dy at B), booked with F's or B's row
-// kernels: its time and bytes count, but not as a launch (it is a copy, not one
-// of the library's kernels).
-zb_status stash_copy(zb_stage* st, zb_kernel_class cls, void* dst, const void* src, size_t bytes,
-                     cudaStream_t s) {
+// Stash copy of a caller tensor (x at F, dy at B), booked in its own class: its
+// time and bytes count, but not as a launch (it is a copy, not one of the
+// library's kernels).
+zb_status stash_copy(zb_stage* st, void* dst, const void* src, size_t bytes, cudaStream_t s) {
     if (!bytes) return ZB_OK;
-    return traced(st, cls, 0, 0.0, 2.0 * bytes, s, [&] {
+    return traced(st, ZB_KCLASS_STASH_COPY, 0, 0.0, 2.0 * bytes, s, [&] {
         return cuda_status(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s));
     });
 }
@@ -694,7 +693,7 @@ zb_status stage_forward_body(zb_stage* st, int slot, const void* x, int t, void*
     const zb_stage_config& c = st->cfg;
     const int H = c.hidden, F = c.ffn, Q = qkv_width(c);
     const double T = t;
-    ZB_TRY(stash_copy(st, ZB_KCLASS_ROW_FORWARD, st->at(slot, st->lay.layers[0].x), x, static_cast<size_t>(t) * H * 2, s));
+    ZB_TRY(stash_copy(st, st->at(slot, st->lay.layers[0].x), x, static_cast<size_t>(t) * H * 2, s));
     if (t == 0) return ZB_OK;
     SplitWs ws;
     ZB_TRY(stage_split_ws(st, s, &ws));
@@ -762,7 +761,7 @@ zb_status stage_backward_input_body(zb_stage* st, int slot, const void* dy, void
     const double T = t;
     const int top = c.n_layers - 1;
     const int out_dim = c.kind == ZB_LAYER_LINEAR ? F : H;
-    ZB_TRY(stash_copy(st, ZB_KCLASS_ROW_BACKWARD_INPUT, st->at(slot, st->lay.layers[top].dy), dy, static_cast<size_t>(t) * out_dim * 2, s));
+    ZB_TRY(stash_copy(st, st->at(slot, st->lay.layers[top].dy), dy, static_cast<size_t>(t) * out_dim * 2, s));
     if (t == 0) return ZB_OK;
     SplitWs ws;
     ZB_TRY(stage_split_ws(st, s, &ws));

@@ -67,18 +67,28 @@ def gemm_flops_per_mb(w):
 # ---------------------------------------------------------------- ncu summaries
 
 GEMM_SOURCES = ("gemm.cu", "device_common.cuh", "launch.h")
+ROW_SOURCES = ("rowops.cu", "device_common.cuh", "launch.h")
 EPILOGUES = {0: "bf16 store", 1: "residual epilogue", 2: "SwiGLU backward epilogue", 3: "float32 TMA reduce-add epilogue"}
+
+
+def _sources_sha(names):
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "backward_split_linear_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def gemm_source_sha():
     """sha256 over the GEMM kernel sources: a stored traffic figure holds only for these bytes."""
-    import hashlib
+    return _sources_sha(GEMM_SOURCES)
 
-    h = hashlib.sha256()
-    for name in GEMM_SOURCES:
-        with open(os.path.join(ROOT, "backward_split_linear_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
-    return h.hexdigest()
+
+def row_source_sha():
+    """sha256 over the row kernels' sources (see gemm_source_sha)."""
+    return _sources_sha(ROW_SOURCES)
 
 
 def kernel_label(name):
@@ -162,6 +172,22 @@ def summarize_ncu(path, command, title, bw_flops=None):
             out += ["", f"B/W GEMM DRAM bytes per algorithmic FLOP: {total / bw_flops:.6e} "
                         f"(GEMM sources sha256 {gemm_source_sha()[:16]}...)"]
     return "\n".join(out) + "\n"
+
+
+ROW_KERNELS = ("rmsnorm_bwd_kernel", "attn_bwd_kv_kernel", "dgamma_partial_kernel", "dgamma_final_kernel")
+
+
+def row_traffic_record(path, command, algorithmic_bytes):
+    """The data file bench.py reads for roofline_rows.traffic: DRAM bytes of the captured B/W row
+    kernel launches per algorithmic byte (`algorithmic_bytes`: their total, counted as the
+    library's tracing counts them)."""
+    rows = [(kernel_label(n), m) for n, m in read_ncu_csv(path)]
+    sel = [m for label, m in rows if label.split("<")[0] in ROW_KERNELS]
+    total = sum(m.get("dram__bytes_read.sum", 0.0) + m.get("dram__bytes_write.sum", 0.0) for m in sel)
+    return {"what": "DRAM bytes (read + write) of the captured B and W row-kernel launches per algorithmic byte",
+            "dram_bytes_per_unit": total / algorithmic_bytes, "unit": "byte per algorithmic byte",
+            "launches": len(sel), "algorithmic_bytes": algorithmic_bytes, "command": command,
+            "source_sha256": row_source_sha()}
 
 
 def gemm_traffic_record(path, command, bw_flops):
@@ -363,6 +389,182 @@ def run_reference(args, w):
 # ---------------------------------------------------------------- GPU leg
 
 
+def run_order(st, order, xs, ys, dys, dxs, stream, ev, record, before=None, after=None):
+    """One step: the (kind, mb) ops of `order` through the stage ('X': one flush).  With
+    `record`, CUDA events from `ev` bracket every B and W call on `stream`; returns the
+    (pass, start, end) spans."""
+    i_ev = 0
+    spans = []
+    for kind, mb in order:
+        if before is not None:
+            before(kind, mb)
+        if kind == "F":
+            st.forward(mb, xs[mb], ys[mb], stream)
+            continue
+        a, b = ev[i_ev]
+        i_ev += 1
+        if record:
+            a.record(stream)
+        if kind == "B":
+            st.backward_input(mb, dys[mb], dxs[mb], stream)
+        elif kind == "W":
+            st.backward_weight(mb, stream)
+        else:
+            st.flush(stream)
+        if record:
+            b.record(stream)
+            spans.append(("B" if kind == "B" else "W", a, b))
+        if after is not None:
+            after(kind, mb)
+    return spans
+
+
+def measure_config(w, order, steps, warmup, peaks, peak_key, params=None, seed=0):
+    """A further workload of the list, timed like the headline on a stage of its own: `warmup`
+    untimed steps, then `steps` steps with events around every B and W call.  Returns its
+    B / W TFLOP/s, the GEMM fraction of `peak_key`'s peak, the row kernels' share and the
+    stash it held.  `params` reuses device weights of the same shapes."""
+    import torch
+
+    from backward_split_linear_gb300 import synth
+    from backward_split_linear_gb300.runtime import Stage, bf16_from_bits
+
+    t = w["tokens"]
+    n_mb = 1 + max(mb for _, mb in order if mb >= 0)
+    slots = w.get("slots", n_mb)
+    inp = synth.stage_inputs(w["kind"], w["n_layers"] if params is None else 0, w["hidden"], w["ffn"], w["n_heads"],
+                             w["n_kv_heads"], w["head_dim"], tokens=t, n_mb=n_mb, seed=seed, gamma="ones")
+    if params is None:
+        st = Stage.from_synth(w["kind"], w["n_layers"], w["hidden"], w["ffn"], w["n_heads"], w["n_kv_heads"],
+                              w["head_dim"], 1e-5, t, slots, inp["params"], attention=w.get("attention", "standin"),
+                              seq_len=w.get("seq_len", 0))
+    else:
+        st = Stage(w["kind"], w["n_layers"], w["hidden"], w["ffn"], w["n_heads"], w["n_kv_heads"], w["head_dim"],
+                   1e-5, t, slots, params, attention=w.get("attention", "standin"), seq_len=w.get("seq_len", 0))
+    xs = [bf16_from_bits(b) for b in inp["x"]]
+    dys = [bf16_from_bits(b) for b in inp["dy"]]
+    ys = [torch.empty(t, st.out_dim, dtype=torch.bfloat16, device="cuda") for _ in range(n_mb)]
+    dxs = [torch.empty(t, w["hidden"], dtype=torch.bfloat16, device="cuda") for _ in range(n_mb)]
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for k, _ in order if k != "F"]
+    st.set_tracing(True)
+    for _ in range(warmup):
+        run_order(st, order, xs, ys, dys, dxs, stream, ev, False)
+    st.sync()
+    st.read_tracing(reset=True)
+    torch.cuda.synchronize()
+    b_ms = w_ms = 0.0
+    n_b = n_w = 0
+    for _ in range(steps):
+        spans = run_order(st, order, xs, ys, dys, dxs, stream, ev, True)
+        torch.cuda.synchronize()
+        for kind, a, b in spans:
+            if kind == "B":
+                b_ms += a.elapsed_time(b)
+                n_b += 1
+            else:
+                w_ms += a.elapsed_time(b)
+                n_w += 1
+    trace = st.read_tracing(reset=True)
+    st.sync()
+    peak_inflight = st.stats()[1]
+    st.close()
+    flops_mb = gemm_flops_per_mb(w)
+    b_fl = w_fl = flops_mb * n_mb * steps
+    gemm = [trace[k] for k in ("gemm_backward_input", "gemm_backward_weight")]
+    g_ms = sum(c["ms"] for c in gemm)
+    g_ach = sum(c["flops"] for c in gemm) / (g_ms * 1e-3) / 1e12
+    rows = [trace[k] for k in ("row_backward_input", "row_backward_weight")]
+    r_ms = sum(c["ms"] for c in rows)
+    peak = peaks[peak_key]
+    rec = {"value": (b_fl + w_fl) / ((b_ms + w_ms) * 1e-3) / 1e12,
+           "b_tflops": b_fl / (b_ms * 1e-3) / 1e12, "w_tflops": w_fl / (w_ms * 1e-3) / 1e12,
+           "pct_of_dense_bf16_peak": {"b": 100 * b_fl / (b_ms * 1e-3) / 1e12 / peak,
+                                      "w": 100 * w_fl / (w_ms * 1e-3) / 1e12 / peak, "peak_tflops": peak,
+                                      "peak_source": f"{peaks['source']} {peak_key}"},
+           "gemm_roofline_frac": g_ach / peak,
+           "row_kernels_share_of_bw_time": r_ms / (b_ms + w_ms),
+           "ms_per_call": {"B": b_ms / max(1, n_b), "W": w_ms / max(1, n_w)},
+           "peak_inflight": peak_inflight, "steps": steps, "warmup": warmup}
+    if w.get("attention") == "causal":
+        ab = trace["attn_backward"]
+        rec["attention_bwd_tflops"] = ab["flops"] / (ab["ms"] * 1e-3) / 1e12 if ab["ms"] else None
+        rec["attention_bwd_share_of_b_time"] = ab["ms"] / b_ms if b_ms else None
+    return rec
+
+
+def wgrad_sweep_record(tokens, steps, warmup, peaks):
+    """One linear (in 4096, out 14336), m = 4 microbatches of `tokens` tokens: W per microbatch
+    (after each B) and W of all four batched by one flush, each against the roofline that binds
+    it: tensor time 2 T in out / peak against DRAM time (2 T (in + out) + 8 in out) / HBM peak
+    (the float32 dW read and written once per W)."""
+    from backward_split_linear_gb300 import binding as zb
+
+    m, n_in, n_out = 4, 4096, 14336
+    w = dict(kind="linear", n_layers=1, hidden=n_in, ffn=n_out, n_heads=0, n_kv_heads=0, head_dim=0, tokens=tokens,
+             m=m)
+    out = {}
+    for mode, order in (("per_microbatch", zb.zb_schedule("zbh1", 0, m, m)),
+                        ("flush", [("F", i) for i in range(m)] + [("B", i) for i in range(m)] + [("X", -1)])):
+        rec = measure_config(w, order, steps, warmup, peaks, "bf16_tflops")
+        t_w = tokens if mode == "per_microbatch" else m * tokens
+        flops = 2.0 * t_w * n_in * n_out
+        nbytes = 2.0 * t_w * (n_in + n_out) + 8.0 * n_in * n_out
+        t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+        w_calls = m if mode == "per_microbatch" else 1
+        t_meas = rec["ms_per_call"]["W"] * 1e-3
+        out[mode] = {"w_tflops": rec["w_tflops"], "b_tflops": rec["b_tflops"],
+                     "w_pct_of_dense_bf16_peak": rec["pct_of_dense_bf16_peak"]["w"],
+                     "w_tokens_per_call": t_w, "w_calls_per_step": w_calls,
+                     "binding_roofline": "hbm" if t_hbm > t_tensor else "tensor",
+                     "w_frac_of_binding_roofline": max(t_hbm, t_tensor) / t_meas,
+                     "w_hbm_gbs": nbytes / t_meas / 1e9}
+    return out
+
+
+def other_configs(args, st, peaks):
+    """The rest of the workload list, each timed on its own stage after the headline: the
+    70B-shaped stage, the ZB-H1 order of stage 3 of p = 8 over 16 microbatches (on the
+    headline's weights), the 8B-shaped stage with the causal attention core, and the wgrad
+    token sweep.  Steps are capped at 5 (at least 3 warm-up steps each)."""
+    import torch
+
+    from backward_split_linear_gb300 import binding as zb
+
+    steps, warmup = max(1, min(args.steps, 5)), 3
+    params = st.params
+    st.close()
+    st.workspace = st.grads = None
+    torch.cuda.empty_cache()
+    out = {"note": "each workload on a stage of its own after the headline's timed region; same timing "
+                   "(events around every B and W call, F untimed); stage GEMM fractions against the "
+                   "sustained peak, the sweep against the burst peak (short steps)"}
+    w8 = dict(WORKLOADS["llama8b_stage"], slots=8)
+    rec = measure_config(w8, zb.zb_schedule("zbh1", 3, 8, 16), steps, warmup, peaks, "bf16_tflops_sustained",
+                         params=params)
+    rec["order"] = "ZB-H1 order of stage 3 of p = 8, m = 16 (library generator), 8 stash slots"
+    out["config4_zbh1_stage3_p8_m16"] = rec
+    del params
+    torch.cuda.empty_cache()
+    w70 = WORKLOADS["llama70b_stage"]
+    rec = measure_config(w70, zb.zb_schedule("zbh1", 0, w70["m"], w70["m"]), steps, warmup, peaks,
+                         "bf16_tflops_sustained")
+    rec["order"] = "ZB-H1 order of stage 0 of p = m = 8"
+    out["llama70b_stage"] = rec
+    torch.cuda.empty_cache()
+    wc = WORKLOADS["llama8b_stage_causal"]
+    rec = measure_config(wc, zb.zb_schedule("zbh1", 0, wc["m"], wc["m"]), steps, warmup, peaks,
+                         "bf16_tflops_sustained")
+    rec["order"] = "ZB-H1 order of stage 0 of p = m = 8"
+    out["llama8b_stage_causal"] = rec
+    torch.cuda.empty_cache()
+    out["wgrad_sweep_in4096_out14336_m4"] = {f"t{t}": wgrad_sweep_record(t, steps, warmup, peaks)
+                                              for t in (512, 1024, 2048, 4096, 8192)}
+    return out
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -408,30 +610,7 @@ def run_ours(args, w):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_b)]
 
     def step(record, before=None, after=None):
-        i_ev = 0
-        spans = []
-        for kind, mb in order:
-            if before is not None:
-                before(kind, mb)
-            if kind == "F":
-                st.forward(mb, xs[mb], ys[mb], stream)
-                continue
-            a, b = ev[i_ev]
-            i_ev += 1
-            if record:
-                a.record(stream)
-            if kind == "B":
-                st.backward_input(mb, dys[mb], dxs[mb], stream)
-            elif kind == "W":
-                st.backward_weight(mb, stream)
-            else:
-                st.flush(stream)
-            if record:
-                b.record(stream)
-                spans.append(("B" if kind == "B" else "W", a, b))
-            if after is not None:
-                after(kind, mb)
-        return spans
+        return run_order(st, order, xs, ys, dys, dxs, stream, ev, record, before, after)
 
     st.set_tracing(True)
     # stash bytes one microbatch holds between its F and its W
@@ -568,11 +747,22 @@ def run_ours(args, w):
                 "ms_per_launch": g_ms / max(1, g_launch)}
     roofline_rows = None
     if r_ach is not None:
+        r_launch = sum(c["launches"] for c in rows.values())
+        # DRAM bytes of an average row-kernel launch: the captured bytes per algorithmic byte times
+        # this run's algorithmic bytes per launch
+        row_ratio, row_src = profiled_traffic("row_traffic", args.workload, row_source_sha()) if not args.overridden \
+            else (None, "workload overridden")
         roofline_rows = {"bound": "hbm", "kernel": "B/W row kernels (RMSNorm backward, stand-in backward, "
-                                                   "gamma reduction, dy stash copy)",
+                                                   "gamma reduction)",
                          "achieved": r_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": r_ach / peaks["hbm_gbs"],
-                         "traffic": None, "launches": sum(c["launches"] for c in rows.values()),
-                         "share_of_bw_time": r_ms / bw_ms}
+                         "traffic": row_ratio * r_bytes / max(1, r_launch) if row_ratio else None,
+                         "traffic_source": row_src, "launches": r_launch,
+                         "bytes_per_launch": r_bytes / max(1, r_launch), "share_of_bw_time": r_ms / bw_ms}
+    copy = trace.get("stash_copy")
+    stash_copy = None
+    if copy and copy["ms"] > 0:
+        stash_copy = {"what": "stash copies of the caller's x (F) and dy (B), cudaMemcpyAsync device to device",
+                      "gbs": copy["bytes"] / (copy["ms"] * 1e-3) / 1e9, "ms": copy["ms"]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -602,7 +792,7 @@ def run_ours(args, w):
                        "timed": "CUDA events around each B and W call; F runs in the step, untimed",
                        "l2": "inputs larger than L2 (stash per microbatch far above 129 MB)",
                        "gamma": "ones", "seed": rank},
-            "roofline": roofline, "roofline_rows": roofline_rows,
+            "roofline": roofline, "roofline_rows": roofline_rows, "stash_copy": stash_copy,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": {"sm_mhz": cs["sm_mhz"], "sm_max_mhz": cs["sm_max_mhz"], "reasons": cs["reasons"],
                        "samples": cs["samples"]},
@@ -640,6 +830,9 @@ def run_ours(args, w):
                 "bwd_share_of_b_time": ab["ms"] / b_ms if b_ms else None,
                 "b_tflops_with_attention": (b_flops + ab["flops"]) / (b_ms * 1e-3) / 1e12,
             }
+        if (world == 1 and args.workload == "llama8b_stage" and args.w_mode == "per-microbatch"
+                and not args.overridden and args.stage == 0 and not args.pipeline and not args.no_configs):
+            line["configs"] = other_configs(args, st, peaks)
         print(json.dumps(line), flush=True)
     st.close()
     if dist is not None:
@@ -731,6 +924,8 @@ def main():
                     help="tokens of the microbatch the host oracle runs (cpu_baseline / reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the sub-records of the other workloads (70B, config 4, causal, wgrad sweep)")
     ap.add_argument("--w-mode", choices=["per-microbatch", "flush"], default="per-microbatch",
                     help="W as one call per microbatch (the ZB-H1 order) or batched in one flush")
     ap.add_argument("--op", choices=["backward_weight", "backward_input", "backward_input_swiglu", "forward",
@@ -745,14 +940,17 @@ def main():
     ap.add_argument("--ncu-command", default="", help="the command that wrote the CSV (for the summary)")
     ap.add_argument("--title", default="ncu launch list")
     ap.add_argument("--bw-flops", type=float, help="algorithmic FLOPs of the B/W GEMM launches in the CSV")
+    ap.add_argument("--row-bytes", type=float, help="algorithmic bytes of the B/W row-kernel launches in the CSV")
     ap.add_argument("--write-json", metavar="PATH", help="with --summarize-ncu and --bw-flops: write the "
                                                          "bytes-per-FLOP data file that roofline.traffic reads")
     args = ap.parse_args()
     if args.summarize_ncu:
         sys.stdout.write(summarize_ncu(args.summarize_ncu, args.ncu_command, args.title, args.bw_flops))
-        if args.write_json and args.bw_flops:
+        if args.write_json and (args.bw_flops or args.row_bytes):
+            rec = (gemm_traffic_record(args.summarize_ncu, args.ncu_command, args.bw_flops) if args.bw_flops else
+                   row_traffic_record(args.summarize_ncu, args.ncu_command, args.row_bytes))
             with open(args.write_json, "w") as fh:
-                json.dump(gemm_traffic_record(args.summarize_ncu, args.ncu_command, args.bw_flops), fh, indent=1)
+                json.dump(rec, fh, indent=1)
                 fh.write("\n")
         return 0
     if args.op:

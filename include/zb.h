@@ -463,12 +463,14 @@ typedef enum {
     ZB_KCLASS_GEMM_FORWARD = 0,      /* F GEMMs */
     ZB_KCLASS_GEMM_BACKWARD_INPUT,   /* B GEMMs, incl. the fused SwiGLU backward */
     ZB_KCLASS_GEMM_BACKWARD_WEIGHT,  /* W GEMMs (float32 accumulation) */
-    ZB_KCLASS_ROW_BACKWARD_INPUT,    /* B row kernels: RMSNorm backward, stand-in
-                                        backward, and the stash copy of dy */
+    ZB_KCLASS_ROW_BACKWARD_INPUT,    /* B row kernels: RMSNorm backward, stand-in backward */
     ZB_KCLASS_ROW_BACKWARD_WEIGHT,   /* W row kernels: gamma-gradient reduction */
-    ZB_KCLASS_ROW_FORWARD,           /* F row kernels and the stash copy of x */
+    ZB_KCLASS_ROW_FORWARD,           /* F row kernels */
     ZB_KCLASS_ATTN_FORWARD,          /* F causal attention */
     ZB_KCLASS_ATTN_BACKWARD,         /* B causal attention (rowsum, dK/dV, dQ kernels) */
+    ZB_KCLASS_STASH_COPY,            /* the stash copies of the caller's x (F) and dy (B):
+                                        device-to-device cudaMemcpyAsync, not a kernel of the
+                                        library (time and bytes count, launches do not) */
     ZB_KCLASS_COUNT
 } zb_kernel_class;
 

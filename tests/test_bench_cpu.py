@@ -93,3 +93,19 @@ def test_reference_arm_json_line():
     for key, val in bench.WORKLOADS["tiny_stage"].items():
         assert d["config"][key] == val, key
     assert d["config"]["sample_tokens_per_step"] > 0
+
+
+def test_row_traffic_record(tmp_path):
+    """Row-kernel DRAM bytes per algorithmic byte, from the B/W row launches of a capture only."""
+    csv = tmp_path / "r.csv"
+    lines = [HEADER]
+    for i, (name, rd, wr) in enumerate([(R, 6.0, 2.0), (W, 100.0, 100.0),
+                                        ("void <unnamed>::dgamma_final_kernel(<unnamed>::GammaBatch, const float *)",
+                                         1.0, 1.0)]):
+        lines.append(row(i, name, "gpu__time_duration.sum", "ns", "1000"))
+        lines.append(row(i, name, "dram__bytes_read.sum", "Mbyte", rd))
+        lines.append(row(i, name, "dram__bytes_write.sum", "Mbyte", wr))
+    csv.write_text("".join(lines))
+    rec = bench.row_traffic_record(str(csv), "cmd", 5e6)
+    assert rec["launches"] == 2 and abs(rec["dram_bytes_per_unit"] - 2.0) < 1e-12
+    assert rec["source_sha256"] == bench.row_source_sha()

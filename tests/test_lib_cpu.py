@@ -230,3 +230,13 @@ def test_stash_tensor_names_follow_the_header():
     body = text[text.index("typedef enum {\n    ZB_STASH_X"):text.index("} zb_stash_tensor;")]
     names = [n.lower() for n in re.findall(r"ZB_STASH_([A-Z0-9]+)", body) if n != "COUNT"]
     assert names == zb.STASH_TENSORS
+
+
+def test_kernel_class_names_follow_the_header():
+    """binding.KERNEL_CLASSES is the zb_kernel_class enum of include/zb.h, in order."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "include", "zb.h")) as fh:
+        text = fh.read()
+    body = text[text.index("    ZB_KCLASS_GEMM_FORWARD = 0"):text.index("} zb_kernel_class;")]
+    names = [n.lower() for n in re.findall(r"ZB_KCLASS_([A-Z_]+)", body) if n != "COUNT"]
+    assert names == zb.KERNEL_CLASSES
