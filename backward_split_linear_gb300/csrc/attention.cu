@@ -7,10 +7,12 @@
 // ("Zero-Bubble Pipeline Parallelism Guide for LLMs", "Core Innovation 1");
 // the core has no weights, so all of its backward belongs to B.
 //
-// Three kernels, each one CTA per 128-row tile, 192 threads:
+// Three kernels, each one CTA per 128-row tile:
 //   warp 0     one thread issues TMA loads
 //   warp 1     allocates tensor memory; one thread issues tcgen05.mma
 //   warps 2-5  one row each: softmax / gradient arithmetic, epilogue
+//   warps 6-9  (backward kernels) a second group of row warps, on every other
+//              64-wide sub-block
 //
 //   attn_causal_fwd_kernel   (head h, query block):  S = Q K^T -> online softmax ->
 //                     O += P V over the key blocks up to the diagonal; writes
@@ -43,6 +45,9 @@ namespace zbk {
 namespace {
 
 constexpr int kAttnThreads = 192;
+// The backward kernels run two groups of four row warps (warps 2-5 and 6-9),
+// each on every other sub-block.
+constexpr int kAttnBwdThreads = 320;
 constexpr int kRows = 128;             // query and key block
 // Every attention CTA allocates all 512 tensor-memory columns; asking for at
 // least this much shared memory keeps two CTAs off one SM (the second would
@@ -107,6 +112,19 @@ __device__ __forceinline__ float lg2(float x) {
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* status) {
     const bool ok = mbar_wait(bar, parity, status, kSiteAttn);
     return __all_sync(0xffffffffu, ok);
+}
+
+// The same for a 64-row tile (a half tile): its 64-column blocks are 8 KiB apart.
+__device__ __forceinline__ uint64_t kdesc64_at(uint64_t base, int kk) {
+    return base + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t mndesc64_base(uint32_t tile) { return smem_desc_sw128(tile, 8192, 1024); }
+
+// Loads one 64-row tile (d / 64 boxes of 64 x 64) of columns col .. col + d - 1 at row r0.
+template <int D>
+__device__ __forceinline__ void load_half(uint32_t dst, const CUtensorMap* map, uint32_t bar, int col, int r0) {
+#pragma unroll
+    for (int b = 0; b < D / 64; ++b) tma_load_2d(dst + b * 8192u, map, bar, col + 64 * b, r0);
 }
 
 // Loads one 128-row tile (d / 64 boxes) of columns col .. col + d - 1 at row r0.
@@ -188,7 +206,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, kTile);
             load_tile<D>(s_q, &map_qkv, q_full, qcol, q0);
-            int issued[NS] = {};
+            uint32_t n_fills = 0;
             for (int j = 0; j < nk; ++j) {
                 const int st = j % NS;
                 if (!mbar_wait(kv_empty(st), ((j / NS) & 1) ^ 1u, p.status, kSiteAttn)) break;
@@ -196,11 +214,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int k0 = (kb0 + j) * kRows;
                 load_tile<D>(s_kv + 2 * st * kTile, &map_qkv, kv_full(st), kcol, k0);
                 load_tile<D>(s_kv + (2 * st + 1) * kTile, &map_qkv, kv_full(st), vcol, k0);
-                ++issued[st];
+                ++n_fills;
             }
             mbar_wait(q_full, 0, p.status, kSiteDrain);
-            for (int s = 0; s < NS; ++s)
-                if (issued[s] > 0) mbar_wait(kv_full(s), (issued[s] - 1) & 1, p.status, kSiteDrain);
+            for (int s = 0; s < NS; ++s) {
+                const uint32_t u = ring_uses(n_fills, NS, s);
+                if (u > 0) mbar_wait(kv_full(s), (u - 1) & 1, p.status, kSiteDrain);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -354,27 +374,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // ------------------------------------------------------------------------ backward: dq
 
 // Work runs in sub-blocks of 64 keys (two per loaded key tile), with two
-// tensor-memory buffers each for S and dP, so the row threads' pass over one
-// sub-block overlaps the tensor cores' work on its neighbours.  dS goes, as
+// tensor-memory buffers each for S and dP, one per group of row warps, so the
+// two groups' passes over neighbouring sub-blocks overlap each other and the
+// tensor cores' work.  dS goes, as
 // packed bf16 pairs, over the buffer columns of S it came from; dQ += dS K
-// takes it from there as its A operand.
+// takes it from there as its A operand.  K and V stream through a ring of four
+// stages, each the 64 key rows of one sub-block, so the loads run three
+// sub-blocks ahead.
 template <int D>
 struct DqSmem {
+    static constexpr int kStages = 4;
     static constexpr uint32_t kTile = D * 256;
+    static constexpr uint32_t kHalf = D * 128;  // 64 rows
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kDO = kTile;
-    static constexpr uint32_t kKV = 2 * kTile;  // stage s: K at kKV + 2 s kTile, V after it
-    static constexpr uint32_t kBars = kKV + 4 * kTile;
+    static constexpr uint32_t kKV = 2 * kTile;  // stage s: K at kKV + 2 s kHalf, V after it
+    static constexpr uint32_t kBars = kKV + 2 * kStages * kHalf;
     static constexpr size_t kBytes = 1024 + kBars + 16 * 8 > kMinSmem ? 1024 + kBars + 16 * 8 : kMinSmem;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnBwdThreads, 1)
     attn_causal_dq_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
-                          const AttnParams p) {
+                          const __grid_constant__ CUtensorMap map_qkv64, const AttnParams p) {
     using L = DqSmem<D>;
-    constexpr uint32_t kTile = L::kTile;
-    constexpr uint32_t kHalfRows = 64 * 128;
+    constexpr int NS = L::kStages;
+    constexpr uint32_t kTile = L::kTile, kHalf = L::kHalf;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -382,11 +407,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t bars = base + L::kBars;
     const uint32_t q_full = bars;
     auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto kv_empty = [&](int s) { return bars + 8u * (3 + s); };
-    auto sp_full = [&](int b) { return bars + 8u * (5 + b); };
-    auto ds_full = [&](int b) { return bars + 8u * (7 + b); };
-    const uint32_t done = bars + 8u * 9, drain = bars + 8u * 10;
-    const uint32_t tmem_slot = bars + 8u * 11;
+    auto kv_empty = [&](int s) { return bars + 8u * (1 + NS + s); };
+    auto sp_full = [&](int b) { return bars + 8u * (1 + 2 * NS + b); };
+    auto ds_full = [&](int b) { return bars + 8u * (3 + 2 * NS + b); };
+    const uint32_t done = bars + 8u * (5 + 2 * NS), drain = bars + 8u * (6 + 2 * NS);
+    const uint32_t tmem_slot = bars + 8u * (7 + 2 * NS);
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -403,17 +428,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
-            mbar_init(sp_full(s), 1);
-            mbar_init(ds_full(s), 128);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sp_full(b), 1);
+            mbar_init(ds_full(b), 128);
         }
         mbar_init(done, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
         tma_prefetch_map(&map_qkv);
         tma_prefetch_map(&map_do);
+        tma_prefetch_map(&map_qkv64);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
@@ -429,19 +457,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_arrive_expect_tx(q_full, 2 * kTile);
             load_tile<D>(s_q, &map_qkv, q_full, h * D, q0);
             load_tile<D>(s_do, &map_do, q_full, h * D, q0);
-            int issued[2] = {0, 0};
-            for (int j = 0; j < nk; ++j) {
-                const int st = j & 1;
-                if (!mbar_wait(kv_empty(st), ((j >> 1) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(kv_full(st), 2 * kTile);
-                const int k0 = (kb0 + j) * kRows;
-                load_tile<D>(s_kv + 2 * st * kTile, &map_qkv, kv_full(st), kcol, k0);
-                load_tile<D>(s_kv + (2 * st + 1) * kTile, &map_qkv, kv_full(st), vcol, k0);
-                ++issued[st];
+            uint32_t n_fills = 0;
+            for (int it = 0; it < n_sub; ++it) {
+                // sub-block it: key rows kb0 * 128 + 64 it .. +63
+                const int st = it % NS;
+                if (!mbar_wait(kv_empty(st), ((it / NS) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(kv_full(st), 2 * kHalf);
+                const int k0 = kb0 * kRows + 64 * it;
+                load_half<D>(s_kv + 2 * st * kHalf, &map_qkv64, kv_full(st), kcol, k0);
+                load_half<D>(s_kv + (2 * st + 1) * kHalf, &map_qkv64, kv_full(st), vcol, k0);
+                ++n_fills;
             }
             mbar_wait(q_full, 0, p.status, kSiteDrain);
-            for (int s = 0; s < 2; ++s)
-                if (issued[s] > 0) mbar_wait(kv_full(s), (issued[s] - 1) & 1, p.status, kSiteDrain);
+            for (int s = 0; s < NS; ++s) {
+                const uint32_t u = ring_uses(n_fills, NS, s);
+                if (u > 0) mbar_wait(kv_full(s), (u - 1) & 1, p.status, kSiteDrain);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -452,36 +483,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (it < n_sub) {
                     // S / dP of sub-block it reuse the buffers of it - 2, whose dS
                     // feeds a product issued earlier, which runs first
-                    const int j = it >> 1, half = it & 1, st = j & 1;
-                    if (half == 0 && !mbar_wait(kv_full(st), (j >> 1) & 1, p.status, kSiteAttn)) {
+                    const int half = it & 1, st = it % NS;
+                    if (!mbar_wait(kv_full(st), (it / NS) & 1, p.status, kSiteAttn)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t k_rows = s_kv + 2 * st * kTile + half * kHalfRows;
+                    const uint32_t k_half = s_kv + 2 * st * kHalf;
                     const uint64_t q_desc = kdesc_base(s_q), do_desc = kdesc_base(s_do);
-                    const uint64_t k_desc = kdesc_base(k_rows), v_desc = kdesc_base(k_rows + kTile);
+                    const uint64_t k_desc = kdesc_base(k_half), v_desc = kdesc_base(k_half + kHalf);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_s + 64 * half, kdesc_at(q_desc, kk), kdesc_at(k_desc, kk), idesc_s, kk > 0);
+                        umma_bf16(t_s + 64 * half, kdesc_at(q_desc, kk), kdesc64_at(k_desc, kk), idesc_s, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_dp + 64 * half, kdesc_at(do_desc, kk), kdesc_at(v_desc, kk), idesc_s, kk > 0);
+                        umma_bf16(t_dp + 64 * half, kdesc_at(do_desc, kk), kdesc64_at(v_desc, kk), idesc_s, kk > 0);
                     umma_commit(sp_full(half));
                 }
                 if (it > 0) {
-                    const int pi = it - 1, j = pi >> 1, half = pi & 1, st = j & 1;
+                    const int pi = it - 1, half = pi & 1, st = pi % NS;
                     if (!mbar_wait(ds_full(half), (pi >> 1) & 1, p.status, kSiteAttn)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t k_desc = mndesc_base(s_kv + 2 * st * kTile + half * kHalfRows);
+                    const uint64_t k_desc = mndesc64_base(s_kv + 2 * st * kHalf);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16_ts(t_dq, t_s + 64 * half + 8 * kk, mndesc_at(k_desc, kk), idesc_q,
                                      (pi > 0 || kk > 0) ? 1u : 0u);
-                    if (half == 1) umma_commit(kv_empty(st));
+                    umma_commit(kv_empty(st));
                 }
             }
             umma_commit(done);
@@ -489,29 +520,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_wait(drain, 0, p.status, kSiteDrain);
         }
     } else {
+        // ---------------- two groups of four warps, one query row per thread in each:
+        // group gi takes the sub-blocks of buffer gi (it = gi, gi + 2, ...)
+        const int gi = (warp - 2) >> 2;
         const int qw = warp & 3;
         const int row = qw * 32 + lane;
         const int q = q0 + row;
         const uint32_t t_row = static_cast<uint32_t>(qw * 32) << 16;
+        const uint32_t t_sb = t_s + t_row + 64 * gi, t_pb = t_dp + t_row + 64 * gi;
         const bool valid = q < s1;
         const float lse = valid ? p.lse[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
         const float dv = valid ? p.dvec[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
         bool ok = true;
-        for (int it = 0; it < n_sub; ++it) {
-            const int half = it & 1;
-            if (!warp_wait(sp_full(half), (it >> 1) & 1, p.status)) {
+        for (int it = gi; it < n_sub; it += 2) {
+            if (!warp_wait(sp_full(gi), (it >> 1) & 1, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int k0 = (kb0 + (it >> 1)) * kRows + 64 * half;
-            const int lim = valid ? min(q - k0, s1 - 1 - k0) : -1;
+            const int k0 = (kb0 + (it >> 1)) * kRows + 64 * gi;
+            const int lim = valid ? min(q - k0, s1 - 1 - k0) : -1;  // last visible key column of this row
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 uint32_t rs[32], rp[32];
-                tmem_load_32(t_s + t_row + 64 * half + 32 * c, rs);
-                tmem_load_32(t_dp + t_row + 64 * half + 32 * c, rp);
+                tmem_load_32(t_sb + 32 * c, rs);
+                tmem_load_32(t_pb + 32 * c, rp);
                 tmem_wait_load();
+                const bool all_vis = __all_sync(0xffffffffu, lim >= 32 * c + 31);
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -519,24 +554,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int i = 2 * e + u;
-                        const int col = 32 * c + i;
-                        const float pr = col <= lim ? ex2(__uint_as_float(rs[i]) * p.scale_log2 - lse) : 0.f;
-                        ds2[u] = pr * (__uint_as_float(rp[i]) - dv);
+                        const float pr = ex2(fmaf(__uint_as_float(rs[i]), p.scale_log2, -lse));
+                        float ds = pr * (__uint_as_float(rp[i]) - dv);
+                        if (!all_vis) ds = 32 * c + i <= lim ? ds : 0.f;
+                        ds2[u] = ds;
                     }
                     w[e] = pack_bf16x2(ds2[0], ds2[1]);
                 }
                 // packed columns 16 c .. 16 c + 15 of the buffer lie in columns already read
-                tmem_store_16(t_s + t_row + 64 * half + 16 * c, w);
+                tmem_store_16(t_sb + 16 * c, w);
             }
             tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(ds_full(half));
+            mbar_arrive(ds_full(gi));
         }
+        // group gi stores dQ columns [D/2 gi, D/2 (gi + 1))
         if (ok && warp_wait(done, 0, p.status)) {
             tc_fence_after();
             uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(q) * p.ld_out + h * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = gi * (D / 64); c < (gi + 1) * (D / 64); ++c) {
                 uint32_t r[32];
                 tmem_load_32(t_dq + t_row + 32 * c, r);
                 tmem_wait_load();
@@ -565,31 +602,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // ------------------------------------------------------------------------ backward: dk, dv
 
 // Work runs in sub-blocks of 64 queries (two per loaded 128-query tile), with
-// two tensor-memory buffers each for S^T and dP^T: while the row threads turn
-// sub-block i into P^T and dS^T, the tensor cores compute S^T and dP^T of
-// sub-block i + 1 and the dV / dK updates of sub-block i - 1.  P^T and dS^T
+// two tensor-memory buffers each for S^T and dP^T, one per group of row warps:
+// while the two groups turn sub-blocks i and i + 1 into P^T and dS^T, the
+// tensor cores run the dV / dK updates of sub-block i - 1 and the S^T and dP^T
+// of the next sub-block as soon as a buffer frees.  P^T and dS^T
 // never touch shared memory: each thread writes its key row of them, as packed
 // bf16 pairs, over the buffer columns it has just read, and the dV and dK
 // products take them as their A operand from tensor memory.  Shared memory
-// holds K, V and two query-side stages.
+// holds K, V and a ring of four query-side stages, each the 64 query rows of
+// one sub-block (Q, dO, lse and dvec): a stage frees as soon as its sub-block's
+// dV / dK products are done, so the loads run three sub-blocks ahead.
 template <int D>
 struct DkvSmem {
+    static constexpr int kStages = 4;
     static constexpr uint32_t kTile = D * 256;
+    static constexpr uint32_t kHalf = D * 128;  // 64 rows
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = kTile;
-    static constexpr uint32_t kQD = 2 * kTile;          // stage s: Q at kQD + 2 s kTile, dO after it
-    static constexpr uint32_t kStat = kQD + 4 * kTile;  // stage s: lse then dvec of its 128 queries (1 KiB)
-    static constexpr uint32_t kBars = kStat + 2048;
+    static constexpr uint32_t kQD = 2 * kTile;                      // stage s: Q at kQD + 2 s kHalf, dO after it
+    static constexpr uint32_t kStat = kQD + 2 * kStages * kHalf;    // stage s: lse then dvec of its 64 queries
+    static constexpr uint32_t kBars = kStat + 512 * kStages;
     static constexpr size_t kBytes = 1024 + kBars + 16 * 8 > kMinSmem ? 1024 + kBars + 16 * 8 : kMinSmem;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_causal_dkdv_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
-                            const AttnParams p) {
+__global__ void __launch_bounds__(kAttnBwdThreads, 1)
+    attn_causal_dkdv_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_qkv64,
+                            const __grid_constant__ CUtensorMap map_do64, const AttnParams p) {
     using L = DkvSmem<D>;
-    constexpr uint32_t kTile = L::kTile;
-    constexpr uint32_t kHalfRows = 64 * 128;  // bytes of 64 rows inside a 64-column block of a tile
+    constexpr int NS = L::kStages;
+    constexpr uint32_t kTile = L::kTile, kHalf = L::kHalf;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -597,11 +639,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t bars = base + L::kBars;
     const uint32_t kv_full = bars;
     auto qd_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto qd_empty = [&](int s) { return bars + 8u * (3 + s); };
-    auto sp_full = [&](int b) { return bars + 8u * (5 + b); };
-    auto pd_full = [&](int b) { return bars + 8u * (7 + b); };
-    const uint32_t done = bars + 8u * 9, drain = bars + 8u * 10;
-    const uint32_t tmem_slot = bars + 8u * 11;
+    auto qd_empty = [&](int s) { return bars + 8u * (1 + NS + s); };
+    auto sp_full = [&](int b) { return bars + 8u * (1 + 2 * NS + b); };
+    auto pd_full = [&](int b) { return bars + 8u * (3 + 2 * NS + b); };
+    const uint32_t done = bars + 8u * (5 + 2 * NS), drain = bars + 8u * (6 + 2 * NS);
+    const uint32_t tmem_slot = bars + 8u * (7 + 2 * NS);
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -618,17 +660,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(qd_full(s), 1);
             mbar_init(qd_empty(s), 1);
-            mbar_init(sp_full(s), 1);
-            mbar_init(pd_full(s), 128);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sp_full(b), 1);
+            mbar_init(pd_full(b), 128);
         }
         mbar_init(done, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
         tma_prefetch_map(&map_qkv);
-        tma_prefetch_map(&map_do);
+        tma_prefetch_map(&map_qkv64);
+        tma_prefetch_map(&map_do64);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
@@ -645,24 +690,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_arrive_expect_tx(kv_full, 2 * kTile);
             load_tile<D>(s_k, &map_qkv, kv_full, kcol, k0);
             load_tile<D>(s_v, &map_qkv, kv_full, vcol, k0);
-            int issued[2] = {0, 0};
-            for (int it = 0; it < n_tiles; ++it) {
-                const int st = it & 1;
-                const int qb = kb + it / group;
-                const int h = g * group + it % group;
-                if (!mbar_wait(qd_empty(st), ((it >> 1) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(qd_full(st), 2 * kTile + 1024);
-                const uint32_t q_tile = s_qd + 2 * st * kTile;
-                load_tile<D>(q_tile, &map_qkv, qd_full(st), h * D, qb * kRows);
-                load_tile<D>(q_tile + kTile, &map_do, qd_full(st), h * D, qb * kRows);
-                const uint32_t stat = s_stat + 1024u * st;
-                bulk_load_1d(stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + qb * kRows, 512, qd_full(st));
-                bulk_load_1d(stat + 512, p.dvec + static_cast<int64_t>(h) * p.ld_stat + qb * kRows, 512, qd_full(st));
-                ++issued[st];
+            uint32_t n_fills = 0;
+            for (int it = 0; it < n_sub; ++it) {
+                // sub-block it: query rows qb * 128 + 64 (it & 1) .. +63 of head h
+                const int st = it % NS, tile = it >> 1;
+                const int qb = kb + tile / group;
+                const int h = g * group + tile % group;
+                const int r0 = qb * kRows + 64 * (it & 1);
+                if (!mbar_wait(qd_empty(st), ((it / NS) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(qd_full(st), 2 * kHalf + 512);
+                const uint32_t q_half = s_qd + 2 * st * kHalf;
+                load_half<D>(q_half, &map_qkv64, qd_full(st), h * D, r0);
+                load_half<D>(q_half + kHalf, &map_do64, qd_full(st), h * D, r0);
+                const uint32_t stat = s_stat + 512u * st;
+                bulk_load_1d(stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + r0, 256, qd_full(st));
+                bulk_load_1d(stat + 256, p.dvec + static_cast<int64_t>(h) * p.ld_stat + r0, 256, qd_full(st));
+                ++n_fills;
             }
             mbar_wait(kv_full, 0, p.status, kSiteDrain);
-            for (int s = 0; s < 2; ++s)
-                if (issued[s] > 0) mbar_wait(qd_full(s), (issued[s] - 1) & 1, p.status, kSiteDrain);
+            for (int s = 0; s < NS; ++s) {
+                const uint32_t u = ring_uses(n_fills, NS, s);
+                if (u > 0) mbar_wait(qd_full(s), (u - 1) & 1, p.status, kSiteDrain);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -673,32 +722,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (it < n_sub) {
                     // S^T / dP^T of sub-block it reuse the buffers of it - 2, whose
                     // P^T / dS^T feed products issued earlier, which run first
-                    const int tile = it >> 1, half = it & 1, st = tile & 1;
-                    if (half == 0 && !mbar_wait(qd_full(st), (tile >> 1) & 1, p.status, kSiteAttn)) {
+                    const int half = it & 1, st = it % NS;
+                    if (!mbar_wait(qd_full(st), (it / NS) & 1, p.status, kSiteAttn)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t q_rows = s_qd + 2 * st * kTile + half * kHalfRows;
+                    const uint32_t q_half = s_qd + 2 * st * kHalf;
                     const uint64_t k_desc = kdesc_base(s_k), v_desc = kdesc_base(s_v);
-                    const uint64_t q_desc = kdesc_base(q_rows), do_desc = kdesc_base(q_rows + kTile);
+                    const uint64_t q_desc = kdesc_base(q_half), do_desc = kdesc_base(q_half + kHalf);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_s + 64 * half, kdesc_at(k_desc, kk), kdesc_at(q_desc, kk), idesc_s, kk > 0);
+                        umma_bf16(t_s + 64 * half, kdesc_at(k_desc, kk), kdesc64_at(q_desc, kk), idesc_s, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_dp + 64 * half, kdesc_at(v_desc, kk), kdesc_at(do_desc, kk), idesc_s, kk > 0);
+                        umma_bf16(t_dp + 64 * half, kdesc_at(v_desc, kk), kdesc64_at(do_desc, kk), idesc_s, kk > 0);
                     umma_commit(sp_full(half));
                 }
                 if (it > 0) {
-                    const int pi = it - 1, tile = pi >> 1, half = pi & 1, st = tile & 1;
+                    const int pi = it - 1, half = pi & 1, st = pi % NS;
                     if (!mbar_wait(pd_full(half), (pi >> 1) & 1, p.status, kSiteAttn)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t q_rows = s_qd + 2 * st * kTile + half * kHalfRows;
-                    const uint64_t q_desc = mndesc_base(q_rows), do_desc = mndesc_base(q_rows + kTile);
+                    const uint32_t q_half = s_qd + 2 * st * kHalf;
+                    const uint64_t q_desc = mndesc64_base(q_half), do_desc = mndesc64_base(q_half + kHalf);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16_ts(t_dv, t_s + 64 * half + 8 * kk, mndesc_at(do_desc, kk), idesc_g,
@@ -707,7 +756,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16_ts(t_dk, t_dp + 64 * half + 8 * kk, mndesc_at(q_desc, kk), idesc_g,
                                      (pi > 0 || kk > 0) ? 1u : 0u);
-                    if (half == 1) umma_commit(qd_empty(st));
+                    umma_commit(qd_empty(st));
                 }
             }
             umma_commit(done);
@@ -715,81 +764,94 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_wait(drain, 0, p.status, kSiteDrain);
         }
     } else {
-        // ---------------- one key row per thread
+        // ---------------- two groups of four warps, one key row per thread in each:
+        // group gi takes the sub-blocks of buffer gi (it = gi, gi + 2, ...), so the
+        // elementwise passes of two neighbouring sub-blocks run at once
+        const int gi = (warp - 2) >> 2;
         const int qw = warp & 3;
         const int row = qw * 32 + lane;
         const int k = k0 + row;
         const uint32_t t_row = static_cast<uint32_t>(qw * 32) << 16;
+        const uint32_t t_sb = t_s + t_row + 64 * gi, t_pb = t_dp + t_row + 64 * gi;
         bool ok = true;
-        for (int it = 0; it < n_sub; ++it) {
-            const int tile = it >> 1, half = it & 1, st = tile & 1;
-            const int q0 = (kb + tile / group) * kRows + 64 * half;
-            if ((half == 0 && !warp_wait(qd_full(st), (tile >> 1) & 1, p.status)) ||
-                !warp_wait(sp_full(half), (it >> 1) & 1, p.status)) {
+        for (int it = gi; it < n_sub; it += 2) {
+            const int tile = it >> 1, st = it % NS;
+            const int q0 = (kb + tile / group) * kRows + 64 * gi;
+            if (!warp_wait(qd_full(st), (it / NS) & 1, p.status) || !warp_wait(sp_full(gi), (it >> 1) & 1, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float* stat_lse = reinterpret_cast<const float*>(smem_raw + (s_stat + 1024u * st - raw)) + 64 * half;
-            const float* stat_dv = stat_lse + 128;
-            // query column c is visible to this key when k <= q0 + c < s1
+            // lse of this sub-block's 64 queries, then (256 bytes on) their dvec
+            const uint32_t stat = s_stat + 512u * st;
+            // query column c is visible to this key when first <= c <= last
             const int first = k - q0;
             const int last = s1 - 1 - q0;
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 uint32_t rs[32], rp[32];
-                tmem_load_32(t_s + t_row + 64 * half + 32 * c, rs);
-                tmem_load_32(t_dp + t_row + 64 * half + 32 * c, rp);
+                tmem_load_32(t_sb + 32 * c, rs);
+                tmem_load_32(t_pb + 32 * c, rp);
                 tmem_wait_load();
+                // below the diagonal and inside the sequence every column is visible:
+                // no per-element mask (statistics past the sequence end are never
+                // written; masked elements are selected away, never used)
+                const bool all_vis = __all_sync(0xffffffffu, first <= 32 * c && last >= 32 * c + 31);
                 uint32_t wp[16], wd[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pv[2], dsv[2];
+                for (int j = 0; j < 8; ++j) {
+                    const float4 l4 = ld_shared_f4(stat + 4u * (32 * c + 4 * j));
+                    const float4 d4 = ld_shared_f4(stat + 256u + 4u * (32 * c + 4 * j));
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pv[4], dsv[4];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int i = 2 * e + u;
-                        const int col = 32 * c + i;
-                        const bool vis = col >= first && col <= last;
-                        // statistics past the sequence end are not written: never read them into a value
-                        const float pr = vis ? ex2(__uint_as_float(rs[i]) * p.scale_log2 - stat_lse[col]) : 0.f;
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = 4 * j + u;
+                        float pr = ex2(fmaf(__uint_as_float(rs[i]), p.scale_log2, -lv[u]));
+                        float ds = pr * (__uint_as_float(rp[i]) - dvv[u]);
+                        if (!all_vis) {
+                            const int col = 32 * c + i;
+                            const bool vis = col >= first && col <= last;
+                            pr = vis ? pr : 0.f;
+                            ds = vis ? ds : 0.f;
+                        }
                         pv[u] = pr;
-                        dsv[u] = vis ? pr * (__uint_as_float(rp[i]) - stat_dv[col]) : 0.f;
+                        dsv[u] = ds;
                     }
-                    wp[e] = pack_bf16x2(pv[0], pv[1]);
-                    wd[e] = pack_bf16x2(dsv[0], dsv[1]);
+                    wp[2 * j] = pack_bf16x2(pv[0], pv[1]);
+                    wp[2 * j + 1] = pack_bf16x2(pv[2], pv[3]);
+                    wd[2 * j] = pack_bf16x2(dsv[0], dsv[1]);
+                    wd[2 * j + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
                 // packed columns 16 c .. 16 c + 15 of the buffer lie in columns already read
-                tmem_store_16(t_s + t_row + 64 * half + 16 * c, wp);
-                tmem_store_16(t_dp + t_row + 64 * half + 16 * c, wd);
+                tmem_store_16(t_sb + 16 * c, wp);
+                tmem_store_16(t_pb + 16 * c, wd);
             }
             tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(pd_full(half));
+            mbar_arrive(pd_full(gi));
         }
+        // group 0 stores dK, group 1 dV
         if (ok && warp_wait(done, 0, p.status)) {
             tc_fence_after();
             const bool valid = k < s1;
-            uint16_t* dk_dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(k) * p.ld_out + kcol;
-            uint16_t* dv_dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(k) * p.ld_out + vcol;
+            const uint32_t t_acc = gi == 0 ? t_dk : t_dv;
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(k) * p.ld_out + (gi == 0 ? kcol : vcol);
+            const float sc = gi == 0 ? p.scale : 1.f;
 #pragma unroll 1
-            for (int pass = 0; pass < 2; ++pass) {
-                const uint32_t t_acc = pass == 0 ? t_dk : t_dv;
-                uint16_t* dst = pass == 0 ? dk_dst : dv_dst;
-                const float sc = pass == 0 ? p.scale : 1.f;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_load_32(t_acc + t_row + 32 * c, r);
-                    tmem_wait_load();
-                    if (valid) {
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_load_32(t_acc + t_row + 32 * c, r);
+                tmem_wait_load();
+                if (valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]) * sc, __uint_as_float(r[8 * q + 1]) * sc),
-                                               pack_bf16x2(__uint_as_float(r[8 * q + 2]) * sc, __uint_as_float(r[8 * q + 3]) * sc),
-                                               pack_bf16x2(__uint_as_float(r[8 * q + 4]) * sc, __uint_as_float(r[8 * q + 5]) * sc),
-                                               pack_bf16x2(__uint_as_float(r[8 * q + 6]) * sc, __uint_as_float(r[8 * q + 7]) * sc));
-                    }
+                    for (int q = 0; q < 4; ++q)
+                        d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]) * sc, __uint_as_float(r[8 * q + 1]) * sc),
+                                           pack_bf16x2(__uint_as_float(r[8 * q + 2]) * sc, __uint_as_float(r[8 * q + 3]) * sc),
+                                           pack_bf16x2(__uint_as_float(r[8 * q + 4]) * sc, __uint_as_float(r[8 * q + 5]) * sc),
+                                           pack_bf16x2(__uint_as_float(r[8 * q + 6]) * sc, __uint_as_float(r[8 * q + 7]) * sc));
                 }
             }
         }
@@ -858,13 +920,13 @@ PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
     return fn;
 }
 
-// [rows, cols] bf16, row stride ld elements; boxes of 64 columns x 128 rows, 128B swizzle.
-bool attn_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld) {
+// [rows, cols] bf16, row stride ld elements; boxes of 64 columns x box_rows rows, 128B swizzle.
+bool attn_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows = 128) {
     auto fn = attn_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -920,8 +982,9 @@ cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const
     if (err != cudaSuccess) return err;
     const int qkv_w = (s.n_heads + 2 * s.n_kv_heads) * D;
     const int hw = s.n_heads * D;
-    CUtensorMap mq, md;
-    if (!attn_map(&mq, qkv, s.tokens, qkv_w, qkv_w) || !attn_map(&md, da, s.tokens, hw, hw))
+    CUtensorMap mq, md, mq64, md64;
+    if (!attn_map(&mq, qkv, s.tokens, qkv_w, qkv_w) || !attn_map(&md, da, s.tokens, hw, hw) ||
+        !attn_map(&mq64, qkv, s.tokens, qkv_w, qkv_w, 64) || !attn_map(&md64, da, s.tokens, hw, hw, 64))
         return cudaErrorInvalidValue;
     AttnParams p = make_params(s);
     if (!p.status) return cudaErrorInvalidDevice;
@@ -934,10 +997,11 @@ cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const
         static_cast<const uint16_t*>(da), static_cast<const uint16_t*>(a), dvec, s.tokens, s.n_heads, D, s.ld_stat);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_causal_dkdv_kernel<D><<<p.n_blocks * s.n_kv_heads, kAttnThreads, DkvSmem<D>::kBytes, stream>>>(mq, md, p);
+    attn_causal_dkdv_kernel<D><<<p.n_blocks * s.n_kv_heads, kAttnBwdThreads, DkvSmem<D>::kBytes, stream>>>(mq, mq64, md64,
+                                                                                                         p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_causal_dq_kernel<D><<<p.n_blocks * s.n_heads, kAttnThreads, DqSmem<D>::kBytes, stream>>>(mq, md, p);
+    attn_causal_dq_kernel<D><<<p.n_blocks * s.n_heads, kAttnBwdThreads, DqSmem<D>::kBytes, stream>>>(mq, md, mq64, p);
     return cudaGetLastError();
 }
 

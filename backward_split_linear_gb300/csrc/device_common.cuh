@@ -74,9 +74,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits until the phase with the given parity has completed.  Gives up when
 // `limit_ns` passes or when another thread of the grid has already set the
 // status word; returns false in both cases (and records `site` in the first).
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status, int site,
-                                       uint64_t limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Everything is inline: on GB300 a call in the path of a thread that issues
+// MMAs costs a few hundred cycles (its frame lives in local memory) even when
+// the phase has long completed, and a call site alone slowed the issue of the
+// MMAs around it; in the attention kernels that starved the tensor pipe.
+__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int* status, int site,
+                                                   uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
@@ -88,6 +91,19 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status, int site,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, status, site, limit_ns);
+}
+
+// Uses of stage s of a ring of `stages` filled round-robin from stage 0 once
+// n fills have been issued in all (kept as one counter: a per-stage array
+// indexed at run time would live in local memory).
+__device__ __forceinline__ uint32_t ring_uses(uint32_t n, uint32_t stages, uint32_t s) {
+    return n / stages + (s < n % stages ? 1u : 0u);
 }
 
 // Teardown wait: until the phase completes or `limit_ns` passes, whatever the
@@ -102,31 +118,37 @@ static __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity, ui
 
 // Same as mbar_wait, with cluster-scope acquire: for barriers that CTAs of the
 // same cluster arrive on (or whose transactions they complete).
-static __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* status, int site,
-                                                      uint64_t limit_ns = kWaitLimitNs) {
-    auto try_once = [&]() {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        return ok != 0;
-    };
-    if (try_once()) return true;
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity, int* status, int site,
+                                                           uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (try_once()) return true;
+            if (mbar_try_wait_cluster(bar, parity)) return true;
         if (*reinterpret_cast<volatile int*>(status) != 0) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             atomicCAS(status, 0, site);
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* status, int site,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return mbar_wait_cluster_slow(bar, parity, status, site, limit_ns);
 }
 
 // ---------------------------------------------------------------- global flags
@@ -258,6 +280,13 @@ __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.b
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
                  : "memory");
     return v;
 }

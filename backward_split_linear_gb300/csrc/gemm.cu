@@ -338,8 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer
-            uint32_t issued[STAGES];
-            for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+            uint32_t n_fills = 0;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -372,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         tma_load_2d(b_dst, &map_b, fb, k0, n0);
                     }
-                    ++issued[stage];
+                    ++n_fills;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -380,10 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Every load issued must land before the CTA's shared memory goes away.
-            for (int s = 0; s < STAGES; ++s)
-                if (issued[s] > 0)
-                    mbar_wait(full_bar(s), (issued[s] - 1u) & 1u, p.status, kSiteDrain,
-                              kWaitLimitNs);
+            for (int s = 0; s < STAGES; ++s) {
+                const uint32_t u = ring_uses(n_fills, STAGES, s);
+                if (u > 0) mbar_wait(full_bar(s), (u - 1u) & 1u, p.status, kSiteDrain, kWaitLimitNs);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -612,8 +611,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (usable && warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer (both CTAs)
-            uint32_t issued[kStages];
-            for (int s = 0; s < kStages; ++s) issued[s] = 0;
+            uint32_t n_fills = 0;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -650,7 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     } else {
                         tma_load_2d_pair(b_dst, &G.map[2 * pi + 1], fb, k0, n0);
                     }
-                    ++issued[stage];
+                    ++n_fills;
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -659,13 +657,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             // Loads must land before shared memory goes away: rank 0 sees its
             // full barriers complete; rank 1 sees the MMA release each stage.
-            for (int s = 0; s < kStages; ++s)
-                if (issued[s] > 0) {
+            for (int s = 0; s < kStages; ++s) {
+                const uint32_t u = ring_uses(n_fills, kStages, s);
+                if (u > 0) {
                     if (leader)
-                        mbar_wait_cluster(full_bar(s), (issued[s] - 1u) & 1u, status, kSiteDrain, kWaitLimitNs);
+                        mbar_wait_cluster(full_bar(s), (u - 1u) & 1u, status, kSiteDrain, kWaitLimitNs);
                     else
-                        mbar_wait_cluster(empty_bar(s), (issued[s] - 1u) & 1u, status, kSiteDrain, kWaitLimitNs);
+                        mbar_wait_cluster(empty_bar(s), (u - 1u) & 1u, status, kSiteDrain, kWaitLimitNs);
                 }
+            }
         }
     } else if (usable && warp == 1) {
         if (lane == 0 && leader) {
