@@ -101,6 +101,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// v where `visible`, else +0.0: a bit mask, not a branch.  A select written as a
+// short-circuit condition per element compiled to a branch per element, and
+// branch resolution then dominated the elementwise passes.
+__device__ __forceinline__ float keep_if(float v, bool visible) {
+    return __uint_as_float(__float_as_uint(v) & (0u - static_cast<uint32_t>(visible)));
+}
+
 __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -112,19 +119,6 @@ __device__ __forceinline__ float lg2(float x) {
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* status) {
     const bool ok = mbar_wait(bar, parity, status, kSiteAttn);
     return __all_sync(0xffffffffu, ok);
-}
-
-// The same for a 64-row tile (a half tile): its 64-column blocks are 8 KiB apart.
-__device__ __forceinline__ uint64_t kdesc64_at(uint64_t base, int kk) {
-    return base + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4);
-}
-__device__ __forceinline__ uint64_t mndesc64_base(uint32_t tile) { return smem_desc_sw128(tile, 8192, 1024); }
-
-// Loads one 64-row tile (d / 64 boxes of 64 x 64) of columns col .. col + d - 1 at row r0.
-template <int D>
-__device__ __forceinline__ void load_half(uint32_t dst, const CUtensorMap* map, uint32_t bar, int col, int r0) {
-#pragma unroll
-    for (int b = 0; b < D / 64; ++b) tma_load_2d(dst + b * 8192u, map, bar, col + 64 * b, r0);
 }
 
 // Loads one 128-row tile (d / 64 boxes) of columns col .. col + d - 1 at row r0.
@@ -290,10 +284,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int k0 = (kb0 + j) * kRows;
             const int lim = min(q - k0, s1 - 1 - k0);  // last visible key column of this row
             float mx = -INFINITY;
+            if (__all_sync(0xffffffffu, lim >= 127)) {  // below the diagonal: no mask
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                s[c] = c <= lim ? s[c] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[c]);
+                for (int c = 0; c < 128; ++c) {
+                    s[c] *= p.scale_log2;
+                    mx = fmaxf(mx, s[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    // -inf where masked, by bit operations (no branch per element)
+                    const uint32_t m = 0u - static_cast<uint32_t>(c <= lim);
+                    s[c] = __uint_as_float((__float_as_uint(s[c] * p.scale_log2) & m) | (0xff800000u & ~m));
+                    mx = fmaxf(mx, s[c]);
+                }
             }
             if (j > 0 && !warp_wait(p_free, (j - 1) & 1, p.status)) {
                 ok = false;
@@ -371,51 +375,65 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------------ backward: common
+
+// Tensor-memory column of the packed bf16 operand of K step kk (16 rows of the
+// contraction) when the two groups of row warps each pack their 64 columns of
+// a 128-column buffer into its first 32: group kk / 4 at 64 (kk / 4), then 8
+// columns per K step.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3)); }
+
 // ------------------------------------------------------------------------ backward: dq
 
-// Work runs in sub-blocks of 64 keys (two per loaded key tile), with two
-// tensor-memory buffers each for S and dP, one per group of row warps, so the
-// two groups' passes over neighbouring sub-blocks overlap each other and the
-// tensor cores' work.  dS goes, as
-// packed bf16 pairs, over the buffer columns of S it came from; dQ += dS K
-// takes it from there as its A operand.  K and V stream through a ring of four
-// stages, each the 64 key rows of one sub-block, so the loads run three
-// sub-blocks ahead.
+// One CTA per (query head, query block) walks the key blocks up to the
+// diagonal, 128 keys a step.  Per step the tensor cores run S = Q K^T,
+// dP = dO V^T (both 128 x 128, K-major operands) and dQ += dS K (A = dS from
+// tensor memory, B = K as an MN-major operand).  S has two tensor-memory
+// buffers, dP one: the MMA order is S[j+1], dP[j+1], dQ[j], so the row warps'
+// pass over step j (P = exp2(S c - lse) into registers as soon as S lands,
+// then dS = P (dP - D), packed over the S columns just read) overlaps the
+// products of its neighbours.  Two groups of four row warps take 64 key
+// columns each.  K streams through three stages, V through two.
 template <int D>
 struct DqSmem {
-    static constexpr int kStages = 4;
+    static constexpr int kKStages = 3, kVStages = 2;
     static constexpr uint32_t kTile = D * 256;
-    static constexpr uint32_t kHalf = D * 128;  // 64 rows
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kDO = kTile;
-    static constexpr uint32_t kKV = 2 * kTile;  // stage s: K at kKV + 2 s kHalf, V after it
-    static constexpr uint32_t kBars = kKV + 2 * kStages * kHalf;
-    static constexpr size_t kBytes = 1024 + kBars + 16 * 8 > kMinSmem ? 1024 + kBars + 16 * 8 : kMinSmem;
+    static constexpr uint32_t kQ = 0, kDO = kTile, kK = 2 * kTile;
+    static constexpr uint32_t kV = kK + kKStages * kTile;
+    static constexpr uint32_t kBars = kV + kVStages * kTile;
+    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 4;
+    static constexpr size_t kBytes = kBars + 8 * kNumBars + 16;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     attn_causal_dq_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
-                          const __grid_constant__ CUtensorMap map_qkv64, const AttnParams p) {
+                          const AttnParams p) {
     using L = DqSmem<D>;
-    constexpr int NS = L::kStages;
-    constexpr uint32_t kTile = L::kTile, kHalf = L::kHalf;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_addr(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t s_q = base + L::kQ, s_do = base + L::kDO, s_kv = base + L::kKV;
+    constexpr int NK = L::kKStages, NV = L::kVStages;
+    constexpr uint32_t kTile = L::kTile;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_addr(smem_raw);
+    if (base & 1023u) {  // the tiles' 128-byte swizzle needs a 1 KiB-aligned start
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, kSiteAttn);
+        return;
+    }
+    const uint32_t s_q = base + L::kQ, s_do = base + L::kDO, s_k = base + L::kK, s_v = base + L::kV;
     const uint32_t bars = base + L::kBars;
     const uint32_t q_full = bars;
-    auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto kv_empty = [&](int s) { return bars + 8u * (1 + NS + s); };
-    auto sp_full = [&](int b) { return bars + 8u * (1 + 2 * NS + b); };
-    auto ds_full = [&](int b) { return bars + 8u * (3 + 2 * NS + b); };
-    const uint32_t done = bars + 8u * (5 + 2 * NS), drain = bars + 8u * (6 + 2 * NS);
-    const uint32_t tmem_slot = bars + 8u * (7 + 2 * NS);
-    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
+    auto k_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto k_empty = [&](int s) { return bars + 8u * (1 + NK + s); };
+    auto v_full = [&](int s) { return bars + 8u * (1 + 2 * NK + s); };
+    auto v_empty = [&](int s) { return bars + 8u * (1 + 2 * NK + NV + s); };
+    constexpr int kB = 1 + 2 * NK + 2 * NV;
+    auto s_full = [&](int b) { return bars + 8u * (kB + b); };
+    const uint32_t dp_full = bars + 8u * (kB + 2), ds_full = bars + 8u * (kB + 3), done = bars + 8u * (kB + 4),
+                   drain = bars + 8u * (kB + 5);
+    const uint32_t tmem_slot = bars + 8u * L::kNumBars;
+    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - base));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qb = p.n_blocks - 1 - static_cast<int>(blockIdx.x) / p.n_heads;
+    const int qb = p.n_blocks - 1 - static_cast<int>(blockIdx.x) / p.n_heads;  // longest rows first
     const int h = static_cast<int>(blockIdx.x) % p.n_heads;
     const int g = h / (p.n_heads / p.n_kv_heads);
     const int q0 = qb * kRows;
@@ -423,97 +441,105 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     seq_bounds(p, q0, s0, s1);
     const int kb0 = s0 / kRows;
     const int nk = qb - kb0 + 1;
-    const int n_sub = 2 * nk;
     const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(kv_full(s), 1);
-            mbar_init(kv_empty(s), 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(sp_full(b), 1);
-            mbar_init(ds_full(b), 128);
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
         }
+        mbar_init(s_full(0), 1);
+        mbar_init(s_full(1), 1);
+        mbar_init(dp_full, 1);
+        mbar_init(ds_full, 256);
         mbar_init(done, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
         tma_prefetch_map(&map_qkv);
         tma_prefetch_map(&map_do);
-        tma_prefetch_map(&map_qkv64);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot_ptr;
-    // columns: S buffers 0-63 and 64-127 (dS packed into the first 32 of a
-    // buffer once read), dP buffers 128-191 and 192-255, dQ 256..
-    const uint32_t t_s = tmem_base, t_dp = tmem_base + 128, t_dq = tmem_base + 256;
+    // columns: S buffers 0-127 and 128-255 (dS packed into columns 0-31 and
+    // 64-95 of a buffer once read), dP 256-383, dQ 384..
+    const uint32_t t_dp = tmem_base + 256, t_dq = tmem_base + 384;
+    auto t_s = [&](int j) { return tmem_base + 128u * static_cast<uint32_t>(j & 1); };
 
     if (warp == 0) {
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, 2 * kTile);
             load_tile<D>(s_q, &map_qkv, q_full, h * D, q0);
             load_tile<D>(s_do, &map_do, q_full, h * D, q0);
-            uint32_t n_fills = 0;
-            for (int it = 0; it < n_sub; ++it) {
-                // sub-block it: key rows kb0 * 128 + 64 it .. +63
-                const int st = it % NS;
-                if (!mbar_wait(kv_empty(st), ((it / NS) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(kv_full(st), 2 * kHalf);
-                const int k0 = kb0 * kRows + 64 * it;
-                load_half<D>(s_kv + 2 * st * kHalf, &map_qkv64, kv_full(st), kcol, k0);
-                load_half<D>(s_kv + (2 * st + 1) * kHalf, &map_qkv64, kv_full(st), vcol, k0);
-                ++n_fills;
+            uint32_t nkf = 0, nvf = 0;
+            for (int j = 0; j < nk; ++j) {
+                const int k0 = (kb0 + j) * kRows;
+                if (!mbar_wait(k_empty(j % NK), ((j / NK) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(k_full(j % NK), kTile);
+                load_tile<D>(s_k + (j % NK) * kTile, &map_qkv, k_full(j % NK), kcol, k0);
+                ++nkf;
+                if (!mbar_wait(v_empty(j % NV), ((j / NV) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(v_full(j % NV), kTile);
+                load_tile<D>(s_v + (j % NV) * kTile, &map_qkv, v_full(j % NV), vcol, k0);
+                ++nvf;
             }
             mbar_wait(q_full, 0, p.status, kSiteDrain);
-            for (int s = 0; s < NS; ++s) {
-                const uint32_t u = ring_uses(n_fills, NS, s);
-                if (u > 0) mbar_wait(kv_full(s), (u - 1) & 1, p.status, kSiteDrain);
+            for (int s = 0; s < NK; ++s) {
+                const uint32_t u = ring_uses(nkf, NK, s);
+                if (u > 0) mbar_wait(k_full(s), (u - 1) & 1, p.status, kSiteDrain);
+            }
+            for (int s = 0; s < NV; ++s) {
+                const uint32_t u = ring_uses(nvf, NV, s);
+                if (u > 0) mbar_wait(v_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 64, false, false);
+            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_q = mma_idesc_bf16(128, D, false, true);
-            bool ok = mbar_wait(q_full, 0, p.status, kSiteAttn);
-            for (int it = 0; ok && it <= n_sub; ++it) {
-                if (it < n_sub) {
-                    // S / dP of sub-block it reuse the buffers of it - 2, whose dS
-                    // feeds a product issued earlier, which runs first
-                    const int half = it & 1, st = it % NS;
-                    if (!mbar_wait(kv_full(st), (it / NS) & 1, p.status, kSiteAttn)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t k_half = s_kv + 2 * st * kHalf;
-                    const uint64_t q_desc = kdesc_base(s_q), do_desc = kdesc_base(s_do);
-                    const uint64_t k_desc = kdesc_base(k_half), v_desc = kdesc_base(k_half + kHalf);
+            const uint64_t q_desc = kdesc_base(s_q), do_desc = kdesc_base(s_do);
+            auto issue_s = [&](int j) {
+                const int st = j % NK;
+                if (!mbar_wait(k_full(st), (j / NK) & 1, p.status, kSiteAttn)) return false;
+                tc_fence_after();
+                const uint64_t k_desc = kdesc_base(s_k + st * kTile);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_s + 64 * half, kdesc_at(q_desc, kk), kdesc64_at(k_desc, kk), idesc_s, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(t_s(j), kdesc_at(q_desc, kk), kdesc_at(k_desc, kk), idesc_s, kk > 0);
+                umma_commit(s_full(j & 1));
+                return true;
+            };
+            auto issue_dp = [&](int j) {
+                const int st = j % NV;
+                if (!mbar_wait(v_full(st), (j / NV) & 1, p.status, kSiteAttn)) return false;
+                tc_fence_after();
+                const uint64_t v_desc = kdesc_base(s_v + st * kTile);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_dp + 64 * half, kdesc_at(do_desc, kk), kdesc64_at(v_desc, kk), idesc_s, kk > 0);
-                    umma_commit(sp_full(half));
-                }
-                if (it > 0) {
-                    const int pi = it - 1, half = pi & 1, st = pi % NS;
-                    if (!mbar_wait(ds_full(half), (pi >> 1) & 1, p.status, kSiteAttn)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t k_desc = mndesc64_base(s_kv + 2 * st * kHalf);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(t_dp, kdesc_at(do_desc, kk), kdesc_at(v_desc, kk), idesc_s, kk > 0);
+                umma_commit(dp_full);
+                umma_commit(v_empty(st));
+                return true;
+            };
+            bool ok = mbar_wait(q_full, 0, p.status, kSiteAttn) && issue_s(0) && issue_dp(0);
+            for (int j = 0; ok && j < nk; ++j) {
+                // S[j+1] into the other buffer; dP[j+1] once the row warps are done with dP[j]
+                if (j + 1 < nk && !issue_s(j + 1)) break;
+                if (!mbar_wait(ds_full, j & 1, p.status, kSiteAttn)) break;
+                tc_fence_after();
+                if (j + 1 < nk && !issue_dp(j + 1)) break;
+                const uint64_t k_mn = mndesc_base(s_k + (j % NK) * kTile);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ts(t_dq, t_s + 64 * half + 8 * kk, mndesc_at(k_desc, kk), idesc_q,
-                                     (pi > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(kv_empty(st));
-                }
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_bf16_ts(t_dq, t_s(j) + packed_col(kk), mndesc_at(k_mn, kk), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(k_empty(j % NK));
             }
             umma_commit(done);
             umma_commit(drain);
@@ -521,61 +547,70 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
         }
     } else {
         // ---------------- two groups of four warps, one query row per thread in each:
-        // group gi takes the sub-blocks of buffer gi (it = gi, gi + 2, ...)
+        // group gi takes key columns 64 gi .. 64 gi + 63 of every step
         const int gi = (warp - 2) >> 2;
         const int qw = warp & 3;
         const int row = qw * 32 + lane;
         const int q = q0 + row;
-        const uint32_t t_row = static_cast<uint32_t>(qw * 32) << 16;
-        const uint32_t t_sb = t_s + t_row + 64 * gi, t_pb = t_dp + t_row + 64 * gi;
+        const uint32_t t_row = (static_cast<uint32_t>(qw * 32) << 16) + 64u * gi;
         const bool valid = q < s1;
         const float lse = valid ? p.lse[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
         const float dv = valid ? p.dvec[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
         bool ok = true;
-        for (int it = gi; it < n_sub; it += 2) {
-            if (!warp_wait(sp_full(gi), (it >> 1) & 1, p.status)) {
+        for (int j = 0; j < nk; ++j) {
+            const int c0 = (kb0 + j) * kRows + 64 * gi;
+            const int lim = valid ? min(q - c0, s1 - 1 - c0) : -1;  // last visible key column of this row
+            if (!warp_wait(s_full(j & 1), (j >> 1) & 1, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int k0 = (kb0 + (it >> 1)) * kRows + 64 * gi;
-            const int lim = valid ? min(q - k0, s1 - 1 - k0) : -1;  // last visible key column of this row
-#pragma unroll 1
+            float pr[64];
+#pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t rs[32], rp[32];
-                tmem_load_32(t_sb + 32 * c, rs);
-                tmem_load_32(t_pb + 32 * c, rp);
+                uint32_t rs[32];
+                tmem_load_32(t_s(j) + t_row + 32 * c, rs);
                 tmem_wait_load();
-                const bool all_vis = __all_sync(0xffffffffu, lim >= 32 * c + 31);
+                if (__all_sync(0xffffffffu, lim >= 32 * c + 31)) {  // every column visible: no mask
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pr[32 * c + i] = ex2(fmaf(__uint_as_float(rs[i]), p.scale_log2, -lse));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        pr[32 * c + i] = keep_if(ex2(fmaf(__uint_as_float(rs[i]), p.scale_log2, -lse)), 32 * c + i <= lim);
+                }
+            }
+            if (!warp_wait(dp_full, j & 1, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t rp[32];
+                tmem_load_32(t_dp + t_row + 32 * c, rp);
+                tmem_wait_load();
                 uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float ds2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int i = 2 * e + u;
-                        const float pr = ex2(fmaf(__uint_as_float(rs[i]), p.scale_log2, -lse));
-                        float ds = pr * (__uint_as_float(rp[i]) - dv);
-                        if (!all_vis) ds = 32 * c + i <= lim ? ds : 0.f;
-                        ds2[u] = ds;
-                    }
-                    w[e] = pack_bf16x2(ds2[0], ds2[1]);
-                }
-                // packed columns 16 c .. 16 c + 15 of the buffer lie in columns already read
-                tmem_store_16(t_sb + 16 * c, w);
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16x2(pr[32 * c + 2 * e] * (__uint_as_float(rp[2 * e]) - dv),
+                                       pr[32 * c + 2 * e + 1] * (__uint_as_float(rp[2 * e + 1]) - dv));
+                // packed columns 16 c .. 16 c + 15 of the group's S columns, all read above
+                tmem_store_16(t_s(j) + t_row + 16 * c, w);
             }
             tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(ds_full(gi));
+            mbar_arrive(ds_full);
         }
         // group gi stores dQ columns [D/2 gi, D/2 (gi + 1))
         if (ok && warp_wait(done, 0, p.status)) {
             tc_fence_after();
             uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(q) * p.ld_out + h * D;
+            const uint32_t t_q = t_dq + (static_cast<uint32_t>(qw * 32) << 16);
 #pragma unroll 1
             for (int c = gi * (D / 64); c < (gi + 1) * (D / 64); ++c) {
                 uint32_t r[32];
-                tmem_load_32(t_dq + t_row + 32 * c, r);
+                tmem_load_32(t_q + 32 * c, r);
                 tmem_wait_load();
                 if (valid) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
@@ -601,50 +636,58 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
 
 // ------------------------------------------------------------------------ backward: dk, dv
 
-// Work runs in sub-blocks of 64 queries (two per loaded 128-query tile), with
-// two tensor-memory buffers each for S^T and dP^T, one per group of row warps:
-// while the two groups turn sub-blocks i and i + 1 into P^T and dS^T, the
-// tensor cores run the dV / dK updates of sub-block i - 1 and the S^T and dP^T
-// of the next sub-block as soon as a buffer frees.  P^T and dS^T
-// never touch shared memory: each thread writes its key row of them, as packed
-// bf16 pairs, over the buffer columns it has just read, and the dV and dK
-// products take them as their A operand from tensor memory.  Shared memory
-// holds K, V and a ring of four query-side stages, each the 64 query rows of
-// one sub-block (Q, dO, lse and dvec): a stage frees as soon as its sub-block's
-// dV / dK products are done, so the loads run three sub-blocks ahead.
+// One CTA per (kv head, key block) walks every query head of the group and
+// every query block from the diagonal on, 128 queries a step.  Per step the
+// tensor cores run S^T = K Q^T and dP^T = V dO^T (128 x 128, K-major
+// operands), then dV += P^T dO and dK += dS^T Q (A = P^T / dS^T from tensor
+// memory, B = dO / Q as MN-major operands).  The MMA order is dV[i],
+// S^T[i+1], dK[i], dP^T[i+1]: the row warps turn S^T[i] into P^T while
+// dK[i-1] and dP^T[i] run, and dP^T[i] into dS^T while dV[i] and S^T[i+1]
+// run, so single S^T and dP^T buffers keep the tensor pipe fed and leave room
+// for the dV and dK accumulators in the 512 tensor-memory columns.  Two groups
+// of four row warps take 64 query columns each; P stays in registers between
+// the two passes.  Shared memory holds K, V, a ring of three Q stages, two dO
+// stages and two stages of the queries' lse and dvec.
 template <int D>
 struct DkvSmem {
-    static constexpr int kStages = 4;
+    static constexpr int kQStages = 3, kDoStages = 2, kStatStages = 2;
     static constexpr uint32_t kTile = D * 256;
-    static constexpr uint32_t kHalf = D * 128;  // 64 rows
-    static constexpr uint32_t kK = 0;
-    static constexpr uint32_t kV = kTile;
-    static constexpr uint32_t kQD = 2 * kTile;                      // stage s: Q at kQD + 2 s kHalf, dO after it
-    static constexpr uint32_t kStat = kQD + 2 * kStages * kHalf;    // stage s: lse then dvec of its 64 queries
-    static constexpr uint32_t kBars = kStat + 512 * kStages;
-    static constexpr size_t kBytes = 1024 + kBars + 16 * 8 > kMinSmem ? 1024 + kBars + 16 * 8 : kMinSmem;
+    static constexpr uint32_t kK = 0, kV = kTile, kQ = 2 * kTile;
+    static constexpr uint32_t kDO = kQ + kQStages * kTile;
+    static constexpr uint32_t kStat = kDO + kDoStages * kTile;  // stage s: lse (512 bytes) then dvec (512 bytes)
+    static constexpr uint32_t kBars = kStat + 1024 * kStatStages;
+    static constexpr int kNumBars = 1 + 2 * (kQStages + kDoStages + kStatStages) + 6;
+    static constexpr size_t kBytes = kBars + 8 * kNumBars + 16;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kAttnBwdThreads, 1)
-    attn_causal_dkdv_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_qkv64,
-                            const __grid_constant__ CUtensorMap map_do64, const AttnParams p) {
+    attn_causal_dkdv_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
+                            const AttnParams p) {
     using L = DkvSmem<D>;
-    constexpr int NS = L::kStages;
-    constexpr uint32_t kTile = L::kTile, kHalf = L::kHalf;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_addr(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t s_k = base + L::kK, s_v = base + L::kV, s_qd = base + L::kQD, s_stat = base + L::kStat;
+    constexpr int NQ = L::kQStages, ND = L::kDoStages, NT = L::kStatStages;
+    constexpr uint32_t kTile = L::kTile;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_addr(smem_raw);
+    if (base & 1023u) {  // the tiles' 128-byte swizzle needs a 1 KiB-aligned start
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, kSiteAttn);
+        return;
+    }
+    const uint32_t s_k = base + L::kK, s_v = base + L::kV, s_q = base + L::kQ, s_do = base + L::kDO,
+                   s_stat = base + L::kStat;
     const uint32_t bars = base + L::kBars;
     const uint32_t kv_full = bars;
-    auto qd_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto qd_empty = [&](int s) { return bars + 8u * (1 + NS + s); };
-    auto sp_full = [&](int b) { return bars + 8u * (1 + 2 * NS + b); };
-    auto pd_full = [&](int b) { return bars + 8u * (3 + 2 * NS + b); };
-    const uint32_t done = bars + 8u * (5 + 2 * NS), drain = bars + 8u * (6 + 2 * NS);
-    const uint32_t tmem_slot = bars + 8u * (7 + 2 * NS);
-    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
+    auto q_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto q_empty = [&](int s) { return bars + 8u * (1 + NQ + s); };
+    auto do_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + s); };
+    auto do_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + s); };
+    auto st_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + s); };
+    auto st_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + NT + s); };
+    constexpr int kB = 1 + 2 * (NQ + ND + NT);
+    const uint32_t s_full = bars + 8u * kB, dp_full = bars + 8u * (kB + 1), p_full = bars + 8u * (kB + 2),
+                   ds_full = bars + 8u * (kB + 3), done = bars + 8u * (kB + 4), drain = bars + 8u * (kB + 5);
+    const uint32_t tmem_slot = bars + 8u * L::kNumBars;
+    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - base));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int group = p.n_heads / p.n_kv_heads;
@@ -654,35 +697,40 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     int s0, s1;
     seq_bounds(p, k0, s0, s1);
     const int qb_last = (s1 - 1) / kRows;
-    const int n_tiles = group * (qb_last - kb + 1);  // (query block, head of the group) pairs
-    const int n_sub = 2 * n_tiles;
+    const int n_steps = group * (qb_last - kb + 1);  // (query block, head of the group) pairs
     const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(qd_full(s), 1);
-            mbar_init(qd_empty(s), 1);
+        for (int s = 0; s < NQ; ++s) {
+            mbar_init(q_full(s), 1);
+            mbar_init(q_empty(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(sp_full(b), 1);
-            mbar_init(pd_full(b), 128);
+        for (int s = 0; s < ND; ++s) {
+            mbar_init(do_full(s), 1);
+            mbar_init(do_empty(s), 1);
         }
+        for (int s = 0; s < NT; ++s) {
+            mbar_init(st_full(s), 1);
+            mbar_init(st_empty(s), 256);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_full, 256);
+        mbar_init(ds_full, 256);
         mbar_init(done, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
         tma_prefetch_map(&map_qkv);
-        tma_prefetch_map(&map_qkv64);
-        tma_prefetch_map(&map_do64);
+        tma_prefetch_map(&map_do);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot_ptr;
-    // columns: S^T buffers 0-63 and 64-127 (P^T packed into the first 32 of a
-    // buffer once read), dP^T buffers 128-191 and 192-255 (dS^T likewise),
-    // dV 256.., dK 256 + D..
+    // columns: S^T 0-127 (P^T packed into 0-31 and 64-95 once read), dP^T
+    // 128-255 (dS^T likewise), dV 256.., dK 256 + D..
     const uint32_t t_s = tmem_base, t_dp = tmem_base + 128, t_dv = tmem_base + 256, t_dk = tmem_base + 256 + D;
 
     if (warp == 0) {
@@ -690,74 +738,86 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             mbar_arrive_expect_tx(kv_full, 2 * kTile);
             load_tile<D>(s_k, &map_qkv, kv_full, kcol, k0);
             load_tile<D>(s_v, &map_qkv, kv_full, vcol, k0);
-            uint32_t n_fills = 0;
-            for (int it = 0; it < n_sub; ++it) {
-                // sub-block it: query rows qb * 128 + 64 (it & 1) .. +63 of head h
-                const int st = it % NS, tile = it >> 1;
-                const int qb = kb + tile / group;
-                const int h = g * group + tile % group;
-                const int r0 = qb * kRows + 64 * (it & 1);
-                if (!mbar_wait(qd_empty(st), ((it / NS) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(qd_full(st), 2 * kHalf + 512);
-                const uint32_t q_half = s_qd + 2 * st * kHalf;
-                load_half<D>(q_half, &map_qkv64, qd_full(st), h * D, r0);
-                load_half<D>(q_half + kHalf, &map_do64, qd_full(st), h * D, r0);
-                const uint32_t stat = s_stat + 512u * st;
-                bulk_load_1d(stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + r0, 256, qd_full(st));
-                bulk_load_1d(stat + 256, p.dvec + static_cast<int64_t>(h) * p.ld_stat + r0, 256, qd_full(st));
-                ++n_fills;
+            uint32_t nq = 0, nd = 0, nt = 0;
+            for (int i = 0; i < n_steps; ++i) {
+                const int qb = kb + i / group;
+                const int h = g * group + i % group;
+                const int r0 = qb * kRows;
+                if (!mbar_wait(q_empty(i % NQ), ((i / NQ) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(q_full(i % NQ), kTile);
+                load_tile<D>(s_q + (i % NQ) * kTile, &map_qkv, q_full(i % NQ), h * D, r0);
+                ++nq;
+                if (!mbar_wait(do_empty(i % ND), ((i / ND) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(do_full(i % ND), kTile);
+                load_tile<D>(s_do + (i % ND) * kTile, &map_do, do_full(i % ND), h * D, r0);
+                ++nd;
+                if (!mbar_wait(st_empty(i % NT), ((i / NT) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                const uint32_t stat = s_stat + 1024u * (i % NT);
+                mbar_arrive_expect_tx(st_full(i % NT), 1024);
+                bulk_load_1d(stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
+                bulk_load_1d(stat + 512, p.dvec + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
+                ++nt;
             }
             mbar_wait(kv_full, 0, p.status, kSiteDrain);
-            for (int s = 0; s < NS; ++s) {
-                const uint32_t u = ring_uses(n_fills, NS, s);
-                if (u > 0) mbar_wait(qd_full(s), (u - 1) & 1, p.status, kSiteDrain);
+            for (int s = 0; s < NQ; ++s) {
+                const uint32_t u = ring_uses(nq, NQ, s);
+                if (u > 0) mbar_wait(q_full(s), (u - 1) & 1, p.status, kSiteDrain);
+            }
+            for (int s = 0; s < ND; ++s) {
+                const uint32_t u = ring_uses(nd, ND, s);
+                if (u > 0) mbar_wait(do_full(s), (u - 1) & 1, p.status, kSiteDrain);
+            }
+            for (int s = 0; s < NT; ++s) {
+                const uint32_t u = ring_uses(nt, NT, s);
+                if (u > 0) mbar_wait(st_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 64, false, false);
+            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_g = mma_idesc_bf16(128, D, false, true);
-            bool ok = mbar_wait(kv_full, 0, p.status, kSiteAttn);
-            for (int it = 0; ok && it <= n_sub; ++it) {
-                if (it < n_sub) {
-                    // S^T / dP^T of sub-block it reuse the buffers of it - 2, whose
-                    // P^T / dS^T feed products issued earlier, which run first
-                    const int half = it & 1, st = it % NS;
-                    if (!mbar_wait(qd_full(st), (it / NS) & 1, p.status, kSiteAttn)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t q_half = s_qd + 2 * st * kHalf;
-                    const uint64_t k_desc = kdesc_base(s_k), v_desc = kdesc_base(s_v);
-                    const uint64_t q_desc = kdesc_base(q_half), do_desc = kdesc_base(q_half + kHalf);
+            const uint64_t k_desc = kdesc_base(s_k), v_desc = kdesc_base(s_v);
+            auto issue_s = [&](int i) {
+                const int st = i % NQ;
+                if (!mbar_wait(q_full(st), (i / NQ) & 1, p.status, kSiteAttn)) return false;
+                tc_fence_after();
+                const uint64_t q_desc = kdesc_base(s_q + st * kTile);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_s + 64 * half, kdesc_at(k_desc, kk), kdesc64_at(q_desc, kk), idesc_s, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(t_s, kdesc_at(k_desc, kk), kdesc_at(q_desc, kk), idesc_s, kk > 0);
+                umma_commit(s_full);
+                return true;
+            };
+            auto issue_dp = [&](int i) {
+                const int st = i % ND;
+                if (!mbar_wait(do_full(st), (i / ND) & 1, p.status, kSiteAttn)) return false;
+                tc_fence_after();
+                const uint64_t do_desc = kdesc_base(s_do + st * kTile);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(t_dp + 64 * half, kdesc_at(v_desc, kk), kdesc64_at(do_desc, kk), idesc_s, kk > 0);
-                    umma_commit(sp_full(half));
-                }
-                if (it > 0) {
-                    const int pi = it - 1, half = pi & 1, st = pi % NS;
-                    if (!mbar_wait(pd_full(half), (pi >> 1) & 1, p.status, kSiteAttn)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t q_half = s_qd + 2 * st * kHalf;
-                    const uint64_t q_desc = mndesc64_base(q_half), do_desc = mndesc64_base(q_half + kHalf);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(t_dp, kdesc_at(v_desc, kk), kdesc_at(do_desc, kk), idesc_s, kk > 0);
+                umma_commit(dp_full);
+                return true;
+            };
+            bool ok = mbar_wait(kv_full, 0, p.status, kSiteAttn) && issue_s(0) && issue_dp(0);
+            for (int i = 0; ok && i < n_steps; ++i) {
+                if (!mbar_wait(p_full, i & 1, p.status, kSiteAttn)) break;
+                tc_fence_after();
+                const uint64_t do_mn = mndesc_base(s_do + (i % ND) * kTile);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ts(t_dv, t_s + 64 * half + 8 * kk, mndesc_at(do_desc, kk), idesc_g,
-                                     (pi > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_bf16_ts(t_dv, t_s + packed_col(kk), mndesc_at(do_mn, kk), idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(do_empty(i % ND));
+                // S^T[i+1] overwrites the S^T buffer after dV[i] has read P^T[i] from it
+                if (i + 1 < n_steps && !issue_s(i + 1)) break;
+                if (!mbar_wait(ds_full, i & 1, p.status, kSiteAttn)) break;
+                tc_fence_after();
+                const uint64_t q_mn = mndesc_base(s_q + (i % NQ) * kTile);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ts(t_dk, t_dp + 64 * half + 8 * kk, mndesc_at(q_desc, kk), idesc_g,
-                                     (pi > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(qd_empty(st));
-                }
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_bf16_ts(t_dk, t_dp + packed_col(kk), mndesc_at(q_mn, kk), idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(q_empty(i % NQ));
+                if (i + 1 < n_steps && !issue_dp(i + 1)) break;
             }
             umma_commit(done);
             umma_commit(drain);
@@ -765,84 +825,104 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
         }
     } else {
         // ---------------- two groups of four warps, one key row per thread in each:
-        // group gi takes the sub-blocks of buffer gi (it = gi, gi + 2, ...), so the
-        // elementwise passes of two neighbouring sub-blocks run at once
+        // group gi takes query columns 64 gi .. 64 gi + 63 of every step
         const int gi = (warp - 2) >> 2;
         const int qw = warp & 3;
         const int row = qw * 32 + lane;
         const int k = k0 + row;
-        const uint32_t t_row = static_cast<uint32_t>(qw * 32) << 16;
-        const uint32_t t_sb = t_s + t_row + 64 * gi, t_pb = t_dp + t_row + 64 * gi;
+        const uint32_t t_row = (static_cast<uint32_t>(qw * 32) << 16) + 64u * gi;
         bool ok = true;
-        for (int it = gi; it < n_sub; it += 2) {
-            const int tile = it >> 1, st = it % NS;
-            const int q0 = (kb + tile / group) * kRows + 64 * gi;
-            if (!warp_wait(qd_full(st), (it / NS) & 1, p.status) || !warp_wait(sp_full(gi), (it >> 1) & 1, p.status)) {
+        for (int i = 0; i < n_steps; ++i) {
+            const int qc0 = (kb + i / group) * kRows + 64 * gi;  // query of this group's first column
+            // query column c is visible to this key when first <= c <= last
+            const int first = k - qc0;
+            const int last = s1 - 1 - qc0;
+            // lse of this group's 64 queries, then (512 bytes on) their dvec; plain
+            // shared-memory reads the compiler may schedule freely (they stay after
+            // the barrier wait above, which clobbers memory)
+            const float4* stat_p =
+                reinterpret_cast<const float4*>(smem_raw + (s_stat - base) + 1024u * (i % NT) + 256u * gi);
+            if (!warp_wait(st_full(i % NT), (i / NT) & 1, p.status) || !warp_wait(s_full, i & 1, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // lse of this sub-block's 64 queries, then (256 bytes on) their dvec
-            const uint32_t stat = s_stat + 512u * st;
-            // query column c is visible to this key when first <= c <= last
-            const int first = k - q0;
-            const int last = s1 - 1 - q0;
-#pragma unroll 1
+            float pr[64];
+#pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t rs[32], rp[32];
-                tmem_load_32(t_sb + 32 * c, rs);
-                tmem_load_32(t_pb + 32 * c, rp);
+                uint32_t rs[32];
+                tmem_load_32(t_s + t_row + 32 * c, rs);
                 tmem_wait_load();
-                // below the diagonal and inside the sequence every column is visible:
-                // no per-element mask (statistics past the sequence end are never
-                // written; masked elements are selected away, never used)
+                // below the diagonal and inside the sequence every column is visible;
+                // statistics past the sequence end are never written, and masked
+                // elements are selected away, never used
                 const bool all_vis = __all_sync(0xffffffffu, first <= 32 * c && last >= 32 * c + 31);
-                uint32_t wp[16], wd[16];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float4 l4 = ld_shared_f4(stat + 4u * (32 * c + 4 * j));
-                    const float4 d4 = ld_shared_f4(stat + 256u + 4u * (32 * c + 4 * j));
+                    const float4 l4 = stat_p[8 * c + j];
                     const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pv[4], dsv[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int i = 4 * j + u;
-                        float pr = ex2(fmaf(__uint_as_float(rs[i]), p.scale_log2, -lv[u]));
-                        float ds = pr * (__uint_as_float(rp[i]) - dvv[u]);
-                        if (!all_vis) {
-                            const int col = 32 * c + i;
-                            const bool vis = col >= first && col <= last;
-                            pr = vis ? pr : 0.f;
-                            ds = vis ? ds : 0.f;
-                        }
-                        pv[u] = pr;
-                        dsv[u] = ds;
-                    }
-                    wp[2 * j] = pack_bf16x2(pv[0], pv[1]);
-                    wp[2 * j + 1] = pack_bf16x2(pv[2], pv[3]);
-                    wd[2 * j] = pack_bf16x2(dsv[0], dsv[1]);
-                    wd[2 * j + 1] = pack_bf16x2(dsv[2], dsv[3]);
+                    for (int u = 0; u < 4; ++u)
+                        pr[32 * c + 4 * j + u] = ex2(fmaf(__uint_as_float(rs[4 * j + u]), p.scale_log2, -lv[u]));
                 }
-                // packed columns 16 c .. 16 c + 15 of the buffer lie in columns already read
-                tmem_store_16(t_sb + 16 * c, wp);
-                tmem_store_16(t_pb + 16 * c, wd);
+                if (!all_vis) {  // one warp-uniform branch per chunk, bit masks inside
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pr[32 * c + i] = keep_if(pr[32 * c + i], (32 * c + i >= first) & (32 * c + i <= last));
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(pr[32 * c + 2 * e], pr[32 * c + 2 * e + 1]);
+                // packed columns 16 c .. 16 c + 15 of the group's columns, all read above
+                tmem_store_16(t_s + t_row + 16 * c, w);
             }
             tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(pd_full(gi));
+            mbar_arrive(p_full);
+            if (!warp_wait(dp_full, i & 1, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t rp[32];
+                tmem_load_32(t_dp + t_row + 32 * c, rp);
+                tmem_wait_load();
+                const bool all_vis = __all_sync(0xffffffffu, first <= 32 * c && last >= 32 * c + 31);
+                float ds[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 d4 = stat_p[32 + 8 * c + j];
+                    const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        ds[4 * j + u] = pr[32 * c + 4 * j + u] * (__uint_as_float(rp[4 * j + u]) - dvv[u]);
+                }
+                if (!all_vis) {  // masked columns may hold statistics past the sequence end
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ds[i] = keep_if(ds[i], (32 * c + i >= first) & (32 * c + i <= last));
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
+                tmem_store_16(t_dp + t_row + 16 * c, w);
+            }
+            tmem_wait_store();
+            tc_fence_before();
+            mbar_arrive(ds_full);
+            mbar_arrive(st_empty(i % NT));
         }
         // group 0 stores dK, group 1 dV
         if (ok && warp_wait(done, 0, p.status)) {
             tc_fence_after();
             const bool valid = k < s1;
-            const uint32_t t_acc = gi == 0 ? t_dk : t_dv;
+            const uint32_t t_acc = (gi == 0 ? t_dk : t_dv) + (static_cast<uint32_t>(qw * 32) << 16);
             uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(k) * p.ld_out + (gi == 0 ? kcol : vcol);
             const float sc = gi == 0 ? p.scale : 1.f;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
-                tmem_load_32(t_acc + t_row + 32 * c, r);
+                tmem_load_32(t_acc + 32 * c, r);
                 tmem_wait_load();
                 if (valid) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
@@ -920,13 +1000,13 @@ PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
     return fn;
 }
 
-// [rows, cols] bf16, row stride ld elements; boxes of 64 columns x box_rows rows, 128B swizzle.
-bool attn_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows = 128) {
+// [rows, cols] bf16, row stride ld elements; boxes of 64 columns x 128 rows, 128B swizzle.
+bool attn_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld) {
     auto fn = attn_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t box[2] = {64, 128};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -982,9 +1062,8 @@ cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const
     if (err != cudaSuccess) return err;
     const int qkv_w = (s.n_heads + 2 * s.n_kv_heads) * D;
     const int hw = s.n_heads * D;
-    CUtensorMap mq, md, mq64, md64;
-    if (!attn_map(&mq, qkv, s.tokens, qkv_w, qkv_w) || !attn_map(&md, da, s.tokens, hw, hw) ||
-        !attn_map(&mq64, qkv, s.tokens, qkv_w, qkv_w, 64) || !attn_map(&md64, da, s.tokens, hw, hw, 64))
+    CUtensorMap mq, md;
+    if (!attn_map(&mq, qkv, s.tokens, qkv_w, qkv_w) || !attn_map(&md, da, s.tokens, hw, hw))
         return cudaErrorInvalidValue;
     AttnParams p = make_params(s);
     if (!p.status) return cudaErrorInvalidDevice;
@@ -997,11 +1076,10 @@ cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const
         static_cast<const uint16_t*>(da), static_cast<const uint16_t*>(a), dvec, s.tokens, s.n_heads, D, s.ld_stat);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_causal_dkdv_kernel<D><<<p.n_blocks * s.n_kv_heads, kAttnBwdThreads, DkvSmem<D>::kBytes, stream>>>(mq, mq64, md64,
-                                                                                                         p);
+    attn_causal_dkdv_kernel<D><<<p.n_blocks * s.n_kv_heads, kAttnBwdThreads, DkvSmem<D>::kBytes, stream>>>(mq, md, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_causal_dq_kernel<D><<<p.n_blocks * s.n_heads, kAttnBwdThreads, DqSmem<D>::kBytes, stream>>>(mq, md, mq64, p);
+    attn_causal_dq_kernel<D><<<p.n_blocks * s.n_heads, kAttnBwdThreads, DqSmem<D>::kBytes, stream>>>(mq, md, p);
     return cudaGetLastError();
 }
 
