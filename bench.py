@@ -524,7 +524,7 @@ def wgrad_sweep_record(tokens, steps, warmup, peaks):
     return out
 
 
-def other_configs(args, st, peaks):
+def other_workloads(args, st, peaks):
     """The rest of the workload list, each timed on its own stage after the headline: the
     70B-shaped stage, the ZB-H1 order of stage 3 of p = 8 over 16 microbatches (on the
     headline's weights), the 8B-shaped stage with the causal attention core, and the wgrad
@@ -545,7 +545,7 @@ def other_configs(args, st, peaks):
     rec = measure_config(w8, zb.zb_schedule("zbh1", 3, 8, 16), steps, warmup, peaks, "bf16_tflops_sustained",
                          params=params)
     rec["order"] = "ZB-H1 order of stage 3 of p = 8, m = 16 (library generator), 8 stash slots"
-    out["config4_zbh1_stage3_p8_m16"] = rec
+    out["zbh1_stage3_p8_m16"] = rec
     del params
     torch.cuda.empty_cache()
     w70 = WORKLOADS["llama70b_stage"]
@@ -831,8 +831,8 @@ def run_ours(args, w):
                 "b_tflops_with_attention": (b_flops + ab["flops"]) / (b_ms * 1e-3) / 1e12,
             }
         if (world == 1 and args.workload == "llama8b_stage" and args.w_mode == "per-microbatch"
-                and not args.overridden and args.stage == 0 and not args.pipeline and not args.no_configs):
-            line["configs"] = other_configs(args, st, peaks)
+                and not args.overridden and args.stage == 0 and not args.pipeline and not args.no_workloads):
+            line["workloads"] = other_workloads(args, st, peaks)
         print(json.dumps(line), flush=True)
     st.close()
     if dist is not None:
@@ -924,8 +924,8 @@ def main():
                     help="tokens of the microbatch the host oracle runs (cpu_baseline / reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-configs", action="store_true",
-                    help="skip the sub-records of the other workloads (70B, config 4, causal, wgrad sweep)")
+    ap.add_argument("--no-workloads", "--no-configs", dest="no_workloads", action="store_true",
+                    help="skip the sub-records of the other workloads (70B-shaped stage, ZB-H1 order of stage 3, causal, wgrad sweep)")
     ap.add_argument("--w-mode", choices=["per-microbatch", "flush"], default="per-microbatch",
                     help="W as one call per microbatch (the ZB-H1 order) or batched in one flush")
     ap.add_argument("--op", choices=["backward_weight", "backward_input", "backward_input_swiglu", "forward",

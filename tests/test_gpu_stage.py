@@ -115,7 +115,7 @@ def test_small_transformer_ragged_tokens():
 
 
 def test_llama8b_shaped_stage_short_microbatches():
-    """Config 2 shapes (4 layers, 4096 / 14336, 32 / 8 heads) with 128- and 100-token microbatches."""
+    """8B-shaped stage (4 layers, 4096 / 14336, 32 / 8 heads) with 128- and 100-token microbatches."""
     c = LLAMA8B
     inp = synth.stage_inputs(c["kind"], 4, 4096, 14336, 32, 8, 128, n_mb=2, seed=0, tokens_per_mb=[128, 100])
     st = make_gpu_stage(c, inp, 128, 2)
@@ -125,7 +125,7 @@ def test_llama8b_shaped_stage_short_microbatches():
 
 
 def test_llama70b_shaped_stage_short_microbatch():
-    """Config 3 shapes (2 layers, 8192 / 28672, 64 / 8 heads) with one 64-token microbatch."""
+    """70B-shaped stage (2 layers, 8192 / 28672, 64 / 8 heads) with one 64-token microbatch."""
     c = LLAMA70B
     inp = synth.stage_inputs(c["kind"], 2, 8192, 28672, 64, 8, 128, n_mb=1, seed=0, tokens=64)
     st = make_gpu_stage(c, inp, 64, 1)
@@ -145,7 +145,7 @@ def sampled_token_check(c, inp, dx_gpu, mb, rows):
     assert_close(got, ref, f"sampled dx of microbatch {mb}", fro_tol=stage_fro_tol(c["n_layers"]))
 
 
-def test_config4_zbh1_order_full_size():
+def test_zbh1_stage3_p8_m16_order_full_size():
     """ZB-H1 order of stage 3 (p = 8, m = 16) on the 8B-shaped stage at 4096 tokens:
     runs within the p-microbatch ceiling, gives the same weight gradients bit for bit as
     the 1F1B order, and sampled tokens match the oracle."""
@@ -201,7 +201,7 @@ def test_concat_identity_full_size():
 
 
 @pytest.mark.parametrize("tokens", [512, 1024, 2048, 4096, 8192])
-def test_config5_linear_sweep(tokens):
+def test_linear_4096x14336_token_sweep(tokens):
     """One linear, in 4096, out 14336, m = 4: dW (float32, accumulated) and dx against the
     oracle on sampled rows; each is a single step, so the single-step tolerance applies."""
     n_in, n_out, m = 4096, 14336, 4

@@ -60,8 +60,13 @@ class Report:
     def worst(self):
         return max(r[1] for r in self.rows), max(r[2] for r in self.rows)
 
-    def assert_ok(self):
+    def assert_ok(self, title=""):
         assert self.rows, "nothing compared"
+        fro = max(self.rows, key=lambda r: r[1])
+        mx = max(self.rows, key=lambda r: r[2])
+        # the worst cases, for the record (shown with pytest -s)
+        print(f"\n{title}: {len(self.rows)} comparisons; worst frobenius {fro[1]:.2e} ({fro[0]}), "
+              f"worst max-abs {mx[2]:.2e} ({mx[0]})")
         assert not self.misses, "\n".join(self.misses)
 
 
@@ -212,12 +217,12 @@ LLAMA70B = dict(kind="transformer", n_layers=2, hidden=8192, ffn=28672, n_heads=
 
 
 def test_tiny_config_every_step_flush():
-    """Config 1 (2 MLP layers, 256 / 1024, 128 tokens, m = 4): every step of both layers of all
+    """The tiny MLP stage (2 layers, 256 / 1024, 128 tokens, m = 4): every step of both layers of all
     four microbatches, W batched by the flush over the four full slots."""
     inp = synth.stage_inputs("mlp", 2, 256, 1024, tokens=128, n_mb=4, seed=0)
     rep, st = run_stash_fed(TINY, inp, 4, w_mode="flush")
     st.close()
-    rep.assert_ok()
+    rep.assert_ok("test_tiny_config_every_step_flush")
 
 
 def test_small_transformer_ragged_every_step():
@@ -226,7 +231,7 @@ def test_small_transformer_ragged_every_step():
     inp = synth.stage_inputs("transformer", 2, 256, 512, 4, 2, 64, n_mb=3, seed=1, tokens_per_mb=[200, 77, 1])
     rep, st = run_stash_fed(SMALL_TF, inp, 3)
     st.close()
-    rep.assert_ok()
+    rep.assert_ok("test_small_transformer_ragged_every_step")
 
 
 def test_causal_8b_widths_every_step():
@@ -236,24 +241,24 @@ def test_causal_8b_widths_every_step():
     inp = synth.stage_inputs("transformer", 2, 4096, 14336, 32, 8, 128, tokens=512, n_mb=2, seed=5)
     rep, st = run_stash_fed(c, inp, 2, w_mode="flush", attention="causal", seq_len=256)
     st.close()
-    rep.assert_ok()
+    rep.assert_ok("test_causal_8b_widths_every_step")
 
 
-def test_config2_full_size_every_step_and_end_to_end():
-    """Config 2 at full size: the 8B-shaped 4-layer stage, one 4096-token microbatch.  Every
+def test_llama8b_stage_full_size_every_step_and_end_to_end():
+    """At full size: the 8B-shaped 4-layer stage, one 4096-token microbatch.  Every
     step of every layer at the per-step bar (its GEMMs split K in their last wave exactly as in
     the benchmark), then dx, all 16 weight gradients and 8 gamma gradients against the oracle
     run end to end on the caller's inputs, at the 4-layer stage tolerance."""
     inp = synth.stage_inputs("transformer", 4, 4096, 14336, 32, 8, 128, tokens=4096, n_mb=1, seed=0)
     rep, st = run_stash_fed(LLAMA8B, inp, 1, end_to_end_tol=stage_fro_tol(4))
     st.close()
-    rep.assert_ok()
+    rep.assert_ok("test_llama8b_stage_full_size_every_step_and_end_to_end")
 
 
-def test_config3_full_size_every_step_and_end_to_end():
-    """Config 3 at full size: the 70B-shaped 2-layer stage (8192 / 28672, 64 / 8 heads), one
-    4096-token microbatch, as for config 2."""
+def test_llama70b_stage_full_size_every_step_and_end_to_end():
+    """At full size: the 70B-shaped 2-layer stage (8192 / 28672, 64 / 8 heads), one
+    4096-token microbatch, as for the 8B-shaped stage."""
     inp = synth.stage_inputs("transformer", 2, 8192, 28672, 64, 8, 128, tokens=4096, n_mb=1, seed=0)
     rep, st = run_stash_fed(LLAMA70B, inp, 1, end_to_end_tol=stage_fro_tol(2))
     st.close()
-    rep.assert_ok()
+    rep.assert_ok("test_llama70b_stage_full_size_every_step_and_end_to_end")

@@ -55,7 +55,7 @@ def test_generator_equals_oracle(zblib, kind):
                 assert zb.zb_schedule(kind, s, p, m) == ref[s], (kind, s, p, m)
 
 
-def test_config4_zbh1_order(zblib):
+def test_zbh1_stage3_p8_m16_order(zblib):
     """ZB-H1 for stage 3 of p = 8, m = 16: W deferred behind B, steady B W F rhythm, drain at the end."""
     got = " ".join(f"{k}{i}" for k, i in zb.zb_schedule("zbh1", 3, 8, 16))
     want = ("F0 F1 F2 F3 F4 B0 F5 B1 F6 B2 F7 B3 W0 F8 B4 W1 F9 B5 W2 F10 B6 W3 F11 B7 W4 F12 "
