@@ -121,6 +121,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* st
     return __all_sync(0xffffffffu, ok);
 }
 
+// One arrival for the whole warp, after every lane's prior work: each lane has
+// waited for its tensor-memory stores and fenced them before this call.  One
+// arrival per warp instead of one per thread keeps 256 shared-memory atomics
+// on one barrier off the path between the row warps and the MMA thread.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
 // Loads one 128-row tile (d / 64 boxes) of columns col .. col + d - 1 at row r0.
 template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, int col, int r0) {
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(kv_empty(s), 1);
         }
         for (int s = 0; s < 2; ++s) mbar_init(s_full(s), 1);
-        mbar_init(p_full, 128);
+        mbar_init(p_full, 4);
         mbar_init(p_free, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
@@ -217,46 +226,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idesc_o = mma_idesc_bf16(128, D, false, true);
-            bool ok = mbar_wait(q_full, 0, p.status, kSiteAttn);
-            for (int j = 0; ok && j <= nk; ++j) {
-                if (j < nk) {
-                    // S_j reuses the buffer of S_{j-2}, whose P feeds O += P V of
-                    // step j - 2: that product was issued before and runs first
-                    const int st = j % NS;
-                    if (!mbar_wait(kv_full(st), (j / NS) & 1, p.status, kSiteAttn)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t a_desc = kdesc_base(s_q), b_desc = kdesc_base(s_kv + 2 * st * kTile);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(tmem_base + (j & 1) * 128, kdesc_at(a_desc, kk), kdesc_at(b_desc, kk), idesc_s,
-                                  kk > 0);
-                    umma_commit(s_full(j & 1));
+        // the whole warp runs the issue loop; its elected lane carries each instruction
+        const uint32_t leader = elect_one_sync();
+        constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
+        constexpr uint32_t idesc_o = mma_idesc_bf16(128, D, false, true);
+        bool ok = warp_wait(q_full, 0, p.status);
+        for (int j = 0; ok && j <= nk; ++j) {
+            if (j < nk) {
+                // S_j reuses the buffer of S_{j-2}, whose P feeds O += P V of
+                // step j - 2: that product was issued before and runs first
+                const int st = j % NS;
+                if (!warp_wait(kv_full(st), (j / NS) & 1, p.status)) {
+                    ok = false;
+                    break;
                 }
-                if (j > 0) {
-                    const int jj = j - 1, st = jj % NS;
-                    if (!mbar_wait(p_full, jj & 1, p.status, kSiteAttn)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t v_desc = mndesc_base(s_kv + (2 * st + 1) * kTile);
-                    const uint32_t t_p = tmem_base + (jj & 1) * 128;
+                tc_fence_after();
+                const uint64_t a_desc = kdesc_base(s_q), b_desc = kdesc_base(s_kv + 2 * st * kTile);
 #pragma unroll
-                    for (int kk = 0; kk < kRows / 16; ++kk)
-                        umma_bf16_ts(t_o, t_p + 8 * kk, mndesc_at(v_desc, kk), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(kv_empty(st));
-                    umma_commit(p_free);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16_elected(leader, tmem_base + (j & 1) * 128, kdesc_at(a_desc, kk), kdesc_at(b_desc, kk),
+                                      idesc_s, kk > 0);
+                umma_commit_elected(leader, s_full(j & 1));
             }
-            umma_commit(drain);
-            mbar_wait(drain, 0, p.status, kSiteDrain);
+            if (j > 0) {
+                const int jj = j - 1, st = jj % NS;
+                if (!warp_wait(p_full, jj & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t v_desc = mndesc_base(s_kv + (2 * st + 1) * kTile);
+                const uint32_t t_p = tmem_base + (jj & 1) * 128;
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_bf16_ts_elected(leader, t_o, t_p + 8 * kk, mndesc_at(v_desc, kk), idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                umma_commit_elected(leader, kv_empty(st));
+                umma_commit_elected(leader, p_free);
+            }
         }
+        umma_commit_elected(leader, drain);
+        mbar_wait(drain, 0, p.status, kSiteDrain);
     } else {
         // ---------------- softmax rows
         const int qw = warp & 3;
@@ -273,13 +282,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             tc_fence_after();
             float s[128];
+            {
+                uint32_t r[128];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_load_32(tmem_base + t_row + sb * 128 + 32 * c, r);
+                for (int c = 0; c < 4; ++c)
+                    tmem_load_32(tmem_base + t_row + sb * 128 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
                 tmem_wait_load();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(r[e]);
+                for (int e = 0; e < 128; ++e) s[e] = __uint_as_float(r[e]);
             }
             const int k0 = (kb0 + j) * kRows;
             const int lim = min(q - k0, s1 - 1 - k0);  // last visible key column of this row
@@ -341,7 +351,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             l += sum;
             tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(p_full);
+            warp_arrive(p_full, lane);
         }
         if (ok && warp_wait(p_free, (nk - 1) & 1, p.status)) {
             tc_fence_after();
@@ -456,7 +466,7 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
         mbar_init(s_full(0), 1);
         mbar_init(s_full(1), 1);
         mbar_init(dp_full, 1);
-        mbar_init(ds_full, 256);
+        mbar_init(ds_full, 8);
         mbar_init(done, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
@@ -501,50 +511,50 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idesc_q = mma_idesc_bf16(128, D, false, true);
-            const uint64_t q_desc = kdesc_base(s_q), do_desc = kdesc_base(s_do);
-            auto issue_s = [&](int j) {
-                const int st = j % NK;
-                if (!mbar_wait(k_full(st), (j / NK) & 1, p.status, kSiteAttn)) return false;
-                tc_fence_after();
-                const uint64_t k_desc = kdesc_base(s_k + st * kTile);
+        // the whole warp runs the issue loop; its elected lane carries each instruction
+        const uint32_t leader = elect_one_sync();
+        constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
+        constexpr uint32_t idesc_q = mma_idesc_bf16(128, D, false, true);
+        const uint64_t q_desc = kdesc_base(s_q), do_desc = kdesc_base(s_do);
+        auto issue_s = [&](int j) {
+            const int st = j % NK;
+            if (!warp_wait(k_full(st), (j / NK) & 1, p.status)) return false;
+            tc_fence_after();
+            const uint64_t k_desc = kdesc_base(s_k + st * kTile);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(t_s(j), kdesc_at(q_desc, kk), kdesc_at(k_desc, kk), idesc_s, kk > 0);
-                umma_commit(s_full(j & 1));
-                return true;
-            };
-            auto issue_dp = [&](int j) {
-                const int st = j % NV;
-                if (!mbar_wait(v_full(st), (j / NV) & 1, p.status, kSiteAttn)) return false;
-                tc_fence_after();
-                const uint64_t v_desc = kdesc_base(s_v + st * kTile);
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_bf16_elected(leader, t_s(j), kdesc_at(q_desc, kk), kdesc_at(k_desc, kk), idesc_s, kk > 0);
+            umma_commit_elected(leader, s_full(j & 1));
+            return true;
+        };
+        auto issue_dp = [&](int j) {
+            const int st = j % NV;
+            if (!warp_wait(v_full(st), (j / NV) & 1, p.status)) return false;
+            tc_fence_after();
+            const uint64_t v_desc = kdesc_base(s_v + st * kTile);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(t_dp, kdesc_at(do_desc, kk), kdesc_at(v_desc, kk), idesc_s, kk > 0);
-                umma_commit(dp_full);
-                umma_commit(v_empty(st));
-                return true;
-            };
-            bool ok = mbar_wait(q_full, 0, p.status, kSiteAttn) && issue_s(0) && issue_dp(0);
-            for (int j = 0; ok && j < nk; ++j) {
-                // S[j+1] into the other buffer; dP[j+1] once the row warps are done with dP[j]
-                if (j + 1 < nk && !issue_s(j + 1)) break;
-                if (!mbar_wait(ds_full, j & 1, p.status, kSiteAttn)) break;
-                tc_fence_after();
-                if (j + 1 < nk && !issue_dp(j + 1)) break;
-                const uint64_t k_mn = mndesc_base(s_k + (j % NK) * kTile);
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_bf16_elected(leader, t_dp, kdesc_at(do_desc, kk), kdesc_at(v_desc, kk), idesc_s, kk > 0);
+            umma_commit_elected(leader, dp_full);
+            umma_commit_elected(leader, v_empty(st));
+            return true;
+        };
+        bool ok = warp_wait(q_full, 0, p.status) && issue_s(0) && issue_dp(0);
+        for (int j = 0; ok && j < nk; ++j) {
+            // S[j+1] into the other buffer; dP[j+1] once the row warps are done with dP[j]
+            if (j + 1 < nk && !issue_s(j + 1)) break;
+            if (!warp_wait(ds_full, j & 1, p.status)) break;
+            tc_fence_after();
+            if (j + 1 < nk && !issue_dp(j + 1)) break;
+            const uint64_t k_mn = mndesc_base(s_k + (j % NK) * kTile);
 #pragma unroll
-                for (int kk = 0; kk < kRows / 16; ++kk)
-                    umma_bf16_ts(t_dq, t_s(j) + packed_col(kk), mndesc_at(k_mn, kk), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(k_empty(j % NK));
-            }
-            umma_commit(done);
-            umma_commit(drain);
-            mbar_wait(drain, 0, p.status, kSiteDrain);
+            for (int kk = 0; kk < kRows / 16; ++kk)
+                umma_bf16_ts_elected(leader, t_dq, t_s(j) + packed_col(kk), mndesc_at(k_mn, kk), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_commit_elected(leader, k_empty(j % NK));
         }
+        umma_commit_elected(leader, done);
+        umma_commit_elected(leader, drain);
+        mbar_wait(drain, 0, p.status, kSiteDrain);
     } else {
         // ---------------- two groups of four warps, one query row per thread in each:
         // group gi takes key columns 64 gi .. 64 gi + 63 of every step
@@ -566,18 +576,19 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             }
             tc_fence_after();
             float pr[64];
+            uint32_t rs[64];
+            tmem_load_32(t_s(j) + t_row, *reinterpret_cast<uint32_t(*)[32]>(rs));
+            tmem_load_32(t_s(j) + t_row + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+            tmem_wait_load();
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t rs[32];
-                tmem_load_32(t_s(j) + t_row + 32 * c, rs);
-                tmem_wait_load();
                 if (__all_sync(0xffffffffu, lim >= 32 * c + 31)) {  // every column visible: no mask
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) pr[32 * c + i] = ex2(fmaf(__uint_as_float(rs[i]), p.scale_log2, -lse));
+                    for (int i = 0; i < 32; ++i) pr[32 * c + i] = ex2(fmaf(__uint_as_float(rs[32 * c + i]), p.scale_log2, -lse));
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        pr[32 * c + i] = keep_if(ex2(fmaf(__uint_as_float(rs[i]), p.scale_log2, -lse)), 32 * c + i <= lim);
+                        pr[32 * c + i] = keep_if(ex2(fmaf(__uint_as_float(rs[32 * c + i]), p.scale_log2, -lse)), 32 * c + i <= lim);
                 }
             }
             if (!warp_wait(dp_full, j & 1, p.status)) {
@@ -585,22 +596,23 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
                 break;
             }
             tc_fence_after();
+            uint32_t rp[64];
+            tmem_load_32(t_dp + t_row, *reinterpret_cast<uint32_t(*)[32]>(rp));
+            tmem_load_32(t_dp + t_row + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+            tmem_wait_load();
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t rp[32];
-                tmem_load_32(t_dp + t_row + 32 * c, rp);
-                tmem_wait_load();
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(pr[32 * c + 2 * e] * (__uint_as_float(rp[2 * e]) - dv),
-                                       pr[32 * c + 2 * e + 1] * (__uint_as_float(rp[2 * e + 1]) - dv));
+                    w[e] = pack_bf16x2(pr[32 * c + 2 * e] * (__uint_as_float(rp[32 * c + 2 * e]) - dv),
+                                       pr[32 * c + 2 * e + 1] * (__uint_as_float(rp[32 * c + 2 * e + 1]) - dv));
                 // packed columns 16 c .. 16 c + 15 of the group's S columns, all read above
                 tmem_store_16(t_s(j) + t_row + 16 * c, w);
             }
             tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(ds_full);
+            warp_arrive(ds_full, lane);
         }
         // group gi stores dQ columns [D/2 gi, D/2 (gi + 1))
         if (ok && warp_wait(done, 0, p.status)) {
@@ -646,26 +658,64 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
 // run, so single S^T and dP^T buffers keep the tensor pipe fed and leave room
 // for the dV and dK accumulators in the 512 tensor-memory columns.  Two groups
 // of four row warps take 64 query columns each; P stays in registers between
-// the two passes.  Shared memory holds K, V, a ring of three Q stages, two dO
-// stages and two stages of the queries' lse and dvec.
+// the two passes.
+//
+// The per-query statistics enter through the tensor cores, not the row warps:
+// each score product gets one more K step whose A operand holds ones and
+// whose B operand holds, per query, -lse / c (for S^T) or -D (for dP^T) as
+// the sum of three bf16 parts, so the accumulators come out as S^T - lse / c
+// and dP^T - D.  Every row thread would otherwise read all 64 statistics of
+// its columns from shared memory each pass, and those broadcast reads took
+// about a quarter of the shared-memory bandwidth that the score products'
+// operands need.  A statistics warp turns each step's lse and D (landed by
+// TMA) into that B operand.  The three-part split leaves an error of about
+// 2^-27 of lse / c, far below the bf16 rounding of P.
 template <int D>
 struct DkvSmem {
-    static constexpr int kQStages = 3, kDoStages = 2, kStatStages = 2;
+    static constexpr int kQStages = 2, kDoStages = 2, kStatStages = 2, kAugStages = 2;
     static constexpr uint32_t kTile = D * 256;
+    static constexpr uint32_t kAugTile = 128 * 16 * 2;  // 128 rows x one K step of 16 bf16, no swizzle
     static constexpr uint32_t kK = 0, kV = kTile, kQ = 2 * kTile;
     static constexpr uint32_t kDO = kQ + kQStages * kTile;
-    static constexpr uint32_t kStat = kDO + kDoStages * kTile;  // stage s: lse (512 bytes) then dvec (512 bytes)
+    static constexpr uint32_t kOnes = kDO + kDoStages * kTile;  // two constant A operands: lse, D selectors
+    static constexpr uint32_t kAug = kOnes + 2 * kAugTile;      // stage s: the B operand of step s
+    static constexpr uint32_t kStat = kAug + kAugStages * kAugTile;  // stage s: lse (512 bytes) then D (512 bytes)
     static constexpr uint32_t kBars = kStat + 1024 * kStatStages;
-    static constexpr int kNumBars = 1 + 2 * (kQStages + kDoStages + kStatStages) + 6;
+    static constexpr int kNumBars = 1 + 2 * (kQStages + kDoStages + kStatStages + kAugStages) + 6;
     static constexpr size_t kBytes = kBars + 8 * kNumBars + 16;
 };
+constexpr int kAttnDkvThreads = kAttnBwdThreads + 32;  // + the statistics warp
+constexpr int kStatWarp = kAttnBwdThreads / 32;
+
+// Byte offset of row r, K chunk kc (8 bf16) of a no-swizzle K-major operand of
+// one K step: 8-row groups 256 bytes apart (the stride-dimension offset), the
+// two 8-column chunks of a row group 128 bytes apart (the leading-dimension
+// offset), rows of a chunk 16 bytes apart.
+__device__ __forceinline__ uint32_t aug_offset(int r, int kc) {
+    return static_cast<uint32_t>((r >> 3) * 256 + kc * 128 + (r & 7) * 16);
+}
+__device__ __forceinline__ uint64_t aug_desc(uint32_t tile) {
+    return static_cast<uint64_t>((tile & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
+           (static_cast<uint64_t>(256 >> 4) << 32) | (1ull << 46);  // swizzle mode 0: none
+}
+
+// v as hi + mid + lo, each bf16 (round to nearest), as the low 48 bits of a
+// 64-bit word (bf16 columns 0, 1, 2; column 3 zero).
+__device__ __forceinline__ uint2 split3_bf16(float v) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    return make_uint2(static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16),
+                      static_cast<uint32_t>(__bfloat16_as_ushort(lo)));
+}
 
 template <int D>
-__global__ void __launch_bounds__(kAttnBwdThreads, 1)
+__global__ void __launch_bounds__(kAttnDkvThreads, 1)
     attn_causal_dkdv_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
                             const AttnParams p) {
     using L = DkvSmem<D>;
-    constexpr int NQ = L::kQStages, ND = L::kDoStages, NT = L::kStatStages;
+    constexpr int NQ = L::kQStages, ND = L::kDoStages, NT = L::kStatStages, NA = L::kAugStages;
     constexpr uint32_t kTile = L::kTile;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_addr(smem_raw);
@@ -674,7 +724,7 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
         return;
     }
     const uint32_t s_k = base + L::kK, s_v = base + L::kV, s_q = base + L::kQ, s_do = base + L::kDO,
-                   s_stat = base + L::kStat;
+                   s_ones = base + L::kOnes, s_aug = base + L::kAug, s_stat = base + L::kStat;
     const uint32_t bars = base + L::kBars;
     const uint32_t kv_full = bars;
     auto q_full = [&](int s) { return bars + 8u * (1 + s); };
@@ -683,7 +733,9 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     auto do_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + s); };
     auto st_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + s); };
     auto st_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + NT + s); };
-    constexpr int kB = 1 + 2 * (NQ + ND + NT);
+    auto aug_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + 2 * NT + s); };
+    auto aug_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + 2 * NT + NA + s); };
+    constexpr int kB = 1 + 2 * (NQ + ND + NT + NA);
     const uint32_t s_full = bars + 8u * kB, dp_full = bars + 8u * (kB + 1), p_full = bars + 8u * (kB + 2),
                    ds_full = bars + 8u * (kB + 3), done = bars + 8u * (kB + 4), drain = bars + 8u * (kB + 5);
     const uint32_t tmem_slot = bars + 8u * L::kNumBars;
@@ -700,6 +752,20 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     const int n_steps = group * (qb_last - kb + 1);  // (query block, head of the group) pairs
     const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
 
+    // The constant A operands of the statistics step (ones in bf16 columns 0-2
+    // for lse, 8-10 for D) and zeros in the B operands' unused columns; the
+    // statistics warp rewrites only columns 0-2 and 8-10 of a B operand.
+    {
+        uint4* z = reinterpret_cast<uint4*>(smem_raw + L::kOnes);
+        constexpr int n16 = (2 + NA) * L::kAugTile / 16;
+        for (int e = threadIdx.x; e < n16; e += kAttnDkvThreads) {
+            const int tile = e / (L::kAugTile / 16);
+            const int kc = (e >> 3) & 1;  // 16-byte rows: 8 rows per chunk, chunks alternate every 128 bytes
+            const bool ones = tile < 2 && kc == tile;
+            z[e] = ones ? make_uint4(0x3F803F80u, 0x3F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+    }
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         for (int s = 0; s < NQ; ++s) {
@@ -712,12 +778,16 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
         }
         for (int s = 0; s < NT; ++s) {
             mbar_init(st_full(s), 1);
-            mbar_init(st_empty(s), 256);
+            mbar_init(st_empty(s), 1);
+        }
+        for (int s = 0; s < NA; ++s) {
+            mbar_init(aug_full(s), 1);
+            mbar_init(aug_empty(s), 1);
         }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
-        mbar_init(p_full, 256);
-        mbar_init(ds_full, 256);
+        mbar_init(p_full, 8);
+        mbar_init(ds_full, 8);
         mbar_init(done, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
@@ -743,6 +813,12 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
                 const int qb = kb + i / group;
                 const int h = g * group + i % group;
                 const int r0 = qb * kRows;
+                if (!mbar_wait(st_empty(i % NT), ((i / NT) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                const uint32_t stat = s_stat + 1024u * (i % NT);
+                mbar_arrive_expect_tx(st_full(i % NT), 1024);
+                bulk_load_1d(stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
+                bulk_load_1d(stat + 512, p.dvec + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
+                ++nt;
                 if (!mbar_wait(q_empty(i % NQ), ((i / NQ) & 1) ^ 1u, p.status, kSiteAttn)) break;
                 mbar_arrive_expect_tx(q_full(i % NQ), kTile);
                 load_tile<D>(s_q + (i % NQ) * kTile, &map_qkv, q_full(i % NQ), h * D, r0);
@@ -751,12 +827,6 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
                 mbar_arrive_expect_tx(do_full(i % ND), kTile);
                 load_tile<D>(s_do + (i % ND) * kTile, &map_do, do_full(i % ND), h * D, r0);
                 ++nd;
-                if (!mbar_wait(st_empty(i % NT), ((i / NT) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                const uint32_t stat = s_stat + 1024u * (i % NT);
-                mbar_arrive_expect_tx(st_full(i % NT), 1024);
-                bulk_load_1d(stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
-                bulk_load_1d(stat + 512, p.dvec + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
-                ++nt;
             }
             mbar_wait(kv_full, 0, p.status, kSiteDrain);
             for (int s = 0; s < NQ; ++s) {
@@ -773,55 +843,84 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idesc_g = mma_idesc_bf16(128, D, false, true);
-            const uint64_t k_desc = kdesc_base(s_k), v_desc = kdesc_base(s_v);
-            auto issue_s = [&](int i) {
-                const int st = i % NQ;
-                if (!mbar_wait(q_full(st), (i / NQ) & 1, p.status, kSiteAttn)) return false;
-                tc_fence_after();
-                const uint64_t q_desc = kdesc_base(s_q + st * kTile);
+        // the whole warp runs the issue loop; its elected lane carries each instruction
+        const uint32_t leader = elect_one_sync();
+        constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
+        constexpr uint32_t idesc_g = mma_idesc_bf16(128, D, false, true);
+        const uint64_t k_desc = kdesc_base(s_k), v_desc = kdesc_base(s_v);
+        const uint64_t ones_lse = aug_desc(s_ones), ones_d = aug_desc(s_ones + L::kAugTile);
+        auto issue_s = [&](int i) {
+            const int st = i % NQ;
+            if (!warp_wait(q_full(st), (i / NQ) & 1, p.status)) return false;
+            if (!warp_wait(aug_full(i % NA), (i / NA) & 1, p.status)) return false;
+            tc_fence_after();
+            const uint64_t q_desc = kdesc_base(s_q + st * kTile);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(t_s, kdesc_at(k_desc, kk), kdesc_at(q_desc, kk), idesc_s, kk > 0);
-                umma_commit(s_full);
-                return true;
-            };
-            auto issue_dp = [&](int i) {
-                const int st = i % ND;
-                if (!mbar_wait(do_full(st), (i / ND) & 1, p.status, kSiteAttn)) return false;
-                tc_fence_after();
-                const uint64_t do_desc = kdesc_base(s_do + st * kTile);
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_bf16_elected(leader, t_s, kdesc_at(k_desc, kk), kdesc_at(q_desc, kk), idesc_s, kk > 0);
+            umma_bf16_elected(leader, t_s, ones_lse, aug_desc(s_aug + (i % NA) * L::kAugTile), idesc_s, 1u);
+            umma_commit_elected(leader, s_full);
+            return true;
+        };
+        auto issue_dp = [&](int i) {  // after issue_s(i), which waited for the statistics operand
+            const int st = i % ND;
+            if (!warp_wait(do_full(st), (i / ND) & 1, p.status)) return false;
+            tc_fence_after();
+            const uint64_t do_desc = kdesc_base(s_do + st * kTile);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(t_dp, kdesc_at(v_desc, kk), kdesc_at(do_desc, kk), idesc_s, kk > 0);
-                umma_commit(dp_full);
-                return true;
-            };
-            bool ok = mbar_wait(kv_full, 0, p.status, kSiteAttn) && issue_s(0) && issue_dp(0);
-            for (int i = 0; ok && i < n_steps; ++i) {
-                if (!mbar_wait(p_full, i & 1, p.status, kSiteAttn)) break;
-                tc_fence_after();
-                const uint64_t do_mn = mndesc_base(s_do + (i % ND) * kTile);
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_bf16_elected(leader, t_dp, kdesc_at(v_desc, kk), kdesc_at(do_desc, kk), idesc_s, kk > 0);
+            umma_bf16_elected(leader, t_dp, ones_d, aug_desc(s_aug + (i % NA) * L::kAugTile), idesc_s, 1u);
+            umma_commit_elected(leader, dp_full);
+            umma_commit_elected(leader, aug_empty(i % NA));
+            return true;
+        };
+        bool ok = warp_wait(kv_full, 0, p.status) && issue_s(0) && issue_dp(0);
+        for (int i = 0; ok && i < n_steps; ++i) {
+            if (!warp_wait(p_full, i & 1, p.status)) break;
+            tc_fence_after();
+            const uint64_t do_mn = mndesc_base(s_do + (i % ND) * kTile);
 #pragma unroll
-                for (int kk = 0; kk < kRows / 16; ++kk)
-                    umma_bf16_ts(t_dv, t_s + packed_col(kk), mndesc_at(do_mn, kk), idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(do_empty(i % ND));
-                // S^T[i+1] overwrites the S^T buffer after dV[i] has read P^T[i] from it
-                if (i + 1 < n_steps && !issue_s(i + 1)) break;
-                if (!mbar_wait(ds_full, i & 1, p.status, kSiteAttn)) break;
-                tc_fence_after();
-                const uint64_t q_mn = mndesc_base(s_q + (i % NQ) * kTile);
+            for (int kk = 0; kk < kRows / 16; ++kk)
+                umma_bf16_ts_elected(leader, t_dv, t_s + packed_col(kk), mndesc_at(do_mn, kk), idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+            umma_commit_elected(leader, do_empty(i % ND));
+            // S^T[i+1] overwrites the S^T buffer after dV[i] has read P^T[i] from it
+            if (i + 1 < n_steps && !issue_s(i + 1)) break;
+            if (!warp_wait(ds_full, i & 1, p.status)) break;
+            tc_fence_after();
+            const uint64_t q_mn = mndesc_base(s_q + (i % NQ) * kTile);
 #pragma unroll
-                for (int kk = 0; kk < kRows / 16; ++kk)
-                    umma_bf16_ts(t_dk, t_dp + packed_col(kk), mndesc_at(q_mn, kk), idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(q_empty(i % NQ));
-                if (i + 1 < n_steps && !issue_dp(i + 1)) break;
+            for (int kk = 0; kk < kRows / 16; ++kk)
+                umma_bf16_ts_elected(leader, t_dk, t_dp + packed_col(kk), mndesc_at(q_mn, kk), idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+            umma_commit_elected(leader, q_empty(i % NQ));
+            if (i + 1 < n_steps && !issue_dp(i + 1)) break;
+        }
+        umma_commit_elected(leader, done);
+        umma_commit_elected(leader, drain);
+        mbar_wait(drain, 0, p.status, kSiteDrain);
+    } else if (warp == kStatWarp) {
+        // ---------------- statistics warp: step i's lse and D into B operand i % NA
+        const float inv_c = 1.f / p.scale_log2;
+        for (int i = 0; i < n_steps; ++i) {
+            if (!warp_wait(st_full(i % NT), (i / NT) & 1, p.status) ||
+                !warp_wait(aug_empty(i % NA), ((i / NA) & 1) ^ 1u, p.status))
+                break;
+            const float* stat = reinterpret_cast<const float*>(smem_raw + L::kStat + 1024u * (i % NT));
+            uint8_t* aug = smem_raw + L::kAug + (i % NA) * L::kAugTile;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = lane + 32 * u;
+                // statistics past the sequence end are never written: whatever they
+                // hold only reaches masked columns
+                *reinterpret_cast<uint2*>(aug + aug_offset(r, 0)) = split3_bf16(-stat[r] * inv_c);
+                *reinterpret_cast<uint2*>(aug + aug_offset(r, 1)) = split3_bf16(-stat[128 + r]);
             }
-            umma_commit(done);
-            umma_commit(drain);
-            mbar_wait(drain, 0, p.status, kSiteDrain);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(aug_full(i % NA));
+                mbar_arrive(st_empty(i % NT));
+            }
         }
     } else {
         // ---------------- two groups of four warps, one key row per thread in each:
@@ -837,37 +936,27 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             // query column c is visible to this key when first <= c <= last
             const int first = k - qc0;
             const int last = s1 - 1 - qc0;
-            // lse of this group's 64 queries, then (512 bytes on) their dvec; plain
-            // shared-memory reads the compiler may schedule freely (they stay after
-            // the barrier wait above, which clobbers memory)
-            const float4* stat_p =
-                reinterpret_cast<const float4*>(smem_raw + (s_stat - base) + 1024u * (i % NT) + 256u * gi);
-            if (!warp_wait(st_full(i % NT), (i / NT) & 1, p.status) || !warp_wait(s_full, i & 1, p.status)) {
+            if (!warp_wait(s_full, i & 1, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             float pr[64];
+            uint32_t rs[64];
+            tmem_load_32(t_s + t_row, *reinterpret_cast<uint32_t(*)[32]>(rs));
+            tmem_load_32(t_s + t_row + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+            tmem_wait_load();
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t rs[32];
-                tmem_load_32(t_s + t_row + 32 * c, rs);
-                tmem_wait_load();
                 // below the diagonal and inside the sequence every column is visible;
-                // statistics past the sequence end are never written, and masked
-                // elements are selected away, never used
+                // masked elements (which may carry statistics past the sequence end)
+                // are selected away, never used
                 const bool all_vis = __all_sync(0xffffffffu, first <= 32 * c && last >= 32 * c + 31);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 l4 = stat_p[8 * c + j];
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        pr[32 * c + 4 * j + u] = ex2(fmaf(__uint_as_float(rs[4 * j + u]), p.scale_log2, -lv[u]));
-                }
+                for (int j = 0; j < 32; ++j) pr[32 * c + j] = ex2(__uint_as_float(rs[32 * c + j]) * p.scale_log2);
                 if (!all_vis) {  // one warp-uniform branch per chunk, bit masks inside
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) pr[32 * c + i] = keep_if(pr[32 * c + i], (32 * c + i >= first) & (32 * c + i <= last));
+                    for (int j = 0; j < 32; ++j) pr[32 * c + j] = keep_if(pr[32 * c + j], (32 * c + j >= first) & (32 * c + j <= last));
                 }
                 uint32_t w[16];
 #pragma unroll
@@ -877,30 +966,25 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             }
             tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(p_full);
+            warp_arrive(p_full, lane);
             if (!warp_wait(dp_full, i & 1, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            uint32_t rp[64];
+            tmem_load_32(t_dp + t_row, *reinterpret_cast<uint32_t(*)[32]>(rp));
+            tmem_load_32(t_dp + t_row + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+            tmem_wait_load();
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                uint32_t rp[32];
-                tmem_load_32(t_dp + t_row + 32 * c, rp);
-                tmem_wait_load();
                 const bool all_vis = __all_sync(0xffffffffu, first <= 32 * c && last >= 32 * c + 31);
                 float ds[32];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 d4 = stat_p[32 + 8 * c + j];
-                    const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        ds[4 * j + u] = pr[32 * c + 4 * j + u] * (__uint_as_float(rp[4 * j + u]) - dvv[u]);
-                }
+                for (int j = 0; j < 32; ++j) ds[j] = pr[32 * c + j] * __uint_as_float(rp[32 * c + j]);
                 if (!all_vis) {  // masked columns may hold statistics past the sequence end
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ds[i] = keep_if(ds[i], (32 * c + i >= first) & (32 * c + i <= last));
+                    for (int j = 0; j < 32; ++j) ds[j] = keep_if(ds[j], (32 * c + j >= first) & (32 * c + j <= last));
                 }
                 uint32_t w[16];
 #pragma unroll
@@ -909,8 +993,7 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             }
             tmem_wait_store();
             tc_fence_before();
-            mbar_arrive(ds_full);
-            mbar_arrive(st_empty(i % NT));
+            warp_arrive(ds_full, lane);
         }
         // group 0 stores dK, group 1 dV
         if (ok && warp_wait(done, 0, p.status)) {
@@ -1050,6 +1133,43 @@ cudaError_t fwd_launch(const AttnShape& s, const void* qkv, void* a, float* lse,
     return cudaGetLastError();
 }
 
+// A second stream per device for the dQ kernel.  dQ and dK/dV read the same
+// inputs and write disjoint columns of dqkv, so they run side by side: the dK/dV
+// kernel's CTAs carry up to 32 times different work (the first key block of
+// each kv head sees every query block), and on one stream the SMs that finish
+// early sat idle until its longest CTAs were done.  The caller's stream forks
+// to the side stream after the row kernel and joins it after both launches; a
+// mutex keeps concurrent callers from interleaving the fork and join events.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;
+};
+
+SideStream* side_stream() {
+    static SideStream sides[64];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    SideStream& s = sides[dev];
+    if (!s.stream) {
+        cudaStream_t st = nullptr;
+        cudaEvent_t f = nullptr, j = nullptr;
+        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+            if (f) cudaEventDestroy(f);
+            cudaStreamDestroy(st);
+            return nullptr;
+        }
+        s.stream = st;
+        s.fork = f;
+        s.join = j;
+    }
+    return &s;
+}
+
 template <int D>
 cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const void* da, const float* lse,
                        float* dvec, void* dqkv, cudaStream_t stream) {
@@ -1076,11 +1196,20 @@ cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const
         static_cast<const uint16_t*>(da), static_cast<const uint16_t*>(a), dvec, s.tokens, s.n_heads, D, s.ld_stat);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attn_causal_dkdv_kernel<D><<<p.n_blocks * s.n_kv_heads, kAttnBwdThreads, DkvSmem<D>::kBytes, stream>>>(mq, md, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    attn_causal_dq_kernel<D><<<p.n_blocks * s.n_heads, kAttnBwdThreads, DqSmem<D>::kBytes, stream>>>(mq, md, p);
-    return cudaGetLastError();
+    SideStream* side = side_stream();
+    if (!side) return cudaErrorInitializationError;
+    std::lock_guard<std::mutex> lock(side->mu);
+    if ((e = cudaEventRecord(side->fork, stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess) return e;
+    attn_causal_dkdv_kernel<D><<<p.n_blocks * s.n_kv_heads, kAttnDkvThreads, DkvSmem<D>::kBytes, stream>>>(mq, md, p);
+    const cudaError_t e_kv = cudaGetLastError();
+    attn_causal_dq_kernel<D><<<p.n_blocks * s.n_heads, kAttnBwdThreads, DqSmem<D>::kBytes, side->stream>>>(mq, md, p);
+    const cudaError_t e_q = cudaGetLastError();
+    // the join is recorded whatever happened above, so the caller's stream never
+    // runs ahead of work already queued on the side stream
+    if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(stream, side->join, 0)) != cudaSuccess) return e;
+    return e_kv != cudaSuccess ? e_kv : e_q;
 }
 
 }  // namespace
