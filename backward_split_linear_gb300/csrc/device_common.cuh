@@ -442,6 +442,28 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask
         : "memory");
 }
 
+// The CTA-pair forms for a converged warp of cluster rank 0 (see elect_one_sync).
+__device__ __forceinline__ void umma_bf16_pair_elected(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
+                                                       uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair_elected(uint32_t leader, uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %2, 0;\n\t"
+        "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+            bar),
+        "h"(cta_mask), "r"(leader)
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
 // (taddr.lane + i), columns taddr.col .. taddr.col + 31.
 __device__ __forceinline__ void tmem_load_32(uint32_t taddr, uint32_t (&r)[32]) {

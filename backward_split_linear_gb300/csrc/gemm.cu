@@ -385,50 +385,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            constexpr uint32_t idesc = mma_idesc_bf16(BM, BN, A_MN, B_MN);
-            int stage = 0;
-            uint32_t phase = 0;
-            int it = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
-                const int acc = it & 1;
-                const uint32_t aph = (static_cast<uint32_t>(it) >> 1) & 1u;
-                if (!mbar_wait(tempty_bar(acc), aph ^ 1u, p.status, kSiteMmaTmemEmpty)) break;
-                tc_fence_after();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, p.status, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a0 = s_a + stage * kAStageBytes;
-                    const uint32_t b0 = s_b + stage * kBStageBytes;
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        // K-major: the 16-element K step is 32 bytes inside the
-                        // 128-byte swizzled row; MN-major: it is 16 rows of 128 B.
-                        const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, p.mn_lbo, p.mn_sbo)
-                                                 : smem_desc_sw128(a0 + k * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, p.mn_lbo, p.mn_sbo)
-                                                 : smem_desc_sw128(b0 + k * 32, 16, 1024);
-                        umma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-                    }
-                    umma_commit(empty_bar(stage));
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+        // ---------------- MMA issuer: the whole warp, its elected lane carries each instruction
+        const uint32_t issuer = elect_one_sync();
+        constexpr uint32_t idesc = mma_idesc_bf16(BM, BN, A_MN, B_MN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t aph = (static_cast<uint32_t>(it) >> 1) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(tempty_bar(acc), aph ^ 1u, p.status, kSiteMmaTmemEmpty))) break;
+            tc_fence_after();
+            const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, p.status, kSiteMmaFull))) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
-                umma_commit(tfull_bar(acc));
+                tc_fence_after();
+                const uint32_t a0 = s_a + stage * kAStageBytes;
+                const uint32_t b0 = s_b + stage * kBStageBytes;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    // K-major: the 16-element K step is 32 bytes inside the
+                    // 128-byte swizzled row; MN-major: it is 16 rows of 128 B.
+                    const uint64_t ad = A_MN ? smem_desc_sw128(a0 + k * 2048, p.mn_lbo, p.mn_sbo)
+                                             : smem_desc_sw128(a0 + k * 32, 16, 1024);
+                    const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, p.mn_lbo, p.mn_sbo)
+                                             : smem_desc_sw128(b0 + k * 32, 16, 1024);
+                    umma_bf16_elected(issuer, d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                }
+                umma_commit_elected(issuer, empty_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            // No MMA may still run when tensor memory is freed.
-            umma_commit(drain_bar);
-            mbar_wait(drain_bar, 0, p.status, kSiteDrain, kWaitLimitNs);
+            if (!ok) break;
+            umma_commit_elected(issuer, tfull_bar(acc));
         }
+        // No MMA may still run when tensor memory is freed.
+        umma_commit_elected(issuer, drain_bar);
+        mbar_wait(drain_bar, 0, p.status, kSiteDrain, kWaitLimitNs);
     } else {
         // ---------------- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31
         const int q = warp & 3;
@@ -668,8 +667,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         }
     } else if (usable && warp == 1) {
-        if (lane == 0 && leader) {
-            // ---------------- MMA issuer (rank 0 only)
+        if (leader) {
+            // ---------------- MMA issuer (rank 0 only): the whole warp, its elected
+            // lane carries each instruction
+            const uint32_t issuer = elect_one_sync();
             constexpr uint32_t idesc = mma_idesc_bf16(kPairM, kPairN, A_MN, B_MN);
             int stage = 0;
             uint32_t phase = 0;
@@ -681,11 +682,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const Unit w = unit_of<SPLIT>(p, u - G.unit_begin[pi]);
                 const int acc = it % NACC;
                 const uint32_t aph = static_cast<uint32_t>(it / NACC) & 1u;
-                if (!mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, status, kSiteMmaTmemEmpty)) break;
+                if (!__all_sync(0xffffffffu, mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, status, kSiteMmaTmemEmpty)))
+                    break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait_cluster(full_bar(stage), phase, status, kSiteMmaFull)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_cluster(full_bar(stage), phase, status, kSiteMmaFull))) {
                         ok = false;
                         break;
                     }
@@ -698,18 +700,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                  : smem_desc_sw128(a0 + k * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc_sw128(b0 + k * 2048, mn_lbo, mn_sbo)
                                                  : smem_desc_sw128(b0 + k * 32, 16, 1024);
-                        umma_bf16_pair(d, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
+                        umma_bf16_pair_elected(issuer, d, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
                     }
-                    umma_commit_pair(empty_bar(stage), 0x3);
+                    umma_commit_pair_elected(issuer, empty_bar(stage), 0x3);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(tfull_bar(acc), 0x3);
+                umma_commit_pair_elected(issuer, tfull_bar(acc), 0x3);
             }
-            umma_commit_pair(drain_bar, 0x1);
+            umma_commit_pair_elected(issuer, drain_bar, 0x1);
             mbar_wait(drain_bar, 0, status, kSiteDrain, kWaitLimitNs);
         }
     } else if (usable && warp >= 2) {
