@@ -117,7 +117,7 @@ __device__ __forceinline__ float lg2(float x) {
 // A wait taken by every lane of a warp, with one verdict for the warp (the
 // tensor-memory loads that follow are warp-wide).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* status) {
-    const bool ok = mbar_wait(bar, parity, status, kSiteAttn);
+    const bool ok = mbar_wait_fast(bar, parity, status, kSiteAttn);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -212,17 +212,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             uint32_t n_fills = 0;
             for (int j = 0; j < nk; ++j) {
                 const int st = j % NS;
-                if (!mbar_wait(kv_empty(st), ((j / NS) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                if (!mbar_wait_fast(kv_empty(st), ((j / NS) & 1) ^ 1u, p.status, kSiteAttn)) break;
                 mbar_arrive_expect_tx(kv_full(st), 2 * kTile);
                 const int k0 = (kb0 + j) * kRows;
                 load_tile<D>(s_kv + 2 * st * kTile, &map_qkv, kv_full(st), kcol, k0);
                 load_tile<D>(s_kv + (2 * st + 1) * kTile, &map_qkv, kv_full(st), vcol, k0);
                 ++n_fills;
             }
-            mbar_wait(q_full, 0, p.status, kSiteDrain);
+            mbar_wait_fast(q_full, 0, p.status, kSiteDrain);
             for (int s = 0; s < NS; ++s) {
                 const uint32_t u = ring_uses(n_fills, NS, s);
-                if (u > 0) mbar_wait(kv_full(s), (u - 1) & 1, p.status, kSiteDrain);
+                if (u > 0) mbar_wait_fast(kv_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
         }
     } else if (warp == 1) {
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
         }
         umma_commit_elected(leader, drain);
-        mbar_wait(drain, 0, p.status, kSiteDrain);
+        mbar_wait_fast(drain, 0, p.status, kSiteDrain);
     } else {
         // ---------------- softmax rows
         const int qw = warp & 3;
@@ -491,23 +491,23 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             uint32_t nkf = 0, nvf = 0;
             for (int j = 0; j < nk; ++j) {
                 const int k0 = (kb0 + j) * kRows;
-                if (!mbar_wait(k_empty(j % NK), ((j / NK) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                if (!mbar_wait_fast(k_empty(j % NK), ((j / NK) & 1) ^ 1u, p.status, kSiteAttn)) break;
                 mbar_arrive_expect_tx(k_full(j % NK), kTile);
                 load_tile<D>(s_k + (j % NK) * kTile, &map_qkv, k_full(j % NK), kcol, k0);
                 ++nkf;
-                if (!mbar_wait(v_empty(j % NV), ((j / NV) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                if (!mbar_wait_fast(v_empty(j % NV), ((j / NV) & 1) ^ 1u, p.status, kSiteAttn)) break;
                 mbar_arrive_expect_tx(v_full(j % NV), kTile);
                 load_tile<D>(s_v + (j % NV) * kTile, &map_qkv, v_full(j % NV), vcol, k0);
                 ++nvf;
             }
-            mbar_wait(q_full, 0, p.status, kSiteDrain);
+            mbar_wait_fast(q_full, 0, p.status, kSiteDrain);
             for (int s = 0; s < NK; ++s) {
                 const uint32_t u = ring_uses(nkf, NK, s);
-                if (u > 0) mbar_wait(k_full(s), (u - 1) & 1, p.status, kSiteDrain);
+                if (u > 0) mbar_wait_fast(k_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
             for (int s = 0; s < NV; ++s) {
                 const uint32_t u = ring_uses(nvf, NV, s);
-                if (u > 0) mbar_wait(v_full(s), (u - 1) & 1, p.status, kSiteDrain);
+                if (u > 0) mbar_wait_fast(v_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
         }
     } else if (warp == 1) {
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
         }
         umma_commit_elected(leader, done);
         umma_commit_elected(leader, drain);
-        mbar_wait(drain, 0, p.status, kSiteDrain);
+        mbar_wait_fast(drain, 0, p.status, kSiteDrain);
     } else {
         // ---------------- two groups of four warps, one query row per thread in each:
         // group gi takes key columns 64 gi .. 64 gi + 63 of every step
@@ -681,7 +681,7 @@ struct DkvSmem {
     static constexpr uint32_t kAug = kOnes + 2 * kAugTile;      // stage s: the B operand of step s
     static constexpr uint32_t kStat = kAug + kAugStages * kAugTile;  // stage s: lse (512 bytes) then D (512 bytes)
     static constexpr uint32_t kBars = kStat + 1024 * kStatStages;
-    static constexpr int kNumBars = 1 + 2 * (kQStages + kDoStages + kStatStages + kAugStages) + 6;
+    static constexpr int kNumBars = 1 + 2 * (kQStages + kDoStages + kStatStages) + kAugStages + 8;
     static constexpr size_t kBytes = kBars + 8 * kNumBars + 16;
 };
 constexpr int kAttnDkvThreads = kAttnBwdThreads + 32;  // + the statistics warp
@@ -733,11 +733,13 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
     auto do_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + s); };
     auto st_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + s); };
     auto st_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + NT + s); };
-    auto aug_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + 2 * NT + s); };
-    auto aug_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + 2 * NT + NA + s); };
-    constexpr int kB = 1 + 2 * (NQ + ND + NT + NA);
-    const uint32_t s_full = bars + 8u * kB, dp_full = bars + 8u * (kB + 1), p_full = bars + 8u * (kB + 2),
-                   ds_full = bars + 8u * (kB + 3), done = bars + 8u * (kB + 4), drain = bars + 8u * (kB + 5);
+    auto aug_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + 2 * NT + s); };
+    constexpr int kB = 1 + 2 * (NQ + ND + NT) + NA;
+    // p_full(c) / ds_full(c): chunk c (32 query columns of each group) of P^T / dS^T is packed
+    auto p_full = [&](int c) { return bars + 8u * (kB + 2 + c); };
+    auto ds_full = [&](int c) { return bars + 8u * (kB + 4 + c); };
+    const uint32_t s_full = bars + 8u * kB, dp_full = bars + 8u * (kB + 1), done = bars + 8u * (kB + 6),
+                   drain = bars + 8u * (kB + 7);
     const uint32_t tmem_slot = bars + 8u * L::kNumBars;
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - base));
 
@@ -769,7 +771,7 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         for (int s = 0; s < NQ; ++s) {
-            mbar_init(q_full(s), 1);
+            mbar_init(q_full(s), 2);  // the Q tile's TMA and the statistics warp's B operand
             mbar_init(q_empty(s), 1);
         }
         for (int s = 0; s < ND; ++s) {
@@ -780,14 +782,13 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
             mbar_init(st_full(s), 1);
             mbar_init(st_empty(s), 1);
         }
-        for (int s = 0; s < NA; ++s) {
-            mbar_init(aug_full(s), 1);
-            mbar_init(aug_empty(s), 1);
-        }
+        for (int s = 0; s < NA; ++s) mbar_init(aug_empty(s), 1);
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
-        mbar_init(p_full, 8);
-        mbar_init(ds_full, 8);
+        for (int c = 0; c < 2; ++c) {
+            mbar_init(p_full(c), 8);
+            mbar_init(ds_full(c), 8);
+        }
         mbar_init(done, 1);
         mbar_init(drain, 1);
         mbar_fence_init();
@@ -813,33 +814,33 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
                 const int qb = kb + i / group;
                 const int h = g * group + i % group;
                 const int r0 = qb * kRows;
-                if (!mbar_wait(st_empty(i % NT), ((i / NT) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                if (!mbar_wait_fast(st_empty(i % NT), ((i / NT) & 1) ^ 1u, p.status, kSiteAttn)) break;
                 const uint32_t stat = s_stat + 1024u * (i % NT);
                 mbar_arrive_expect_tx(st_full(i % NT), 1024);
                 bulk_load_1d(stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
                 bulk_load_1d(stat + 512, p.dvec + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
                 ++nt;
-                if (!mbar_wait(q_empty(i % NQ), ((i / NQ) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                if (!mbar_wait_fast(q_empty(i % NQ), ((i / NQ) & 1) ^ 1u, p.status, kSiteAttn)) break;
                 mbar_arrive_expect_tx(q_full(i % NQ), kTile);
                 load_tile<D>(s_q + (i % NQ) * kTile, &map_qkv, q_full(i % NQ), h * D, r0);
                 ++nq;
-                if (!mbar_wait(do_empty(i % ND), ((i / ND) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                if (!mbar_wait_fast(do_empty(i % ND), ((i / ND) & 1) ^ 1u, p.status, kSiteAttn)) break;
                 mbar_arrive_expect_tx(do_full(i % ND), kTile);
                 load_tile<D>(s_do + (i % ND) * kTile, &map_do, do_full(i % ND), h * D, r0);
                 ++nd;
             }
-            mbar_wait(kv_full, 0, p.status, kSiteDrain);
+            mbar_wait_fast(kv_full, 0, p.status, kSiteDrain);
             for (int s = 0; s < NQ; ++s) {
                 const uint32_t u = ring_uses(nq, NQ, s);
-                if (u > 0) mbar_wait(q_full(s), (u - 1) & 1, p.status, kSiteDrain);
+                if (u > 0) mbar_wait_fast(q_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
             for (int s = 0; s < ND; ++s) {
                 const uint32_t u = ring_uses(nd, ND, s);
-                if (u > 0) mbar_wait(do_full(s), (u - 1) & 1, p.status, kSiteDrain);
+                if (u > 0) mbar_wait_fast(do_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
             for (int s = 0; s < NT; ++s) {
                 const uint32_t u = ring_uses(nt, NT, s);
-                if (u > 0) mbar_wait(st_full(s), (u - 1) & 1, p.status, kSiteDrain);
+                if (u > 0) mbar_wait_fast(st_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
         }
     } else if (warp == 1) {
@@ -851,8 +852,8 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
         const uint64_t ones_lse = aug_desc(s_ones), ones_d = aug_desc(s_ones + L::kAugTile);
         auto issue_s = [&](int i) {
             const int st = i % NQ;
+            // Q tile i and statistics operand i % NA (NA = NQ) complete one phase together
             if (!warp_wait(q_full(st), (i / NQ) & 1, p.status)) return false;
-            if (!warp_wait(aug_full(i % NA), (i / NA) & 1, p.status)) return false;
             tc_fence_after();
             const uint64_t q_desc = kdesc_base(s_q + st * kTile);
 #pragma unroll
@@ -876,28 +877,51 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
             return true;
         };
         bool ok = warp_wait(kv_full, 0, p.status) && issue_s(0) && issue_dp(0);
+        // K steps of dV / dK in the order their P^T / dS^T chunks are packed:
+        // chunk c of group g holds the K steps 4 g + 2 c and 4 g + 2 c + 1
+        constexpr int kOrder[8] = {0, 1, 4, 5, 2, 3, 6, 7};
         for (int i = 0; ok && i < n_steps; ++i) {
-            if (!warp_wait(p_full, i & 1, p.status)) break;
-            tc_fence_after();
             const uint64_t do_mn = mndesc_base(s_do + (i % ND) * kTile);
 #pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk)
-                umma_bf16_ts_elected(leader, t_dv, t_s + packed_col(kk), mndesc_at(do_mn, kk), idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+            for (int c = 0; c < 2; ++c) {
+                if (!warp_wait(p_full(c), i & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int kk = kOrder[4 * c + e];
+                    umma_bf16_ts_elected(leader, t_dv, t_s + packed_col(kk), mndesc_at(do_mn, kk), idesc_g,
+                                         (i > 0 || kk > 0) ? 1u : 0u);
+                }
+            }
+            if (!ok) break;
             umma_commit_elected(leader, do_empty(i % ND));
             // S^T[i+1] overwrites the S^T buffer after dV[i] has read P^T[i] from it
             if (i + 1 < n_steps && !issue_s(i + 1)) break;
-            if (!warp_wait(ds_full, i & 1, p.status)) break;
-            tc_fence_after();
             const uint64_t q_mn = mndesc_base(s_q + (i % NQ) * kTile);
 #pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk)
-                umma_bf16_ts_elected(leader, t_dk, t_dp + packed_col(kk), mndesc_at(q_mn, kk), idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+            for (int c = 0; c < 2; ++c) {
+                if (!warp_wait(ds_full(c), i & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int kk = kOrder[4 * c + e];
+                    umma_bf16_ts_elected(leader, t_dk, t_dp + packed_col(kk), mndesc_at(q_mn, kk), idesc_g,
+                                         (i > 0 || kk > 0) ? 1u : 0u);
+                }
+            }
+            if (!ok) break;
             umma_commit_elected(leader, q_empty(i % NQ));
             if (i + 1 < n_steps && !issue_dp(i + 1)) break;
         }
         umma_commit_elected(leader, done);
         umma_commit_elected(leader, drain);
-        mbar_wait(drain, 0, p.status, kSiteDrain);
+        mbar_wait_fast(drain, 0, p.status, kSiteDrain);
     } else if (warp == kStatWarp) {
         // ---------------- statistics warp: step i's lse and D into B operand i % NA
         const float inv_c = 1.f / p.scale_log2;
@@ -918,7 +942,7 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(aug_full(i % NA));
+                mbar_arrive(q_full(i % NQ));
                 mbar_arrive(st_empty(i % NT));
             }
         }
@@ -963,10 +987,10 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
                 for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(pr[32 * c + 2 * e], pr[32 * c + 2 * e + 1]);
                 // packed columns 16 c .. 16 c + 15 of the group's columns, all read above
                 tmem_store_16(t_s + t_row + 16 * c, w);
+                tmem_wait_store();
+                tc_fence_before();
+                warp_arrive(p_full(c), lane);
             }
-            tmem_wait_store();
-            tc_fence_before();
-            warp_arrive(p_full, lane);
             if (!warp_wait(dp_full, i & 1, p.status)) {
                 ok = false;
                 break;
@@ -990,10 +1014,10 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
                 tmem_store_16(t_dp + t_row + 16 * c, w);
+                tmem_wait_store();
+                tc_fence_before();
+                warp_arrive(ds_full(c), lane);
             }
-            tmem_wait_store();
-            tc_fence_before();
-            warp_arrive(ds_full, lane);
         }
         // group 0 stores dK, group 1 dV
         if (ok && warp_wait(done, 0, p.status)) {

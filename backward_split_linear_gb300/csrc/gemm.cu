@@ -395,11 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
             const uint32_t aph = (static_cast<uint32_t>(it) >> 1) & 1u;
-            if (!__all_sync(0xffffffffu, mbar_wait(tempty_bar(acc), aph ^ 1u, p.status, kSiteMmaTmemEmpty))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait_fast(tempty_bar(acc), aph ^ 1u, p.status, kSiteMmaTmemEmpty))) break;
             tc_fence_after();
             const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
             for (int kb = 0; kb < p.k_blocks; ++kb) {
-                if (!__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, p.status, kSiteMmaFull))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_fast(full_bar(stage), phase, p.status, kSiteMmaFull))) {
                     ok = false;
                     break;
                 }
@@ -682,12 +682,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const Unit w = unit_of<SPLIT>(p, u - G.unit_begin[pi]);
                 const int acc = it % NACC;
                 const uint32_t aph = static_cast<uint32_t>(it / NACC) & 1u;
-                if (!__all_sync(0xffffffffu, mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, status, kSiteMmaTmemEmpty)))
+                if (!__all_sync(0xffffffffu, mbar_wait_cluster_fast(tempty_bar(acc), aph ^ 1u, status, kSiteMmaTmemEmpty)))
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kPairN);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!__all_sync(0xffffffffu, mbar_wait_cluster(full_bar(stage), phase, status, kSiteMmaFull))) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_cluster_fast(full_bar(stage), phase, status, kSiteMmaFull))) {
                         ok = false;
                         break;
                     }
