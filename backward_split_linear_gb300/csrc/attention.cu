@@ -9,10 +9,13 @@
 //
 // Three kernels, each one CTA per 128-row tile:
 //   warp 0     one thread issues TMA loads
-//   warp 1     allocates tensor memory; one thread issues tcgen05.mma
+//   warp 1     allocates tensor memory; the whole warp runs the MMA issue loop
+//              and its elected lane carries each tcgen05.mma and commit
 //   warps 2-5  one row each: softmax / gradient arithmetic, epilogue
-//   warps 6-9  (backward kernels) a second group of row warps, on every other
-//              64-wide sub-block
+//   warps 6-9  (backward kernels) a second group of row warps, on the other
+//              64 columns of every 128-wide step
+//   warp 10    (dK/dV) the statistics warp: lse and D of each step's queries
+//              into the B operand of the score products' extra K step
 //
 //   attn_causal_fwd_kernel   (head h, query block):  S = Q K^T -> online softmax ->
 //                     O += P V over the key blocks up to the diagonal; writes
@@ -25,7 +28,8 @@
 //                     above, dQ += dS K over the key blocks up to the diagonal.
 // dQ has its own kernel (it recomputes S and dP) so that no two CTAs add into
 // the same output: results are the same bits on every run.  D = rowsum(dO * O)
-// comes from a small row kernel first.
+// comes from a small row kernel first; then dK/dV (on the caller's stream) and
+// dQ (on a side stream forked from it and joined back) run side by side.
 //
 // Tiles are 128 rows x d columns of bf16 in 128-byte-swizzled layout: d / 64
 // blocks of 128 rows x 128 bytes (16 KiB each), as TMA writes them.  A tile
