@@ -415,7 +415,7 @@ struct DqSmem {
     static constexpr uint32_t kQ = 0, kDO = kTile, kK = 2 * kTile;
     static constexpr uint32_t kV = kK + kKStages * kTile;
     static constexpr uint32_t kBars = kV + kVStages * kTile;
-    static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 4;
+    static constexpr int kNumBars = 1 + 2 * kKStages + kVStages + 2 + 4;
     static constexpr size_t kBytes = kBars + 8 * kNumBars + 16;
 };
 
@@ -437,9 +437,8 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     const uint32_t q_full = bars;
     auto k_full = [&](int s) { return bars + 8u * (1 + s); };
     auto k_empty = [&](int s) { return bars + 8u * (1 + NK + s); };
-    auto v_full = [&](int s) { return bars + 8u * (1 + 2 * NK + s); };
-    auto v_empty = [&](int s) { return bars + 8u * (1 + 2 * NK + NV + s); };
-    constexpr int kB = 1 + 2 * NK + 2 * NV;
+    auto v_empty = [&](int s) { return bars + 8u * (1 + 2 * NK + s); };
+    constexpr int kB = 1 + 2 * NK + NV;
     auto s_full = [&](int b) { return bars + 8u * (kB + b); };
     const uint32_t dp_full = bars + 8u * (kB + 2), ds_full = bars + 8u * (kB + 3), done = bars + 8u * (kB + 4),
                    drain = bars + 8u * (kB + 5);
@@ -464,7 +463,6 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             mbar_init(k_empty(s), 1);
         }
         for (int s = 0; s < NV; ++s) {
-            mbar_init(v_full(s), 1);
             mbar_init(v_empty(s), 1);
         }
         mbar_init(s_full(0), 1);
@@ -492,26 +490,21 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             mbar_arrive_expect_tx(q_full, 2 * kTile);
             load_tile<D>(s_q, &map_qkv, q_full, h * D, q0);
             load_tile<D>(s_do, &map_do, q_full, h * D, q0);
-            uint32_t nkf = 0, nvf = 0;
+            uint32_t nkf = 0;
             for (int j = 0; j < nk; ++j) {
                 const int k0 = (kb0 + j) * kRows;
+                // K[j] and V[j] land on one barrier: one wait per step for the MMA warp
                 if (!mbar_wait_fast(k_empty(j % NK), ((j / NK) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(k_full(j % NK), kTile);
-                load_tile<D>(s_k + (j % NK) * kTile, &map_qkv, k_full(j % NK), kcol, k0);
-                ++nkf;
                 if (!mbar_wait_fast(v_empty(j % NV), ((j / NV) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(v_full(j % NV), kTile);
-                load_tile<D>(s_v + (j % NV) * kTile, &map_qkv, v_full(j % NV), vcol, k0);
-                ++nvf;
+                mbar_arrive_expect_tx(k_full(j % NK), 2 * kTile);
+                load_tile<D>(s_k + (j % NK) * kTile, &map_qkv, k_full(j % NK), kcol, k0);
+                load_tile<D>(s_v + (j % NV) * kTile, &map_qkv, k_full(j % NK), vcol, k0);
+                ++nkf;
             }
             mbar_wait_fast(q_full, 0, p.status, kSiteDrain);
             for (int s = 0; s < NK; ++s) {
                 const uint32_t u = ring_uses(nkf, NK, s);
                 if (u > 0) mbar_wait_fast(k_full(s), (u - 1) & 1, p.status, kSiteDrain);
-            }
-            for (int s = 0; s < NV; ++s) {
-                const uint32_t u = ring_uses(nvf, NV, s);
-                if (u > 0) mbar_wait_fast(v_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
         }
     } else if (warp == 1) {
@@ -532,9 +525,7 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             return true;
         };
         auto issue_dp = [&](int j) {
-            const int st = j % NV;
-            if (!warp_wait(v_full(st), (j / NV) & 1, p.status)) return false;
-            tc_fence_after();
+            const int st = j % NV;  // V[j] landed with K[j] (issue_s(j) waited for both)
             const uint64_t v_desc = kdesc_base(s_v + st * kTile);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
@@ -685,7 +676,7 @@ struct DkvSmem {
     static constexpr uint32_t kAug = kOnes + 2 * kAugTile;      // stage s: the B operand of step s
     static constexpr uint32_t kStat = kAug + kAugStages * kAugTile;  // stage s: lse (512 bytes) then D (512 bytes)
     static constexpr uint32_t kBars = kStat + 1024 * kStatStages;
-    static constexpr int kNumBars = 1 + 2 * (kQStages + kDoStages + kStatStages) + kAugStages + 8;
+    static constexpr int kNumBars = 1 + 2 * (kQStages + kStatStages) + kDoStages + kAugStages + 8;
     static constexpr size_t kBytes = kBars + 8 * kNumBars + 16;
 };
 constexpr int kAttnDkvThreads = kAttnBwdThreads + 32;  // + the statistics warp
@@ -733,12 +724,11 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
     const uint32_t kv_full = bars;
     auto q_full = [&](int s) { return bars + 8u * (1 + s); };
     auto q_empty = [&](int s) { return bars + 8u * (1 + NQ + s); };
-    auto do_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + s); };
-    auto do_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + s); };
-    auto st_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + s); };
-    auto st_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + NT + s); };
-    auto aug_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * ND + 2 * NT + s); };
-    constexpr int kB = 1 + 2 * (NQ + ND + NT) + NA;
+    auto do_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + s); };
+    auto st_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + s); };
+    auto st_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + NT + s); };
+    auto aug_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + 2 * NT + s); };
+    constexpr int kB = 1 + 2 * (NQ + NT) + ND + NA;
     // p_full(c) / ds_full(c): chunk c (32 query columns of each group) of P^T / dS^T is packed
     auto p_full = [&](int c) { return bars + 8u * (kB + 2 + c); };
     auto ds_full = [&](int c) { return bars + 8u * (kB + 4 + c); };
@@ -775,13 +765,10 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         for (int s = 0; s < NQ; ++s) {
-            mbar_init(q_full(s), 2);  // the Q tile's TMA and the statistics warp's B operand
+            mbar_init(q_full(s), 2);  // the Q and dO tiles' TMA and the statistics warp's B operand
             mbar_init(q_empty(s), 1);
         }
-        for (int s = 0; s < ND; ++s) {
-            mbar_init(do_full(s), 1);
-            mbar_init(do_empty(s), 1);
-        }
+        for (int s = 0; s < ND; ++s) mbar_init(do_empty(s), 1);
         for (int s = 0; s < NT; ++s) {
             mbar_init(st_full(s), 1);
             mbar_init(st_empty(s), 1);
@@ -813,7 +800,7 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
             mbar_arrive_expect_tx(kv_full, 2 * kTile);
             load_tile<D>(s_k, &map_qkv, kv_full, kcol, k0);
             load_tile<D>(s_v, &map_qkv, kv_full, vcol, k0);
-            uint32_t nq = 0, nd = 0, nt = 0;
+            uint32_t nq = 0, nt = 0;
             for (int i = 0; i < n_steps; ++i) {
                 const int qb = kb + i / group;
                 const int h = g * group + i % group;
@@ -824,23 +811,19 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
                 bulk_load_1d(stat, p.lse + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
                 bulk_load_1d(stat + 512, p.dvec + static_cast<int64_t>(h) * p.ld_stat + r0, 512, st_full(i % NT));
                 ++nt;
+                // Q[i] and dO[i] land on one barrier (with the statistics operand):
+                // one wait per step for the MMA warp
                 if (!mbar_wait_fast(q_empty(i % NQ), ((i / NQ) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(q_full(i % NQ), kTile);
-                load_tile<D>(s_q + (i % NQ) * kTile, &map_qkv, q_full(i % NQ), h * D, r0);
-                ++nq;
                 if (!mbar_wait_fast(do_empty(i % ND), ((i / ND) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(do_full(i % ND), kTile);
-                load_tile<D>(s_do + (i % ND) * kTile, &map_do, do_full(i % ND), h * D, r0);
-                ++nd;
+                mbar_arrive_expect_tx(q_full(i % NQ), 2 * kTile);
+                load_tile<D>(s_q + (i % NQ) * kTile, &map_qkv, q_full(i % NQ), h * D, r0);
+                load_tile<D>(s_do + (i % ND) * kTile, &map_do, q_full(i % NQ), h * D, r0);
+                ++nq;
             }
             mbar_wait_fast(kv_full, 0, p.status, kSiteDrain);
             for (int s = 0; s < NQ; ++s) {
                 const uint32_t u = ring_uses(nq, NQ, s);
                 if (u > 0) mbar_wait_fast(q_full(s), (u - 1) & 1, p.status, kSiteDrain);
-            }
-            for (int s = 0; s < ND; ++s) {
-                const uint32_t u = ring_uses(nd, ND, s);
-                if (u > 0) mbar_wait_fast(do_full(s), (u - 1) & 1, p.status, kSiteDrain);
             }
             for (int s = 0; s < NT; ++s) {
                 const uint32_t u = ring_uses(nt, NT, s);
@@ -867,10 +850,8 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
             umma_commit_elected(leader, s_full);
             return true;
         };
-        auto issue_dp = [&](int i) {  // after issue_s(i), which waited for the statistics operand
+        auto issue_dp = [&](int i) {  // after issue_s(i), which waited for dO[i] and the statistics too
             const int st = i % ND;
-            if (!warp_wait(do_full(st), (i / ND) & 1, p.status)) return false;
-            tc_fence_after();
             const uint64_t do_desc = kdesc_base(s_do + st * kTile);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
