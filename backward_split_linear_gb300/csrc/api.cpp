@@ -929,6 +929,7 @@ extern "C" zb_status zb_stage_forward(zb_stage_t st, int32_t mb, const void* x, 
         }
     if (slot < 0) return ZB_ERR_STASH_FULL;
     ZB_TRY(device_ok());
+    if (st->cfg.attention == ZB_ATTN_CAUSAL && zbk::attention_prepare() != cudaSuccess) return ZB_ERR_CUDA;
     ZB_TRY(stage_forward_body(st, slot, x, tokens, y, as_stream(stream)));
     st->slot_used[slot] = 1;
     st->mbs[mb] = MbEntry{MbState::Forwarded, slot, tokens};

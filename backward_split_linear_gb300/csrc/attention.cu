@@ -1231,6 +1231,8 @@ cudaError_t launch_attention_causal_forward(const AttnShape& s, const void* qkv,
     return cudaErrorInvalidValue;
 }
 
+cudaError_t attention_prepare() { return side_stream() ? cudaSuccess : cudaErrorInitializationError; }
+
 cudaError_t launch_attention_causal_backward(const AttnShape& s, const void* qkv, const void* a, const void* da,
                                              const float* lse, float* dvec, void* dqkv, cudaStream_t stream) {
     if (s.tokens <= 0) return cudaSuccess;

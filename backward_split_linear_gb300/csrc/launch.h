@@ -109,9 +109,15 @@ struct AttnShape {
 };
 cudaError_t launch_attention_causal_forward(const AttnShape& s, const void* qkv, void* a, float* lse,
                                             cudaStream_t stream);
-// Writes all of dqkv (dq, dk, dv); dvec is scratch of the lse's shape.
+// Writes all of dqkv (dq, dk, dv); dvec is scratch of the lse's shape.  Runs the
+// dK/dV kernel on `stream` and the dQ kernel on a per-device side stream forked
+// from it and joined back.
 cudaError_t launch_attention_causal_backward(const AttnShape& s, const void* qkv, const void* a, const void* da,
                                              const float* lse, float* dvec, void* dqkv, cudaStream_t stream);
+// Creates the current device's side stream and events ahead of the first
+// backward (a stage calls it at its first forward, so that no stream or event
+// is created while the caller's stream may be capturing a graph).
+cudaError_t attention_prepare();
 
 // Device status word of the current device (see zb_device_status).
 int* status_word();

@@ -275,7 +275,14 @@ zb_status zb_op_attention_forward(const void* qkv, void* a, int32_t tokens,
  *    return ZB_ERR_SHAPE.
  *  - The backward writes every column of dqkv.  Each output element is
  *    written by one thread after a fixed-order sum, so results are bitwise
- *    reproducible. */
+ *    reproducible.
+ *  - Streams: the backward runs its dK/dV kernel on `stream` and its dQ
+ *    kernel on a library-owned stream of the current device, forked from
+ *    `stream` after the work already queued there and joined back before the
+ *    call returns; work queued on `stream` afterwards sees all of dqkv.  The
+ *    library creates that stream (and two events) at the first causal
+ *    backward on a device, or at a causal stage's first forward; it lives
+ *    until the process ends. */
 int32_t zb_op_attention_stat_stride(int32_t tokens);
 zb_status zb_op_attention_causal_forward(const void* qkv, void* a, float* lse, int32_t tokens,
                                          int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,

@@ -213,3 +213,37 @@ def test_causal_stage_8b_shaped():
             assert_close(st.grads[li][k].cpu().numpy(), ref, f"layer {li} d{k}", fro_tol=causal_stage_fro_tol(2),
                          max_tol=CAUSAL_MAX_TOL)
     st.close()
+
+
+def test_backward_orders_with_the_callers_stream():
+    """The backward forks dQ onto a side stream and joins it back: on a caller's stream, work
+    queued before the call (a copy that writes the inputs) must land before either kernel reads,
+    and work queued after it (a copy of dqkv) must see every column written.  Nothing is
+    synchronised in between; the result must equal the same call on synchronised inputs, bit
+    for bit."""
+    t, nh, nkv, d = 1024, 8, 2, 128
+    rng = np.random.default_rng(7)
+    qkvb, _ = draw_bf16(rng, (t, (nh + 2 * nkv) * d))
+    dab, _ = draw_bf16(rng, (t, nh * d))
+    qkv, a, lse = run_forward(qkvb, t, nh, nkv, d, 0)
+    torch.cuda.synchronize()
+    ref = run_backward(qkv, a, lse, dab, t, nh, nkv, d, 0)
+    torch.cuda.synchronize()
+
+    s = torch.cuda.Stream()
+    src_qkv, src_da = qkv.clone(), bf16_from_bits(dab)
+    qkv2 = torch.zeros_like(qkv)
+    da2 = torch.zeros_like(src_da)
+    dvec = torch.zeros_like(lse)
+    dqkv = torch.full_like(ref, float("nan"))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        # a slow producer: many small copies in front of the inputs' final copy
+        for _ in range(200):
+            qkv2.add_(0)
+        qkv2.copy_(src_qkv)
+        da2.copy_(src_da)
+        zb.zb_op_attention_causal_backward(qkv2, a, da2, lse, dvec, dqkv, t, nh, nkv, d, 0, stream=s)
+        out = dqkv.clone()
+    s.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

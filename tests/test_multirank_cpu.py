@@ -38,7 +38,7 @@ def _rank_main(rank, world, port, out):
 def test_max_over_ranks_two_gloo_ranks():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         for r in range(world):
@@ -92,7 +92,7 @@ def test_replicas_two_gloo_ranks_equal_single_process():
 
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank_replica, args=(world, port, out), nprocs=world, join=True)
         got = {r: out[r] for r in range(world)}
