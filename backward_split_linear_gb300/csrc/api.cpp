@@ -92,6 +92,34 @@ zb_status run_linear_forward(const void* x, const void* w, const void* residual,
     return cuda_status(zbk::launch_gemm(g, s));
 }
 
+// F of the gate|up linear with the SwiGLU forward in its epilogue: gu = x w_gu^T
+// ([g | u], bf16) and s = silu(g) u from the bf16 g and u.  The CTA-pair GEMM
+// only (t >= 256, ffn a multiple of 128); see swiglu_forward_fused below.
+zb_status run_linear_forward_swiglu(const void* x, const void* w_gu, void* gu, void* s_out, int t, int hidden,
+                                    int ffn, cudaStream_t s, const SplitWs* ws = nullptr) {
+    GemmArgs g{};
+    g.kind = GemmKind::Forward;
+    g.epi = Epilogue::SwigluFwd;
+    g.a = x;
+    g.lda = hidden;
+    g.b = w_gu;
+    g.ldb = hidden;
+    g.m = t;
+    g.n = 2 * ffn;
+    g.k = hidden;
+    g.out = gu;
+    g.ldo = 2 * static_cast<int64_t>(ffn);
+    g.out2 = s_out;
+    g.ldo2 = ffn;
+    g.ffn = ffn;
+    set_split(g, ws);
+    return cuda_status(zbk::launch_gemm(g, s));
+}
+
+// Whether the gate|up F runs fused with the SwiGLU forward (the CTA-pair GEMM
+// takes outputs of at least 256 rows; a tile holds 128 features of g and u).
+bool swiglu_forward_fused(int t, int ffn) { return t >= 256 && ffn % 128 == 0; }
+
 zb_status run_backward_input(const void* dy, const void* w, void* dx, int t, int in, int out,
                              int64_t ldo, cudaStream_t s, const SplitWs* ws = nullptr) {
     GemmArgs g{};
@@ -741,11 +769,23 @@ zb_status stage_forward_body(zb_stage* st, int slot, const void* x, int t, void*
             return cuda_status(zbk::launch_rmsnorm_forward(h, p.gamma2, c.eps, st->at(slot, L.n2),
                                                            st->at<float>(slot, L.r2), t, H, s));
         }));
-        ZB_TRY(traced(st, ZB_KCLASS_GEMM_FORWARD, 1, gemm_flops(T, 2.0 * F, H), fwd_bytes(T, 2.0 * F, H, false), s,
-                      [&] { return run_linear_forward(st->at(slot, L.n2), p.w_gu, nullptr, st->at(slot, L.gu), t, H, 2 * F, s, &ws); }));
-        ZB_TRY(traced(st, ZB_KCLASS_ROW_FORWARD, 1, 0.0, 6.0 * T * F, s, [&] {
-            return cuda_status(zbk::launch_swiglu_forward(st->at(slot, L.gu), st->at(slot, L.s), t, F, s));
-        }));
+        if (swiglu_forward_fused(t, F)) {
+            // one launch: the epilogue also writes s (2 T F bytes more than the plain GEMM)
+            ZB_TRY(traced(st, ZB_KCLASS_GEMM_FORWARD, 1, gemm_flops(T, 2.0 * F, H),
+                          fwd_bytes(T, 2.0 * F, H, false) + 2.0 * T * F, s, [&] {
+                              return run_linear_forward_swiglu(st->at(slot, L.n2), p.w_gu, st->at(slot, L.gu),
+                                                               st->at(slot, L.s), t, H, F, s, &ws);
+                          }));
+        } else {
+            ZB_TRY(traced(st, ZB_KCLASS_GEMM_FORWARD, 1, gemm_flops(T, 2.0 * F, H), fwd_bytes(T, 2.0 * F, H, false),
+                          s, [&] {
+                              return run_linear_forward(st->at(slot, L.n2), p.w_gu, nullptr, st->at(slot, L.gu), t, H,
+                                                        2 * F, s, &ws);
+                          }));
+            ZB_TRY(traced(st, ZB_KCLASS_ROW_FORWARD, 1, 0.0, 6.0 * T * F, s, [&] {
+                return cuda_status(zbk::launch_swiglu_forward(st->at(slot, L.gu), st->at(slot, L.s), t, F, s));
+            }));
+        }
         ZB_TRY(traced(st, ZB_KCLASS_GEMM_FORWARD, 1, gemm_flops(T, H, F), fwd_bytes(T, H, F, true), s, [&] {
             return run_linear_forward(st->at(slot, L.s), p.w_down, h, yout, t, F, H, s, &ws);
         }));

@@ -595,6 +595,12 @@ __host__ __device__ constexpr uint32_t mma_idesc_bf16(int m, int n, bool a_mn, b
 
 // ---------------------------------------------------------------- bf16 packing
 
+// s = silu(g) u: the one expression of every SwiGLU forward in the library (the
+// row kernel and the gate|up GEMM epilogue give the same bits).
+__device__ __forceinline__ float swiglu_value(float g, float u) {
+    return g * __fdividef(1.0f, 1.0f + __expf(-g)) * u;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

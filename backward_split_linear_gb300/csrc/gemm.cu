@@ -532,10 +532,22 @@ template <int EPI>
 __host__ __device__ constexpr bool tma_out() {
     return EPI != static_cast<int>(Epilogue::SwigluBwd);
 }
-// Output staging (two boxes per epilogue warp, used in turn) or the side-input ring.
+// Output staging or the side-input ring.  Staging: two boxes per epilogue
+// warp, used in turn; the SwiGLU forward has one set of three (its g, u and s
+// boxes), so that the operand ring keeps all six stages (with two sets and five
+// stages its GEMM ran 2 % slower).
+template <int EPI>
+__host__ __device__ constexpr uint32_t pair_boxes_per_set() {
+    return EPI == static_cast<int>(Epilogue::SwigluFwd) ? 3 : 1;
+}
+template <int EPI>
+__host__ __device__ constexpr uint32_t pair_out_sets() {
+    return EPI == static_cast<int>(Epilogue::SwigluFwd) ? 1 : 2;
+}
 template <int EPI>
 __host__ __device__ constexpr uint32_t pair_out_bytes() {
-    return tma_out<EPI>() ? 4 * 2 * out_box_bytes<EPI>() : 4 * kSideSlots * kSideSlotBytes;
+    return tma_out<EPI>() ? 4 * pair_out_sets<EPI>() * pair_boxes_per_set<EPI>() * out_box_bytes<EPI>()
+                          : 4 * kSideSlots * kSideSlotBytes;
 }
 template <int EPI>
 __host__ __device__ constexpr size_t pair_smem_bytes() {
@@ -543,6 +555,31 @@ __host__ __device__ constexpr size_t pair_smem_bytes() {
 }
 static_assert(pair_smem_bytes<static_cast<int>(Epilogue::AccumF32)>() <= 232448, "shared memory");
 static_assert(pair_smem_bytes<static_cast<int>(Epilogue::SwigluBwd)>() <= 232448, "shared memory");
+static_assert(pair_smem_bytes<static_cast<int>(Epilogue::SwigluFwd)>() <= 232448, "shared memory");
+
+// SwiGLU forward of one 32-column chunk pair: g (rg) and u (ru) rounded to bf16
+// into their boxes, and s = silu(g) u from the rounded values into the third
+// (64-byte swizzle, as for every bf16 box).
+__device__ __forceinline__ void swiglu_fwd_chunk_to_smem(uint32_t set, int lane, const uint32_t (&rg)[32],
+                                                         const uint32_t (&ru)[32]) {
+    const uint32_t l = static_cast<uint32_t>(lane);
+    const uint32_t sw = (l >> 1) & 3u;
+    const uint32_t grow = set + l * 64u, urow = grow + kBf16BoxBytes, srow = grow + 2 * kBf16BoxBytes;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t gw[4], uw[4], sv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            gw[e] = pack_bf16x2(__uint_as_float(rg[8 * j + 2 * e]), __uint_as_float(rg[8 * j + 2 * e + 1]));
+            uw[e] = pack_bf16x2(__uint_as_float(ru[8 * j + 2 * e]), __uint_as_float(ru[8 * j + 2 * e + 1]));
+            sv[e] = pack_bf16x2(swiglu_value(bf16_lo(gw[e]), bf16_lo(uw[e])), swiglu_value(bf16_hi(gw[e]), bf16_hi(uw[e])));
+        }
+        const uint32_t off = (static_cast<uint32_t>(j) ^ sw) << 4;
+        st_shared_v4(grow + off, make_uint4(gw[0], gw[1], gw[2], gw[3]));
+        st_shared_v4(urow + off, make_uint4(uw[0], uw[1], uw[2], uw[3]));
+        st_shared_v4(srow + off, make_uint4(sv[0], sv[1], sv[2], sv[3]));
+    }
+}
 
 template <bool A_MN, bool B_MN, int EPI, int NACC, bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -621,7 +658,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 int tm, tn;
                 tile_coords(p, w.tile, tm, tn);
                 const int m0 = tm * kPairM + static_cast<int>(rank) * kHalf;
-                const int n0 = tn * kPairN + static_cast<int>(rank) * kHalf;
+                // SwiGLU forward: rank 0 takes 128 gate rows, rank 1 the same 128 up
+                // rows (ffn further on), so each CTA's accumulator holds g and u of
+                // the same features side by side
+                const int n0 = EPI == static_cast<int>(Epilogue::SwigluFwd)
+                                   ? tn * kHalf + (rank != 0 ? p.ffn : 0)
+                                   : tn * kPairN + static_cast<int>(rank) * kHalf;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, status, kSiteProducerEmpty)) {
                         ok = false;
@@ -720,7 +762,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         constexpr int kChunks = kPairN / 32;
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        const uint32_t out_stage = s_out + static_cast<uint32_t>(q) * 2u * kBoxBytes;
+        constexpr uint32_t kSetBytes = pair_boxes_per_set<EPI>() * kBoxBytes;
+        const uint32_t out_stage = s_out + static_cast<uint32_t>(q) * pair_out_sets<EPI>() * kSetBytes;
         uint32_t n_stored = 0;  // staged chunks this warp has handed to TMA stores
         // Side-input ring (SwiGLU backward): chunk k of this warp is column
         // chunk k % 8 of its (k / 8)-th work unit; lane 0 requests the g and u
@@ -799,103 +842,169 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 __syncwarp();  // the partial rows read below come after lane 0's acquire
             }
             const bool run_epi = row_ok && !store_partial && !give_up;
+            if constexpr (EPI == static_cast<int>(Epilogue::SwigluFwd)) {
+                // columns 0-127 of the accumulator are g, 128-255 u, of features
+                // tn * 128 ...: four rounds of one 32-column g chunk and its u chunk
 #pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-                const int n = n_base + c * 32;
-                const bool ok = run_epi && n < p.n;
-                uint4 x0[4];
-                if constexpr (EPI == static_cast<int>(Epilogue::AddResidual)) {
-                    if (ok) {
-                        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.aux) +
-                                                                          static_cast<int64_t>(m) * p.ld_aux + n);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) x0[j] = src[j];
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t rg[32], ru[32];
+                    tmem_load_32(tbase + static_cast<uint32_t>(c * 32), rg);
+                    tmem_load_32(tbase + static_cast<uint32_t>(kHalf + c * 32), ru);
+                    tmem_wait_load();
+                    if (c == 3) {
+                        tc_fence_before();
+                        if (leader)
+                            mbar_arrive(tempty_bar(acc));
+                        else
+                            mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
                     }
-                }
-                if constexpr (kSide) {
-                    const uint32_t sb = side_bar(k % kSideSlots);
-                    const uint32_t sph = static_cast<uint32_t>(k / kSideSlots) & 1u;
-                    if (!__all_sync(0xffffffffu, mbar_wait(sb, sph, status, kSiteEpiSideInput))) {
-                        alive = false;
-                        break;
-                    }
-                }
-                uint32_t r[32];
-                tmem_load_32(tbase + static_cast<uint32_t>(c * 32), r);
-                tmem_wait_load();
-                if (c == kChunks - 1) {
-                    tc_fence_before();
-                    if (leader)
-                        mbar_arrive(tempty_bar(acc));
-                    else
-                        mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
-                }
-                bool stored = false;
-                if (SPLIT && store_partial) {
-                    float4* dst = reinterpret_cast<float4*>(const_cast<float*>(prow) + c * 32);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                             __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                } else {
-                    if (SPLIT && w.split && ok) {
-                        const float4* src = reinterpret_cast<const float4*>(prow + c * 32);
+                    if (SPLIT && store_partial) {
+                        float4* dg = reinterpret_cast<float4*>(const_cast<float*>(prow) + c * 32);
+                        float4* du = reinterpret_cast<float4*>(const_cast<float*>(prow) + kHalf + c * 32);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            const float4 v = src[j];
-                            r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
-                            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
-                            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
-                            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                            dg[j] = make_float4(__uint_as_float(rg[4 * j]), __uint_as_float(rg[4 * j + 1]),
+                                                __uint_as_float(rg[4 * j + 2]), __uint_as_float(rg[4 * j + 3]));
+                            du[j] = make_float4(__uint_as_float(ru[4 * j]), __uint_as_float(ru[4 * j + 1]),
+                                                __uint_as_float(ru[4 * j + 2]), __uint_as_float(ru[4 * j + 3]));
+                        }
+                        continue;
+                    }
+                    if (SPLIT && w.split && run_epi) {
+                        const float4* sg = reinterpret_cast<const float4*>(prow + c * 32);
+                        const float4* su = reinterpret_cast<const float4*>(prow + kHalf + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 vg = sg[j], vu = su[j];
+                            rg[4 * j] = __float_as_uint(__uint_as_float(rg[4 * j]) + vg.x);
+                            rg[4 * j + 1] = __float_as_uint(__uint_as_float(rg[4 * j + 1]) + vg.y);
+                            rg[4 * j + 2] = __float_as_uint(__uint_as_float(rg[4 * j + 2]) + vg.z);
+                            rg[4 * j + 3] = __float_as_uint(__uint_as_float(rg[4 * j + 3]) + vg.w);
+                            ru[4 * j] = __float_as_uint(__uint_as_float(ru[4 * j]) + vu.x);
+                            ru[4 * j + 1] = __float_as_uint(__uint_as_float(ru[4 * j + 1]) + vu.y);
+                            ru[4 * j + 2] = __float_as_uint(__uint_as_float(ru[4 * j + 2]) + vu.z);
+                            ru[4 * j + 3] = __float_as_uint(__uint_as_float(ru[4 * j + 3]) + vu.w);
                         }
                     }
-                    // The box is stored when any of the warp's rows lies inside
-                    // M (the TMA drops rows >= M and columns >= N); the
-                    // decision is warp-uniform.
-                    stored = !give_up && row0 < p.m && n < p.n;
-                    if (stored) {
-                        if constexpr (kSide) {
-                            const uint32_t slot = ring + static_cast<uint32_t>(k % kSideSlots) * kSideSlotBytes;
-                            if (ok) swiglu_chunk_in_smem(slot, lane, r);
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                tma_store_2d(&G.xmap[2], slot, n, row0);
-                                tma_store_2d(&G.xmap[3], slot + kBf16BoxBytes, n, row0);
-                                bulk_commit_group();
-                            }
-                        } else {
-                            // a box is rewritten only after the store that read
-                            // it, two chunks back, has finished reading
-                            const uint32_t box = out_stage + (n_stored & 1u) * kBoxBytes;
-                            if (lane == 0) bulk_wait_group_read<1>();
-                            __syncwarp();
-                            if (ok) epilogue_chunk_to_smem<EPI>(box, lane, r, x0);
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                if constexpr (EPI == static_cast<int>(Epilogue::AccumF32))
-                                    tma_reduce_add_2d(&G.omap[pi], box, n, row0);
-                                else
-                                    tma_store_2d(&G.omap[pi], box, n, row0);
-                                bulk_commit_group();
-                            }
-                            ++n_stored;
+                    // the TMA drops rows >= M; every column is a feature below ffn
+                    if (!give_up && row0 < p.m) {
+                        // the set is rewritten only after the previous round's
+                        // stores have finished reading it
+                        const uint32_t set = out_stage;
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+                        if (run_epi) swiglu_fwd_chunk_to_smem(set, lane, rg, ru);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int col = tn * kHalf + c * 32;
+                            tma_store_2d(&G.omap[pi], set, col, row0);
+                            tma_store_2d(&G.omap[pi], set + kBf16BoxBytes, p.ffn + col, row0);
+                            tma_store_2d(&G.xmap[0], set + 2 * kBf16BoxBytes, col, row0);
+                            bulk_commit_group();
                         }
+                        ++n_stored;
                     }
                 }
-                if constexpr (kSide) {
-                    // Refill the slot chunk k - 1 used, once the stores that
-                    // read it are done (all but this chunk's own group).
-                    if (lane == 0 && issued < n_chunks) {
-                        if (stored)
-                            bulk_wait_group_read<1>();
-                        else
-                            bulk_wait_group_read<0>();
-                        issue_side(issued);
-                        ++issued;
+            } else {
+    #pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
+                    const int n = n_base + c * 32;
+                    const bool ok = run_epi && n < p.n;
+                    uint4 x0[4];
+                    if constexpr (EPI == static_cast<int>(Epilogue::AddResidual)) {
+                        if (ok) {
+                            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.aux) +
+                                                                              static_cast<int64_t>(m) * p.ld_aux + n);
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) x0[j] = src[j];
+                        }
                     }
-                    ++k;
+                    if constexpr (kSide) {
+                        const uint32_t sb = side_bar(k % kSideSlots);
+                        const uint32_t sph = static_cast<uint32_t>(k / kSideSlots) & 1u;
+                        if (!__all_sync(0xffffffffu, mbar_wait(sb, sph, status, kSiteEpiSideInput))) {
+                            alive = false;
+                            break;
+                        }
+                    }
+                    uint32_t r[32];
+                    tmem_load_32(tbase + static_cast<uint32_t>(c * 32), r);
+                    tmem_wait_load();
+                    if (c == kChunks - 1) {
+                        tc_fence_before();
+                        if (leader)
+                            mbar_arrive(tempty_bar(acc));
+                        else
+                            mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+                    }
+                    bool stored = false;
+                    if (SPLIT && store_partial) {
+                        float4* dst = reinterpret_cast<float4*>(const_cast<float*>(prow) + c * 32);
+    #pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    } else {
+                        if (SPLIT && w.split && ok) {
+                            const float4* src = reinterpret_cast<const float4*>(prow + c * 32);
+    #pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 v = src[j];
+                                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
+                                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
+                                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
+                                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                            }
+                        }
+                        // The box is stored when any of the warp's rows lies inside
+                        // M (the TMA drops rows >= M and columns >= N); the
+                        // decision is warp-uniform.
+                        stored = !give_up && row0 < p.m && n < p.n;
+                        if (stored) {
+                            if constexpr (kSide) {
+                                const uint32_t slot = ring + static_cast<uint32_t>(k % kSideSlots) * kSideSlotBytes;
+                                if (ok) swiglu_chunk_in_smem(slot, lane, r);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&G.xmap[2], slot, n, row0);
+                                    tma_store_2d(&G.xmap[3], slot + kBf16BoxBytes, n, row0);
+                                    bulk_commit_group();
+                                }
+                            } else {
+                                // a box is rewritten only after the store that read
+                                // it, two chunks back, has finished reading
+                                const uint32_t box = out_stage + (n_stored & 1u) * kBoxBytes;
+                                if (lane == 0) bulk_wait_group_read<1>();
+                                __syncwarp();
+                                if (ok) epilogue_chunk_to_smem<EPI>(box, lane, r, x0);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    if constexpr (EPI == static_cast<int>(Epilogue::AccumF32))
+                                        tma_reduce_add_2d(&G.omap[pi], box, n, row0);
+                                    else
+                                        tma_store_2d(&G.omap[pi], box, n, row0);
+                                    bulk_commit_group();
+                                }
+                                ++n_stored;
+                            }
+                        }
+                    }
+                    if constexpr (kSide) {
+                        // Refill the slot chunk k - 1 used, once the stores that
+                        // read it are done (all but this chunk's own group).
+                        if (lane == 0 && issued < n_chunks) {
+                            if (stored)
+                                bulk_wait_group_read<1>();
+                            else
+                                bulk_wait_group_read<0>();
+                            issue_side(issued);
+                            ++issued;
+                        }
+                        ++k;
+                    }
                 }
             }
             if (SPLIT && store_partial && alive) {
@@ -1126,10 +1235,12 @@ cudaError_t dispatch_pair(const GemmArgs& g, const PairGroup& G, cudaStream_t st
     constexpr int kResid = static_cast<int>(Epilogue::AddResidual);
     constexpr int kSwiglu = static_cast<int>(Epilogue::SwigluBwd);
     constexpr int kAccum = static_cast<int>(Epilogue::AccumF32);
+    constexpr int kSwigluFwd = static_cast<int>(Epilogue::SwigluFwd);
     switch (g.kind) {
         case GemmKind::Forward:
             if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, false, kStore>(G, stream);
             if (g.epi == Epilogue::AddResidual) return launch_pair_variant<false, false, kResid>(G, stream);
+            if (g.epi == Epilogue::SwigluFwd) return launch_pair_variant<false, false, kSwigluFwd>(G, stream);
             break;
         case GemmKind::BackwardInput:
             if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, true, kStore>(G, stream);
@@ -1222,6 +1333,16 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
              encode_map(&mx[2], out, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
              encode_map(&mx[3], out + g.ffn, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     }
+    // SwiGLU forward (CTA-pair kernel only): [g | u] out through the output map,
+    // s through the first extra map, 32 x 32 boxes each; each 256-column tile
+    // holds 128 features of g and the same 128 of u.
+    if (g.epi == Epilogue::SwigluFwd) {
+        if (!pair || !mx || g.kind != GemmKind::Forward || g.ffn <= 0 || g.ffn % kHalf != 0 || g.n != 2 * g.ffn ||
+            !g.out2)
+            return cudaErrorInvalidValue;
+        ok = ok && encode_map(&mo, g.out, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+             encode_map(&mx[0], g.out2, g.m, g.ffn, g.ldo2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    }
     if (!ok) return cudaErrorInvalidValue;
     p = KParams{};
     p.m = g.m;
@@ -1303,7 +1424,7 @@ cudaError_t launch_gemm_group(const GemmArgs* gs, int n, cudaStream_t stream) {
     bool grouped = n > 1 && n <= kMaxGroup;
     for (int i = 0; grouped && i < n; ++i)
         grouped = gs[i].m >= kPairM && gs[i].n >= kPairN && gs[i].k > 0 && gs[i].kind == gs[0].kind &&
-                  gs[i].epi == gs[0].epi && gs[i].epi != Epilogue::SwigluBwd;
+                  gs[i].epi == gs[0].epi && gs[i].epi != Epilogue::SwigluBwd && gs[i].epi != Epilogue::SwigluFwd;
     if (!grouped) {
         for (int i = 0; i < n; ++i) {
             const cudaError_t e = launch_gemm(gs[i], stream);

@@ -20,6 +20,8 @@ enum class Epilogue : int {
     AddResidual = 1,   // out bf16 = acc + aux (bf16, row stride ld_aux)
     SwigluBwd = 2,     // acc = ds; aux holds [g | u] (row stride ld_aux), out = [dg | du]
     AccumF32 = 3,      // out f32 += acc
+    SwigluFwd = 4,     // b = [W_gate; W_up] (2 ffn rows): out = [g | u] (bf16, row stride ldo) and
+                       // out2 = silu(g) u from the bf16 g and u (row stride ldo2); n = 2 ffn
 };
 
 struct GemmArgs {
@@ -34,7 +36,9 @@ struct GemmArgs {
     int64_t ldo;
     const void* aux;   // residual or [g | u]
     int64_t ld_aux;
-    int ffn;           // SwigluBwd: column offset of u in aux and of du in out
+    int ffn;           // SwigluBwd, SwigluFwd: column offset of u (and du) in aux and out
+    void* out2;        // SwigluFwd: s [m, ffn] bf16
+    int64_t ldo2;
     // Optional K-split scratch.  A CTA-pair launch whose last wave of tiles
     // would leave at least half of the CTA pairs idle cuts the K of that
     // wave's tiles in two halves computed by different CTA pairs; the half

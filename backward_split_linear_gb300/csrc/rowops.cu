@@ -302,7 +302,7 @@ __global__ void swiglu_fwd_kernel(const uint16_t* __restrict__ gu, uint16_t* __r
         const V8 u = load8(row + ffn + 8 * c);
         float o[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = g.v[e] * __fdividef(1.0f, 1.0f + __expf(-g.v[e])) * u.v[e];
+        for (int e = 0; e < 8; ++e) o[e] = swiglu_value(g.v[e], u.v[e]);
         store8(s + t * ffn + 8 * c, o);
     }
 }
