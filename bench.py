@@ -68,7 +68,8 @@ def gemm_flops_per_mb(w):
 
 GEMM_SOURCES = ("gemm.cu", "device_common.cuh", "launch.h")
 ROW_SOURCES = ("rowops.cu", "device_common.cuh", "launch.h")
-EPILOGUES = {0: "bf16 store", 1: "residual epilogue", 2: "SwiGLU backward epilogue", 3: "float32 TMA reduce-add epilogue"}
+EPILOGUES = {0: "bf16 store", 1: "residual epilogue", 2: "SwiGLU backward epilogue", 3: "float32 TMA reduce-add epilogue",
+             4: "SwiGLU forward epilogue"}
 
 
 def _sources_sha(names):
