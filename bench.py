@@ -492,7 +492,19 @@ def measure_config(w, order, steps, warmup, peaks, peak_key, params=None, seed=0
         ab = trace["attn_backward"]
         rec["attention_bwd_tflops"] = ab["flops"] / (ab["ms"] * 1e-3) / 1e12 if ab["ms"] else None
         rec["attention_bwd_share_of_b_time"] = ab["ms"] / b_ms if b_ms else None
+        rec["attention_bwd_roofline"] = attention_roofline(ab, peaks, peak_key)
     return rec
+
+
+def attention_roofline(ab, peaks, peak_key):
+    """The causal attention backward (row kernel, dK/dV and dQ kernels, events around each call) against
+    the dense bf16 peak, on its algorithmic count (5 products of 2 d per visible query-key pair)."""
+    if not ab["ms"]:
+        return None
+    achieved = ab["flops"] / (ab["ms"] * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peaks[peak_key], "unit": "TFLOP/s",
+            "frac": achieved / peaks[peak_key], "peak_source": f"{peaks['source']} {peak_key}",
+            "launches": ab["launches"], "ms_per_launch": ab["ms"] / max(1, ab["launches"])}
 
 
 def wgrad_sweep_record(tokens, steps, warmup, peaks):
@@ -830,6 +842,7 @@ def run_ours(args, w):
                                      "dQ recomputes S and dP)",
                 "bwd_share_of_b_time": ab["ms"] / b_ms if b_ms else None,
                 "b_tflops_with_attention": (b_flops + ab["flops"]) / (b_ms * 1e-3) / 1e12,
+                "bwd_roofline": attention_roofline(ab, peaks, "bf16_tflops_sustained"),
             }
         if (world == 1 and args.workload == "llama8b_stage" and args.w_mode == "per-microbatch"
                 and not args.overridden and args.stage == 0 and not args.pipeline and not args.no_workloads):

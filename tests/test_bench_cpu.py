@@ -109,3 +109,16 @@ def test_row_traffic_record(tmp_path):
     rec = bench.row_traffic_record(str(csv), "cmd", 5e6)
     assert rec["launches"] == 2 and abs(rec["dram_bytes_per_unit"] - 2.0) < 1e-12
     assert rec["source_sha256"] == bench.row_source_sha()
+
+
+def test_attention_roofline_record():
+    import bench
+
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "measured"}
+    ab = {"flops": 343.7e9 * 4, "ms": 1.4, "launches": 4}
+    rec = bench.attention_roofline(ab, peaks, "bf16_tflops_sustained")
+    assert rec["bound"] == "tensor" and rec["unit"] == "TFLOP/s"
+    assert abs(rec["achieved"] - 343.7e9 * 4 / 1.4e-3 / 1e12) < 1e-9
+    assert abs(rec["frac"] - rec["achieved"] / 1700.0) < 1e-12
+    assert rec["ms_per_launch"] == 0.35
+    assert bench.attention_roofline({"flops": 0.0, "ms": 0.0, "launches": 0}, peaks, "bf16_tflops") is None
