@@ -54,9 +54,11 @@ def test_fused_forward_equals_gemm_then_row_kernel(tokens, hidden, ffn):
     st.close()
 
 
-def test_short_microbatch_keeps_two_launches():
-    """Below 256 tokens the one-CTA GEMM runs and the SwiGLU stays a row kernel."""
-    tokens, hidden, ffn = 200, 512, 1024
+@pytest.mark.parametrize("tokens,ffn", [(200, 1024), (512, 1344)])
+def test_unfused_cases_keep_two_launches(tokens, ffn):
+    """Below 256 tokens (the one-CTA GEMM) or with ffn not a multiple of 128 (a 256-column
+    tile would not hold g and u of the same features) the SwiGLU stays a row kernel."""
+    hidden = 512
     inp = synth.stage_inputs("mlp", 1, hidden, ffn, tokens=tokens, n_mb=1, seed=12)
     st = Stage.from_synth("mlp", 1, hidden, ffn, max_tokens=tokens, max_inflight=1, params_bits=inp["params"])
     y = torch.empty(tokens, hidden, dtype=torch.bfloat16, device="cuda")
