@@ -508,14 +508,15 @@ constexpr int kHalf = 128;
 constexpr uint32_t kPairAStage = kHalf * BK * 2;  // 16 KiB
 constexpr uint32_t kPairBStage = kHalf * BK * 2;  // 16 KiB
 constexpr uint32_t kPairStage = kPairAStage + kPairBStage;
-// Side-input ring of the SwiGLU backward: per epilogue warp four slots, each
-// the g and u boxes of one 32-column chunk; the operand ring gives up a stage
-// to make room.
-constexpr int kSideSlots = 4;
+// Side-input ring of the SwiGLU backward: per epilogue warp two slots, each
+// the g and u boxes of one 32-column chunk, so that the operand ring keeps all
+// six stages (four slots and five stages: the SwiGLU dgrad took 306.7 us
+// against 295.5 us, same bits; three slots and five stages: 310.3 us).
+constexpr int kSideSlots = 2;
 constexpr uint32_t kSideSlotBytes = 2 * kBf16BoxBytes;
 template <int EPI>
 __host__ __device__ constexpr int pair_stages() {
-    return EPI == static_cast<int>(Epilogue::SwigluBwd) ? 5 : 6;
+    return 6;
 }
 template <int EPI>
 __host__ __device__ constexpr int pair_num_bars() {
@@ -526,7 +527,7 @@ __host__ __device__ constexpr int pair_num_bars() {
 // 4096 x 28672 forward on GB300), and the float32 weight-gradient sums through
 // TMA reduce-adds, where the L2 does the read-modify-write.  The SwiGLU
 // backward has its side inputs g and u brought in by TMA as well, into a ring
-// that runs three chunks ahead, computes dg and du in place there and stores
+// that runs one chunk ahead, computes dg and du in place there and stores
 // them by TMA: its epilogue warps touch no global memory with per-row accesses.
 template <int EPI>
 __host__ __device__ constexpr bool tma_out() {
