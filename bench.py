@@ -496,6 +496,48 @@ def measure_config(w, order, steps, warmup, peaks, peak_key, params=None, seed=0
     return rec
 
 
+def attention_layer_alone(w, peaks, reps=5, warmup=3):
+    """The causal attention of one layer of workload `w` through its C-ABI ops alone (seeded N(0, 1)
+    qkv and da, the forward's a and lse): CUDA events around `reps` back-to-back calls of the forward
+    and of the backward after `warmup` calls, against the burst bf16 peak (nothing else runs, so
+    the clocks are the unloaded ones)."""
+    import torch
+
+    from backward_split_linear_gb300 import binding as zb
+
+    t, nh, nkv, d = w["tokens"], w["n_heads"], w["n_kv_heads"], w["head_dim"]
+    seq = w.get("seq_len", 0)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    qkv = torch.randn(t, (nh + 2 * nkv) * d, device="cuda", generator=g).to(torch.bfloat16)
+    da = torch.randn(t, nh * d, device="cuda", generator=g).to(torch.bfloat16)
+    a = torch.empty(t, nh * d, device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(nh, zb.zb_op_attention_stat_stride(t), device="cuda", dtype=torch.float32)
+    dvec = torch.empty_like(lse)
+    dqkv = torch.empty_like(qkv)
+    fwd = lambda: zb.zb_op_attention_causal_forward(qkv, a, lse, t, nh, nkv, d, seq)
+    bwd = lambda: zb.zb_op_attention_causal_backward(qkv, a, da, lse, dvec, dqkv, t, nh, nkv, d, seq)
+    times = {}
+    for name, fn in (("fwd", fwd), ("bwd", bwd)):
+        for _ in range(warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times[name] = e0.elapsed_time(e1) / reps
+    # visible (query, key) pairs and head: sum over sequences of L (L + 1) / 2, times the heads
+    lens = [seq] * (t // seq) + ([t % seq] if t % seq else []) if seq else [t]
+    pairs = nh * sum(n * (n + 1) // 2 for n in lens)
+    fwd_tf = 4 * d * pairs / (times["fwd"] * 1e-3) / 1e12
+    bwd_tf = 10 * d * pairs / (times["bwd"] * 1e-3) / 1e12
+    return {"fwd_ms": times["fwd"], "bwd_ms": times["bwd"], "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "bwd_frac_of_burst_peak": bwd_tf / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} bf16_tflops",
+            "flops_counted": "4 d (forward) and 10 d (backward) per visible query-key pair and head"}
+
+
 def attention_roofline(ab, peaks, peak_key):
     """The causal attention backward (row kernel, dK/dV and dQ kernels, events around each call) against
     the dense bf16 peak, on its algorithmic count (5 products of 2 d per visible query-key pair)."""
@@ -571,6 +613,7 @@ def other_workloads(args, st, peaks):
     rec = measure_config(wc, zb.zb_schedule("zbh1", 0, wc["m"], wc["m"]), steps, warmup, peaks,
                          "bf16_tflops_sustained")
     rec["order"] = "ZB-H1 order of stage 0 of p = m = 8"
+    rec["attention_layer_alone"] = attention_layer_alone(wc, peaks)
     out["llama8b_stage_causal"] = rec
     torch.cuda.empty_cache()
     out["wgrad_sweep_in4096_out14336_m4"] = {f"t{t}": wgrad_sweep_record(t, steps, warmup, peaks)
@@ -843,6 +886,7 @@ def run_ours(args, w):
                 "bwd_share_of_b_time": ab["ms"] / b_ms if b_ms else None,
                 "b_tflops_with_attention": (b_flops + ab["flops"]) / (b_ms * 1e-3) / 1e12,
                 "bwd_roofline": attention_roofline(ab, peaks, "bf16_tflops_sustained"),
+                "layer_alone": attention_layer_alone(w, peaks) if not args.overridden else None,
             }
         if (world == 1 and args.workload == "llama8b_stage" and args.w_mode == "per-microbatch"
                 and not args.overridden and args.stage == 0 and not args.pipeline and not args.no_workloads):
