@@ -7,7 +7,8 @@
 // ("Zero-Bubble Pipeline Parallelism Guide for LLMs", "Core Innovation 1");
 // the core has no weights, so all of its backward belongs to B.
 //
-// Three kernels, each one CTA per 128-row tile:
+// Three kernels on 128-row tiles (the forward and dK/dV one CTA per tile, dQ
+// persistent with one CTA per SM):
 //   warp 0     one thread issues TMA loads
 //   warp 1     allocates tensor memory; the whole warp runs the MMA issue loop
 //              and its elected lane carries each tcgen05.mma and commit
@@ -24,8 +25,9 @@
 //                     and every query block from the diagonal on:
 //                     S^T = K Q^T, dP^T = V dO^T, P^T = exp2(S^T c - lse),
 //                     dS^T = P^T (dP^T - D); dV += P^T dO, dK += dS^T Q.
-//   attn_causal_dq_kernel    (head h, query block): S = Q K^T, dP = dO V^T, dS as
-//                     above, dQ += dS K over the key blocks up to the diagonal.
+//   attn_causal_dq_kernel    tiles (head h, query block), taken from a counter:
+//                     S = Q K^T, dP = dO V^T, dS as above, dQ += dS K over
+//                     the key blocks up to the diagonal.
 // dQ has its own kernel (it recomputes S and dP) so that no two CTAs add into
 // the same output: results are the same bits on every run.  D = rowsum(dO * O)
 // comes from a small row kernel first; then dK/dV (on the caller's stream) and
@@ -39,6 +41,7 @@
 // columns it has read, and the next product takes them as its A operand.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -139,6 +142,12 @@ template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, int col, int r0) {
 #pragma unroll
     for (int b = 0; b < D / 64; ++b) tma_load_2d(dst + b * 16384u, map, bar, col + 64 * b, r0);
+}
+// The same boxes into L2 only.
+template <int D>
+__device__ __forceinline__ void prefetch_tile(const CUtensorMap* map, int col, int r0) {
+#pragma unroll
+    for (int b = 0; b < D / 64; ++b) tma_prefetch_l2_2d(map, col + 64 * b, r0);
 }
 
 // ------------------------------------------------------------------------ forward
@@ -399,15 +408,30 @@ __device__ __forceinline__ uint32_t packed_col(int kk) { return static_cast<uint
 
 // ------------------------------------------------------------------------ backward: dq
 
-// One CTA per (query head, query block) walks the key blocks up to the
-// diagonal, 128 keys a step.  Per step the tensor cores run S = Q K^T,
-// dP = dO V^T (both 128 x 128, K-major operands) and dQ += dS K (A = dS from
-// tensor memory, B = K as an MN-major operand).  S has two tensor-memory
-// buffers, dP one: the MMA order is S[j+1], dP[j+1], dQ[j], so the row warps'
-// pass over step j (P = exp2(S c - lse) into registers as soon as S lands,
-// then dS = P (dP - D), packed over the S columns just read) overlaps the
-// products of its neighbours.  Two groups of four row warps take 64 key
-// columns each.  K streams through three stages, V through two.
+// A persistent kernel, one CTA per SM.  Each CTA takes (query head, query
+// block) tiles from a counter in global memory, longest rows first, and walks
+// a tile's key blocks up to the diagonal, 128 keys a step.  Per step the
+// tensor cores run S = Q K^T, dP = dO V^T (both 128 x 128, K-major operands)
+// and dQ += dS K (A = dS from tensor memory, B = K as an MN-major operand).
+// S has two tensor-memory buffers, dP one: the MMA order is S[j+1], dP[j+1],
+// dQ[j], so the row warps' pass over step j (P = exp2(S c - lse) into
+// registers as soon as S lands, then dS = P (dP - D), packed over the S
+// columns just read) overlaps the products of its neighbours.  Two groups of
+// four row warps take 64 key columns each.  K streams through three stages,
+// V through two, on one barrier per step.
+//
+// The steps of a CTA's tiles form one sequence: the rings, the S buffers and
+// the barriers' phases run on from one tile to the next.  The next tile's Q
+// and dO load as soon as the last S and dP products of the current one are
+// done, and its first products run while the row warps store the finished
+// tile's dQ.  (With one CTA per tile, an SM sat idle for about 4.6 us between
+// one CTA's exit and the next one's start, and again while Q and dO loaded:
+// with about 7 tiles per SM, a fifth of the kernel.)  A tile goes to whichever
+// CTA asks next, so CTAs that start late, on SMs held by the dK/dV kernel's
+// longest CTAs, take fewer; a CTA asks when it issues its current tile's last
+// K / V load, and pulls the new tile's Q and dO into L2 at once.  Each tile is
+// computed by one CTA in one order: the results do not depend on which CTA
+// took it.
 template <int D>
 struct DqSmem {
     static constexpr int kKStages = 3, kVStages = 2;
@@ -415,14 +439,37 @@ struct DqSmem {
     static constexpr uint32_t kQ = 0, kDO = kTile, kK = 2 * kTile;
     static constexpr uint32_t kV = kK + kKStages * kTile;
     static constexpr uint32_t kBars = kV + kVStages * kTile;
-    static constexpr int kNumBars = 1 + 2 * kKStages + kVStages + 2 + 4;
-    static constexpr size_t kBytes = kBars + 8 * kNumBars + 16;
+    // q full / empty, the K ring (full, empty), the V ring (empty), S (2), dP,
+    // dS, done, drain, the two tile slots (full, empty)
+    static constexpr int kNumBars = 2 + 2 * kKStages + kVStages + 2 + 4 + 4;
+    static constexpr uint32_t kTmemSlot = kBars + 8 * kNumBars;
+    static constexpr uint32_t kTileSlot = kTmemSlot + 8;  // the tile number held by each slot (two ints)
+    static constexpr size_t kUsed = kTileSlot + 8 + 16;
+    static constexpr size_t kBytes = kUsed > kMinSmem ? kUsed : kMinSmem;
 };
+
+// Tile t of the dQ kernel: query block n_blocks - 1 - t / n_heads (the
+// longest rows first), head t % n_heads; its key blocks run from the first
+// of the query block's sequence up to the diagonal.
+struct DqTile {
+    int h, q0, s1, kb0, nk;
+};
+__device__ __forceinline__ DqTile dq_tile(const AttnParams& p, int t) {
+    DqTile d;
+    const int qb = p.n_blocks - 1 - t / p.n_heads;
+    d.h = t % p.n_heads;
+    d.q0 = qb * kRows;
+    int s0;
+    seq_bounds(p, d.q0, s0, d.s1);
+    d.kb0 = s0 / kRows;
+    d.nk = qb - d.kb0 + 1;
+    return d;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     attn_causal_dq_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
-                          const AttnParams p) {
+                          const AttnParams p, int* tile_counter) {
     using L = DqSmem<D>;
     constexpr int NK = L::kKStages, NV = L::kVStages;
     constexpr uint32_t kTile = L::kTile;
@@ -434,43 +481,42 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     }
     const uint32_t s_q = base + L::kQ, s_do = base + L::kDO, s_k = base + L::kK, s_v = base + L::kV;
     const uint32_t bars = base + L::kBars;
-    const uint32_t q_full = bars;
-    auto k_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto k_empty = [&](int s) { return bars + 8u * (1 + NK + s); };
-    auto v_empty = [&](int s) { return bars + 8u * (1 + 2 * NK + s); };
-    constexpr int kB = 1 + 2 * NK + NV;
-    auto s_full = [&](int b) { return bars + 8u * (kB + b); };
+    const uint32_t q_full = bars, q_empty = bars + 8u;
+    auto k_full = [&](uint32_t s) { return bars + 8u * (2 + s); };
+    auto k_empty = [&](uint32_t s) { return bars + 8u * (2 + NK + s); };
+    auto v_empty = [&](uint32_t s) { return bars + 8u * (2 + 2 * NK + s); };
+    constexpr int kB = 2 + 2 * NK + NV;
+    auto s_full = [&](uint32_t b) { return bars + 8u * (kB + b); };
     const uint32_t dp_full = bars + 8u * (kB + 2), ds_full = bars + 8u * (kB + 3), done = bars + 8u * (kB + 4),
                    drain = bars + 8u * (kB + 5);
-    const uint32_t tmem_slot = bars + 8u * L::kNumBars;
-    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - base));
+    auto tile_full = [&](uint32_t s) { return bars + 8u * (kB + 6 + s); };
+    auto tile_empty = [&](uint32_t s) { return bars + 8u * (kB + 8 + s); };
+    const uint32_t tmem_slot = base + L::kTmemSlot;
+    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + L::kTmemSlot);
+    volatile int* tile_slot = reinterpret_cast<volatile int*>(smem_raw + L::kTileSlot);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qb = p.n_blocks - 1 - static_cast<int>(blockIdx.x) / p.n_heads;  // longest rows first
-    const int h = static_cast<int>(blockIdx.x) % p.n_heads;
-    const int g = h / (p.n_heads / p.n_kv_heads);
-    const int q0 = qb * kRows;
-    int s0, s1;
-    seq_bounds(p, q0, s0, s1);
-    const int kb0 = s0 / kRows;
-    const int nk = qb - kb0 + 1;
-    const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
+    const int n_tiles = p.n_blocks * p.n_heads;
+    const int group = p.n_heads / p.n_kv_heads;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < NK; ++s) {
             mbar_init(k_full(s), 1);
             mbar_init(k_empty(s), 1);
         }
-        for (int s = 0; s < NV; ++s) {
-            mbar_init(v_empty(s), 1);
-        }
+        for (int s = 0; s < NV; ++s) mbar_init(v_empty(s), 1);
         mbar_init(s_full(0), 1);
         mbar_init(s_full(1), 1);
         mbar_init(dp_full, 1);
         mbar_init(ds_full, 8);
         mbar_init(done, 1);
         mbar_init(drain, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(tile_full(s), 1);
+            mbar_init(tile_empty(s), 9);  // the MMA warp and the eight row warps
+        }
         mbar_fence_init();
         tma_prefetch_map(&map_qkv);
         tma_prefetch_map(&map_do);
@@ -483,28 +529,71 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     // columns: S buffers 0-127 and 128-255 (dS packed into columns 0-31 and
     // 64-95 of a buffer once read), dP 256-383, dQ 384..
     const uint32_t t_dp = tmem_base + 256, t_dq = tmem_base + 384;
-    auto t_s = [&](int j) { return tmem_base + 128u * static_cast<uint32_t>(j & 1); };
+    auto t_s = [&](uint32_t g) { return tmem_base + 128u * (g & 1u); };
+    // A consumer warp's view of tile slot n & 1: the tile number (-1: none left),
+    // after which the warp releases the slot.
+    auto take_tile = [&](uint32_t n, int& t) {
+        if (!warp_wait(tile_full(n & 1u), (n >> 1) & 1u, p.status)) return false;
+        t = tile_slot[n & 1u];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tile_empty(n & 1u));
+        return true;
+    };
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, 2 * kTile);
-            load_tile<D>(s_q, &map_qkv, q_full, h * D, q0);
-            load_tile<D>(s_do, &map_do, q_full, h * D, q0);
-            uint32_t nkf = 0;
-            for (int j = 0; j < nk; ++j) {
-                const int k0 = (kb0 + j) * kRows;
-                // K[j] and V[j] land on one barrier: one wait per step for the MMA warp
-                if (!mbar_wait_fast(k_empty(j % NK), ((j / NK) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                if (!mbar_wait_fast(v_empty(j % NV), ((j / NV) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                mbar_arrive_expect_tx(k_full(j % NK), 2 * kTile);
-                load_tile<D>(s_k + (j % NK) * kTile, &map_qkv, k_full(j % NK), kcol, k0);
-                load_tile<D>(s_v + (j % NV) * kTile, &map_qkv, k_full(j % NK), vcol, k0);
-                ++nkf;
+            // Fills slot n & 1 with the number of this CTA's tile n once every
+            // consumer has read the slot's previous tile; -1 when none is left,
+            // -2 when the wait failed.
+            auto fetch = [&](uint32_t n) {
+                if (!mbar_wait_fast(tile_empty(n & 1u), ((n >> 1) & 1u) ^ 1u, p.status, kSiteAttn)) return -2;
+                int t = atomicAdd(tile_counter, 1);
+                if (t >= n_tiles) t = -1;
+                tile_slot[n & 1u] = t;
+                mbar_arrive(tile_full(n & 1u));
+                return t;
+            };
+            uint32_t nq = 0, nkf = 0;  // Q / dO loads and K / V steps issued
+            int t = fetch(0);
+            for (uint32_t n = 0; t >= 0; ++n) {
+                const DqTile tl = dq_tile(p, t);
+                // Q and dO once the previous tile's S and dP products are done
+                if (!mbar_wait_fast(q_empty, (n & 1u) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(q_full, 2 * kTile);
+                load_tile<D>(s_q, &map_qkv, q_full, tl.h * D, tl.q0);
+                load_tile<D>(s_do, &map_do, q_full, tl.h * D, tl.q0);
+                ++nq;
+                const int g = tl.h / group;
+                const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
+                int t_next = -2;
+                for (int j = 0; j < tl.nk; ++j) {
+                    const uint32_t u = nkf;
+                    // K[j] and V[j] land on one barrier: one wait per step for the MMA warp
+                    if (!mbar_wait_fast(k_empty(u % NK), ((u / NK) & 1u) ^ 1u, p.status, kSiteAttn)) break;
+                    if (!mbar_wait_fast(v_empty(u % NV), ((u / NV) & 1u) ^ 1u, p.status, kSiteAttn)) break;
+                    mbar_arrive_expect_tx(k_full(u % NK), 2 * kTile);
+                    load_tile<D>(s_k + (u % NK) * kTile, &map_qkv, k_full(u % NK), kcol, (tl.kb0 + j) * kRows);
+                    load_tile<D>(s_v + (u % NV) * kTile, &map_qkv, k_full(u % NK), vcol, (tl.kb0 + j) * kRows);
+                    ++nkf;
+                    // The next tile's number at this tile's last load, two or three steps
+                    // before its end (taken earlier, the CTAs that start first took more
+                    // than their share of the long tiles), and its Q and dO into L2.
+                    if (j == tl.nk - 1) {
+                        t_next = fetch(n + 1);
+                        if (t_next >= 0) {
+                            const DqTile nx = dq_tile(p, t_next);
+                            prefetch_tile<D>(&map_qkv, nx.h * D, nx.q0);
+                            prefetch_tile<D>(&map_do, nx.h * D, nx.q0);
+                        }
+                    }
+                }
+                t = t_next;  // -2 after a failed wait ends the loop
             }
-            mbar_wait_fast(q_full, 0, p.status, kSiteDrain);
+            // no copy may land after the CTA has gone
+            if (nq > 0) mbar_wait_fast(q_full, (nq - 1) & 1u, p.status, kSiteDrain);
             for (int s = 0; s < NK; ++s) {
                 const uint32_t u = ring_uses(nkf, NK, s);
-                if (u > 0) mbar_wait_fast(k_full(s), (u - 1) & 1, p.status, kSiteDrain);
+                if (u > 0) mbar_wait_fast(k_full(s), (u - 1) & 1u, p.status, kSiteDrain);
             }
         }
     } else if (warp == 1) {
@@ -513,41 +602,63 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
         constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
         constexpr uint32_t idesc_q = mma_idesc_bf16(128, D, false, true);
         const uint64_t q_desc = kdesc_base(s_q), do_desc = kdesc_base(s_do);
-        auto issue_s = [&](int j) {
-            const int st = j % NK;
-            if (!warp_wait(k_full(st), (j / NK) & 1, p.status)) return false;
+        auto issue_s = [&](uint32_t g) {
+            const uint32_t st = g % NK;
+            if (!warp_wait(k_full(st), (g / NK) & 1u, p.status)) return false;
             tc_fence_after();
             const uint64_t k_desc = kdesc_base(s_k + st * kTile);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                umma_bf16_elected(leader, t_s(j), kdesc_at(q_desc, kk), kdesc_at(k_desc, kk), idesc_s, kk > 0);
-            umma_commit_elected(leader, s_full(j & 1));
+                umma_bf16_elected(leader, t_s(g), kdesc_at(q_desc, kk), kdesc_at(k_desc, kk), idesc_s, kk > 0);
+            umma_commit_elected(leader, s_full(g & 1u));
             return true;
         };
-        auto issue_dp = [&](int j) {
-            const int st = j % NV;  // V[j] landed with K[j] (issue_s(j) waited for both)
+        auto issue_dp = [&](uint32_t g) {
+            const uint32_t st = g % NV;  // V[g] landed with K[g] (issue_s(g) waited for both)
             const uint64_t v_desc = kdesc_base(s_v + st * kTile);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 umma_bf16_elected(leader, t_dp, kdesc_at(do_desc, kk), kdesc_at(v_desc, kk), idesc_s, kk > 0);
             umma_commit_elected(leader, dp_full);
             umma_commit_elected(leader, v_empty(st));
-            return true;
         };
-        bool ok = warp_wait(q_full, 0, p.status) && issue_s(0) && issue_dp(0);
-        for (int j = 0; ok && j < nk; ++j) {
-            // S[j+1] into the other buffer; dP[j+1] once the row warps are done with dP[j]
-            if (j + 1 < nk && !issue_s(j + 1)) break;
-            if (!warp_wait(ds_full, j & 1, p.status)) break;
+        uint32_t g = 0;  // steps of this CTA so far, over all its tiles
+        bool ok = true;
+        for (uint32_t n = 0; ok; ++n) {
+            int t;
+            if (!take_tile(n, t) || t < 0) break;
+            const int nk = dq_tile(p, t).nk;
+            if (!warp_wait(q_full, n & 1u, p.status)) break;
             tc_fence_after();
-            if (j + 1 < nk && !issue_dp(j + 1)) break;
-            const uint64_t k_mn = mndesc_base(s_k + (j % NK) * kTile);
+            if (!issue_s(g)) break;
+            issue_dp(g);
+            // Q and dO are free for the next tile once the tile's last S and dP are done
+            if (nk == 1) umma_commit_elected(leader, q_empty);
+            for (int j = 0; j < nk; ++j, ++g) {
+                // S[j+1] into the other buffer; dP[j+1] once the row warps are done with dP[j]
+                const bool more = j + 1 < nk;
+                if (more && !issue_s(g + 1)) {
+                    ok = false;
+                    break;
+                }
+                if (!warp_wait(ds_full, g & 1u, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (more) {
+                    issue_dp(g + 1);
+                    if (j + 2 == nk) umma_commit_elected(leader, q_empty);
+                }
+                const uint64_t k_mn = mndesc_base(s_k + (g % NK) * kTile);
 #pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk)
-                umma_bf16_ts_elected(leader, t_dq, t_s(j) + packed_col(kk), mndesc_at(k_mn, kk), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
-            umma_commit_elected(leader, k_empty(j % NK));
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_bf16_ts_elected(leader, t_dq, t_s(g) + packed_col(kk), mndesc_at(k_mn, kk), idesc_q,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit_elected(leader, k_empty(g % NK));
+            }
+            if (ok) umma_commit_elected(leader, done);
         }
-        umma_commit_elected(leader, done);
         umma_commit_elected(leader, drain);
         mbar_wait_fast(drain, 0, p.status, kSiteDrain);
     } else {
@@ -556,78 +667,90 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
         const int gi = (warp - 2) >> 2;
         const int qw = warp & 3;
         const int row = qw * 32 + lane;
-        const int q = q0 + row;
         const uint32_t t_row = (static_cast<uint32_t>(qw * 32) << 16) + 64u * gi;
-        const bool valid = q < s1;
-        const float lse = valid ? p.lse[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
-        const float dv = valid ? p.dvec[static_cast<int64_t>(h) * p.ld_stat + q] : 0.f;
+        uint32_t g = 0;
         bool ok = true;
-        for (int j = 0; j < nk; ++j) {
-            const int c0 = (kb0 + j) * kRows + 64 * gi;
-            const int lim = valid ? min(q - c0, s1 - 1 - c0) : -1;  // last visible key column of this row
-            if (!warp_wait(s_full(j & 1), (j >> 1) & 1, p.status)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float pr[64];
-            uint32_t rs[64];
-            tmem_load_32(t_s(j) + t_row, *reinterpret_cast<uint32_t(*)[32]>(rs));
-            tmem_load_32(t_s(j) + t_row + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
-            tmem_wait_load();
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                if (__all_sync(0xffffffffu, lim >= 32 * c + 31)) {  // every column visible: no mask
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) pr[32 * c + i] = ex2(fmaf(__uint_as_float(rs[32 * c + i]), p.scale_log2, -lse));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        pr[32 * c + i] = keep_if(ex2(fmaf(__uint_as_float(rs[32 * c + i]), p.scale_log2, -lse)), 32 * c + i <= lim);
+        for (uint32_t n = 0; ok; ++n) {
+            int t;
+            if (!take_tile(n, t) || t < 0) break;
+            const DqTile tl = dq_tile(p, t);
+            const int q = tl.q0 + row;
+            const bool valid = q < tl.s1;
+            const float lse = valid ? p.lse[static_cast<int64_t>(tl.h) * p.ld_stat + q] : 0.f;
+            const float dv = valid ? p.dvec[static_cast<int64_t>(tl.h) * p.ld_stat + q] : 0.f;
+            for (int j = 0; j < tl.nk; ++j, ++g) {
+                const int c0 = (tl.kb0 + j) * kRows + 64 * gi;
+                const int lim = valid ? min(q - c0, tl.s1 - 1 - c0) : -1;  // last visible key column of this row
+                if (!warp_wait(s_full(g & 1u), (g >> 1) & 1u, p.status)) {
+                    ok = false;
+                    break;
                 }
-            }
-            if (!warp_wait(dp_full, j & 1, p.status)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t rp[64];
-            tmem_load_32(t_dp + t_row, *reinterpret_cast<uint32_t(*)[32]>(rp));
-            tmem_load_32(t_dp + t_row + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
-            tmem_wait_load();
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(pr[32 * c + 2 * e] * (__uint_as_float(rp[32 * c + 2 * e]) - dv),
-                                       pr[32 * c + 2 * e + 1] * (__uint_as_float(rp[32 * c + 2 * e + 1]) - dv));
-                // packed columns 16 c .. 16 c + 15 of the group's S columns, all read above
-                tmem_store_16(t_s(j) + t_row + 16 * c, w);
-            }
-            tmem_wait_store();
-            tc_fence_before();
-            warp_arrive(ds_full, lane);
-        }
-        // group gi stores dQ columns [D/2 gi, D/2 (gi + 1))
-        if (ok && warp_wait(done, 0, p.status)) {
-            tc_fence_after();
-            uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(q) * p.ld_out + h * D;
-            const uint32_t t_q = t_dq + (static_cast<uint32_t>(qw * 32) << 16);
-#pragma unroll 1
-            for (int c = gi * (D / 64); c < (gi + 1) * (D / 64); ++c) {
-                uint32_t r[32];
-                tmem_load_32(t_q + 32 * c, r);
+                tc_fence_after();
+                float pr[64];
+                uint32_t rs[64];
+                tmem_load_32(t_s(g) + t_row, *reinterpret_cast<uint32_t(*)[32]>(rs));
+                tmem_load_32(t_s(g) + t_row + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
                 tmem_wait_load();
-                if (valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-                    const float sc = p.scale;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    if (__all_sync(0xffffffffu, lim >= 32 * c + 31)) {  // every column visible: no mask
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            pr[32 * c + i] = ex2(fmaf(__uint_as_float(rs[32 * c + i]), p.scale_log2, -lse));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            pr[32 * c + i] =
+                                keep_if(ex2(fmaf(__uint_as_float(rs[32 * c + i]), p.scale_log2, -lse)), 32 * c + i <= lim);
+                    }
+                }
+                if (!warp_wait(dp_full, g & 1u, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t rp[64];
+                tmem_load_32(t_dp + t_row, *reinterpret_cast<uint32_t(*)[32]>(rp));
+                tmem_load_32(t_dp + t_row + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+                tmem_wait_load();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack_bf16x2(pr[32 * c + 2 * e] * (__uint_as_float(rp[32 * c + 2 * e]) - dv),
+                                           pr[32 * c + 2 * e + 1] * (__uint_as_float(rp[32 * c + 2 * e + 1]) - dv));
+                    // packed columns 16 c .. 16 c + 15 of the group's S columns, all read above
+                    tmem_store_16(t_s(g) + t_row + 16 * c, w);
+                }
+                tmem_wait_store();
+                tc_fence_before();
+                warp_arrive(ds_full, lane);
+            }
+            if (!ok || !warp_wait(done, n & 1u, p.status)) break;
+            // group gi stores dQ columns [D/2 gi, D/2 (gi + 1)); the tile's next
+            // dQ product waits for this group's next dS arrival, after these loads
+            tc_fence_after();
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(q) * p.ld_out + tl.h * D;
+            const uint32_t t_q = t_dq + (static_cast<uint32_t>(qw * 32) << 16) + 32u * (gi * (D / 64));
+            constexpr int kChunks = D / 64;  // 32-column chunks of this group's half
+            uint32_t r[kChunks][32];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) tmem_load_32(t_q + 32 * c, r[c]);
+            tmem_wait_load();
+            tc_fence_before();
+            if (valid) {
+                const float sc = p.scale;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * (gi * kChunks + c));
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        d4[k] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * k]) * sc, __uint_as_float(r[8 * k + 1]) * sc),
-                                           pack_bf16x2(__uint_as_float(r[8 * k + 2]) * sc, __uint_as_float(r[8 * k + 3]) * sc),
-                                           pack_bf16x2(__uint_as_float(r[8 * k + 4]) * sc, __uint_as_float(r[8 * k + 5]) * sc),
-                                           pack_bf16x2(__uint_as_float(r[8 * k + 6]) * sc, __uint_as_float(r[8 * k + 7]) * sc));
+                        d4[k] = make_uint4(
+                            pack_bf16x2(__uint_as_float(r[c][8 * k]) * sc, __uint_as_float(r[c][8 * k + 1]) * sc),
+                            pack_bf16x2(__uint_as_float(r[c][8 * k + 2]) * sc, __uint_as_float(r[c][8 * k + 3]) * sc),
+                            pack_bf16x2(__uint_as_float(r[c][8 * k + 4]) * sc, __uint_as_float(r[c][8 * k + 5]) * sc),
+                            pack_bf16x2(__uint_as_float(r[c][8 * k + 6]) * sc, __uint_as_float(r[c][8 * k + 7]) * sc));
                 }
             }
         }
@@ -1149,9 +1272,14 @@ cudaError_t fwd_launch(const AttnShape& s, const void* qkv, void* a, float* lse,
 // early sat idle until its longest CTAs were done.  The caller's stream forks
 // to the side stream after the row kernel and joins it after both launches; a
 // mutex keeps concurrent callers from interleaving the fork and join events.
+// The stream also owns the dQ kernel's tile counter (one int of device memory,
+// zeroed on the side stream before each launch) and the device's SM count
+// (the persistent kernel's grid).
 struct SideStream {
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
+    int* tiles = nullptr;
+    int sms = 0;
     std::mutex mu;
 };
 
@@ -1165,16 +1293,26 @@ SideStream* side_stream() {
     if (!s.stream) {
         cudaStream_t st = nullptr;
         cudaEvent_t f = nullptr, j = nullptr;
-        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        int* tiles = nullptr;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return nullptr;
+        if (cudaMalloc(&tiles, sizeof(int)) != cudaSuccess) return nullptr;
+        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaFree(tiles);
+            return nullptr;
+        }
         if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
             if (f) cudaEventDestroy(f);
             cudaStreamDestroy(st);
+            cudaFree(tiles);
             return nullptr;
         }
         s.stream = st;
         s.fork = f;
         s.join = j;
+        s.tiles = tiles;
+        s.sms = sms;
     }
     return &s;
 }
@@ -1212,8 +1350,13 @@ cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const
     if ((e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess) return e;
     attn_causal_dkdv_kernel<D><<<p.n_blocks * s.n_kv_heads, kAttnDkvThreads, DkvSmem<D>::kBytes, stream>>>(mq, md, p);
     const cudaError_t e_kv = cudaGetLastError();
-    attn_causal_dq_kernel<D><<<p.n_blocks * s.n_heads, kAttnBwdThreads, DqSmem<D>::kBytes, side->stream>>>(mq, md, p);
-    const cudaError_t e_q = cudaGetLastError();
+    const int n_tiles = p.n_blocks * s.n_heads;
+    cudaError_t e_q = cudaMemsetAsync(side->tiles, 0, sizeof(int), side->stream);
+    if (e_q == cudaSuccess) {
+        attn_causal_dq_kernel<D><<<static_cast<unsigned>(std::min(n_tiles, side->sms)), kAttnBwdThreads,
+                                   DqSmem<D>::kBytes, side->stream>>>(mq, md, p, side->tiles);
+        e_q = cudaGetLastError();
+    }
     // the join is recorded whatever happened above, so the caller's stream never
     // runs ahead of work already queued on the side stream
     if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess) return e;

@@ -118,9 +118,9 @@ cudaError_t launch_attention_causal_forward(const AttnShape& s, const void* qkv,
 // from it and joined back.
 cudaError_t launch_attention_causal_backward(const AttnShape& s, const void* qkv, const void* a, const void* da,
                                              const float* lse, float* dvec, void* dqkv, cudaStream_t stream);
-// Creates the current device's side stream and events ahead of the first
-// backward (a stage calls it at its first forward, so that no stream or event
-// is created while the caller's stream may be capturing a graph).
+// Creates the current device's side stream, events and dQ tile counter ahead
+// of the first backward (a stage calls it at its first forward, so that nothing
+// is created or allocated while the caller's stream may be capturing a graph).
 cudaError_t attention_prepare();
 
 // Device status word of the current device (see zb_device_status).

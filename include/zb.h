@@ -280,9 +280,10 @@ zb_status zb_op_attention_forward(const void* qkv, void* a, int32_t tokens,
  *    kernel on a library-owned stream of the current device, forked from
  *    `stream` after the work already queued there and joined back before the
  *    call returns; work queued on `stream` afterwards sees all of dqkv.  The
- *    library creates that stream (and two events) at the first causal
- *    backward on a device, or at a causal stage's first forward; it lives
- *    until the process ends. */
+ *    library creates that stream, two events and a 4-byte device counter
+ *    (the dQ kernel's tile counter, zeroed on that stream before each
+ *    launch) at the first causal backward on a device, or at a causal
+ *    stage's first forward; they live until the process ends. */
 int32_t zb_op_attention_stat_stride(int32_t tokens);
 zb_status zb_op_attention_causal_forward(const void* qkv, void* a, float* lse, int32_t tokens,
                                          int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
