@@ -16,7 +16,8 @@
 //   warps 6-9  (backward kernels) a second group of row warps, on the other
 //              64 columns of every 128-wide step
 //   warp 10    (dK/dV) the statistics warp: lse and D of each step's queries
-//              into the B operand of the score products' extra K step
+//              into the B operand of the score products' extra K step;
+//              (dQ) a second MMA warp, for the dQ products
 //
 //   attn_causal_fwd_kernel   (head h, query block):  S = Q K^T -> online softmax ->
 //                     O += P V over the key blocks up to the diagonal; writes
@@ -55,6 +56,9 @@ constexpr int kAttnThreads = 192;
 // The backward kernels run two groups of four row warps (warps 2-5 and 6-9),
 // each on every other sub-block.
 constexpr int kAttnBwdThreads = 320;
+// The dQ kernel adds a warp that issues the dQ products (warp 10).
+constexpr int kAttnDqThreads = kAttnBwdThreads + 32;
+constexpr int kDqWarp = kAttnBwdThreads / 32;
 constexpr int kRows = 128;             // query and key block
 // Every attention CTA allocates all 512 tensor-memory columns; asking for at
 // least this much shared memory keeps two CTAs off one SM (the second would
@@ -420,6 +424,15 @@ __device__ __forceinline__ uint32_t packed_col(int kk) { return static_cast<uint
 // four row warps take 64 key columns each.  K streams through three stages,
 // V through two, on one barrier per step.
 //
+// Two warps issue the MMAs: warp 1 the S and dP products, warp 10 the dQ
+// products.  With one issuing warp, every wait and commit between two batches
+// of 128 x 128 products left the tensor pipe idle (its queue holds little more
+// than one such product), about a quarter of each step; with two, one warp's
+// waits run while the other's products execute.  The warps order their
+// products through two barriers: S[j+2] reuses the buffer that dQ[j] reads,
+// so warp 1 issues it after warp 10 has issued dQ[j]; and warp 10 issues
+// dQ[j] after warp 1 has issued dP[j+1], which the row warps wait for.
+//
 // The steps of a CTA's tiles form one sequence: the rings, the S buffers and
 // the barriers' phases run on from one tile to the next.  The next tile's Q
 // and dO load as soon as the last S and dP products of the current one are
@@ -440,8 +453,8 @@ struct DqSmem {
     static constexpr uint32_t kV = kK + kKStages * kTile;
     static constexpr uint32_t kBars = kV + kVStages * kTile;
     // q full / empty, the K ring (full, empty), the V ring (empty), S (2), dP,
-    // dS, done, drain, the two tile slots (full, empty)
-    static constexpr int kNumBars = 2 + 2 * kKStages + kVStages + 2 + 4 + 4;
+    // dS (2), done, drain, the two tile slots (full, empty), dQ issued (2)
+    static constexpr int kNumBars = 2 + 2 * kKStages + kVStages + 2 + 5 + 4 + 4;
     static constexpr uint32_t kTmemSlot = kBars + 8 * kNumBars;
     static constexpr uint32_t kTileSlot = kTmemSlot + 8;  // the tile number held by each slot (two ints)
     static constexpr size_t kUsed = kTileSlot + 8 + 16;
@@ -467,7 +480,7 @@ __device__ __forceinline__ DqTile dq_tile(const AttnParams& p, int t) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnBwdThreads, 1)
+__global__ void __launch_bounds__(kAttnDqThreads, 1)
     attn_causal_dq_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_do,
                           const AttnParams p, int* tile_counter) {
     using L = DqSmem<D>;
@@ -487,10 +500,12 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     auto v_empty = [&](uint32_t s) { return bars + 8u * (2 + 2 * NK + s); };
     constexpr int kB = 2 + 2 * NK + NV;
     auto s_full = [&](uint32_t b) { return bars + 8u * (kB + b); };
-    const uint32_t dp_full = bars + 8u * (kB + 2), ds_full = bars + 8u * (kB + 3), done = bars + 8u * (kB + 4),
-                   drain = bars + 8u * (kB + 5);
-    auto tile_full = [&](uint32_t s) { return bars + 8u * (kB + 6 + s); };
-    auto tile_empty = [&](uint32_t s) { return bars + 8u * (kB + 8 + s); };
+    const uint32_t dp_full = bars + 8u * (kB + 2), done = bars + 8u * (kB + 3), drain = bars + 8u * (kB + 4);
+    auto ds_full = [&](uint32_t g) { return bars + 8u * (kB + 5 + (g & 1u)); };
+    auto tile_full = [&](uint32_t s) { return bars + 8u * (kB + 7 + s); };
+    auto tile_empty = [&](uint32_t s) { return bars + 8u * (kB + 9 + s); };
+    auto dq_issued = [&](uint32_t g) { return bars + 8u * (kB + 11 + (g & 1u)); };
+    auto dp_issued = [&](uint32_t g) { return bars + 8u * (kB + 13 + (g & 1u)); };
     const uint32_t tmem_slot = base + L::kTmemSlot;
     volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + L::kTmemSlot);
     volatile int* tile_slot = reinterpret_cast<volatile int*>(smem_raw + L::kTileSlot);
@@ -510,12 +525,14 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
         mbar_init(s_full(0), 1);
         mbar_init(s_full(1), 1);
         mbar_init(dp_full, 1);
-        mbar_init(ds_full, 8);
         mbar_init(done, 1);
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);  // both MMA warps
         for (int s = 0; s < 2; ++s) {
+            mbar_init(ds_full(s), 8);
             mbar_init(tile_full(s), 1);
-            mbar_init(tile_empty(s), 9);  // the MMA warp and the eight row warps
+            mbar_init(tile_empty(s), 10);  // the two MMA warps and the eight row warps
+            mbar_init(dq_issued(s), 1);
+            mbar_init(dp_issued(s), 1);
         }
         mbar_fence_init();
         tma_prefetch_map(&map_qkv);
@@ -597,10 +614,10 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             }
         }
     } else if (warp == 1) {
-        // the whole warp runs the issue loop; its elected lane carries each instruction
+        // ---------------- S and dP products.  The whole warp runs the issue loop;
+        // its elected lane carries each instruction.
         const uint32_t leader = elect_one_sync();
         constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
-        constexpr uint32_t idesc_q = mma_idesc_bf16(128, D, false, true);
         const uint64_t q_desc = kdesc_base(s_q), do_desc = kdesc_base(s_do);
         auto issue_s = [&](uint32_t g) {
             const uint32_t st = g % NK;
@@ -622,6 +639,21 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             umma_commit_elected(leader, dp_full);
             umma_commit_elected(leader, v_empty(st));
         };
+        // S[g] overwrites the S buffer of step g - 2 once the dQ warp has issued
+        // dQ[g - 2], which reads dS[g - 2] from it; dP[g] overwrites dP[g - 1]
+        // once the row warps are done with it.
+        auto may_issue_s = [&](uint32_t g) {
+            if (g < 2) return true;
+            if (!warp_wait(dq_issued(g - 2), ((g - 2) >> 1) & 1u, p.status)) return false;
+            tc_fence_after();
+            return true;
+        };
+        auto may_issue_dp = [&](uint32_t g) {
+            if (g < 1) return true;
+            if (!warp_wait(ds_full(g - 1), ((g - 1) >> 1) & 1u, p.status)) return false;
+            tc_fence_after();
+            return true;
+        };
         uint32_t g = 0;  // steps of this CTA so far, over all its tiles
         bool ok = true;
         for (uint32_t n = 0; ok; ++n) {
@@ -630,32 +662,48 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             const int nk = dq_tile(p, t).nk;
             if (!warp_wait(q_full, n & 1u, p.status)) break;
             tc_fence_after();
-            if (!issue_s(g)) break;
-            issue_dp(g);
-            // Q and dO are free for the next tile once the tile's last S and dP are done
-            if (nk == 1) umma_commit_elected(leader, q_empty);
+            // the MMA order per step is S[g+1], dP[g+1] (here) beside dQ[g] (the dQ warp)
             for (int j = 0; j < nk; ++j, ++g) {
-                // S[j+1] into the other buffer; dP[j+1] once the row warps are done with dP[j]
-                const bool more = j + 1 < nk;
-                if (more && !issue_s(g + 1)) {
+                if (!may_issue_s(g) || !issue_s(g) || !may_issue_dp(g)) {
                     ok = false;
                     break;
                 }
-                if (!warp_wait(ds_full, g & 1u, p.status)) {
+                issue_dp(g);
+                tc_fence_before();
+                if (leader) mbar_arrive(dp_issued(g));
+                // Q and dO are free for the next tile once its last S and dP are done
+                if (j + 1 == nk) umma_commit_elected(leader, q_empty);
+            }
+        }
+        umma_commit_elected(leader, drain);
+        mbar_wait_fast(drain, 0, p.status, kSiteDrain);
+    } else if (warp == kDqWarp) {
+        // ---------------- dQ products: dQ[g] += dS[g] K[g] as soon as the row warps
+        // have packed dS[g]; then the K stage goes back to the producer and the S
+        // warp may overwrite the buffer.
+        const uint32_t leader = elect_one_sync();
+        constexpr uint32_t idesc_q = mma_idesc_bf16(128, D, false, true);
+        uint32_t g = 0;
+        bool ok = true;
+        for (uint32_t n = 0; ok; ++n) {
+            int t;
+            if (!take_tile(n, t) || t < 0) break;
+            const int nk = dq_tile(p, t).nk;
+            for (int j = 0; j < nk; ++j, ++g) {
+                if (!warp_wait(ds_full(g), (g >> 1) & 1u, p.status) ||
+                    (j + 1 < nk && !warp_wait(dp_issued(g + 1), ((g + 1) >> 1) & 1u, p.status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (more) {
-                    issue_dp(g + 1);
-                    if (j + 2 == nk) umma_commit_elected(leader, q_empty);
-                }
                 const uint64_t k_mn = mndesc_base(s_k + (g % NK) * kTile);
 #pragma unroll
                 for (int kk = 0; kk < kRows / 16; ++kk)
                     umma_bf16_ts_elected(leader, t_dq, t_s(g) + packed_col(kk), mndesc_at(k_mn, kk), idesc_q,
                                          (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit_elected(leader, k_empty(g % NK));
+                tc_fence_before();
+                if (leader) mbar_arrive(dq_issued(g));
             }
             if (ok) umma_commit_elected(leader, done);
         }
@@ -725,7 +773,7 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
                 }
                 tmem_wait_store();
                 tc_fence_before();
-                warp_arrive(ds_full, lane);
+                warp_arrive(ds_full(g), lane);
             }
             if (!ok || !warp_wait(done, n & 1u, p.status)) break;
             // group gi stores dQ columns [D/2 gi, D/2 (gi + 1)); the tile's next
@@ -1353,7 +1401,7 @@ cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const
     const int n_tiles = p.n_blocks * s.n_heads;
     cudaError_t e_q = cudaMemsetAsync(side->tiles, 0, sizeof(int), side->stream);
     if (e_q == cudaSuccess) {
-        attn_causal_dq_kernel<D><<<static_cast<unsigned>(std::min(n_tiles, side->sms)), kAttnBwdThreads,
+        attn_causal_dq_kernel<D><<<static_cast<unsigned>(std::min(n_tiles, side->sms)), kAttnDqThreads,
                                    DqSmem<D>::kBytes, side->stream>>>(mq, md, p, side->tiles);
         e_q = cudaGetLastError();
     }
