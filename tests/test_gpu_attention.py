@@ -151,6 +151,25 @@ def test_full_size_one_group():
     assert torch.isfinite(dqkv.float()).all()
 
 
+def test_dq_tiles_outnumber_the_sms():
+    """More (head, query block) tiles than SMs, of mixed lengths (sequences of 1024 tokens: 1 to
+    8 key blocks per tile), so that each CTA of the persistent dQ kernel takes several tiles from
+    its counter, in an order that depends on timing.  Every column of dqkv against the oracle,
+    and three runs bit for bit."""
+    t, nh, nkv, d, seq_len = 4096, 8, 2, 128, 1024
+    rng = np.random.default_rng(13)
+    qkvb, qkv64 = draw_bf16(rng, (t, (nh + 2 * nkv) * d))
+    dab, da64 = draw_bf16(rng, (t, nh * d))
+    qkv, a, lse = run_forward(qkvb, t, nh, nkv, d, seq_len)
+    outs = [run_backward(qkv, a, lse, dab, t, nh, nkv, d, seq_len) for _ in range(3)]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref = S.attention_causal_grad(da64, qkv64, nh, nkv, d, seq_len)
+    got = f64_from_bf16(outs[0])
+    assert_close(got[:, : nh * d], ref[:, : nh * d], "dq")
+    assert_close(got[:, nh * d : (nh + nkv) * d], ref[:, nh * d : (nh + nkv) * d], "dk")
+    assert_close(got[:, (nh + nkv) * d :], ref[:, (nh + nkv) * d :], "dv")
+
+
 CAUSAL_TF = dict(kind="transformer", n_layers=2, hidden=256, ffn=512, n_heads=4, n_kv_heads=2, head_dim=64)
 
 
