@@ -238,6 +238,30 @@ def test_backward_input_many_tiles(t, n_in, n_out):
     assert_close(f64_from_bf16(dx), dy @ w, "backward input, many tiles")
 
 
+@pytest.mark.parametrize("residual", [False, True])
+def test_narrow_last_wave_same_bits(residual):
+    """On 76 CTA pairs, 4096 x 4096 outputs leave a last wave of 28 of 256 tiles, which the GEMM
+    runs as 56 units of 256 x 128; 4352 rows (272 tiles, 44 left over) keep whole tiles.  Every
+    output element takes the same K steps in both, so the first 4096 rows agree bit for bit;
+    both against the float64 product on sampled rows."""
+    n_in, n_out = 512, 4096
+    rng = np.random.default_rng(24)
+    xb, x = draw_bf16(rng, (4352, n_in))
+    wb, w = draw_bf16(rng, (n_out, n_in), 0.05)
+    rb, r = draw_bf16(rng, (4352, n_out))
+    ys = []
+    for t in (4096, 4352):
+        y = empty_bf16(t, n_out)
+        zb.zb_op_linear_forward(bf16_from_bits(xb[:t]), bf16_from_bits(wb), bf16_from_bits(rb[:t]) if residual else None,
+                                y, t, n_in, n_out)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0], ys[1][:4096])
+    rows = np.sort(np.append(rng.choice(4096, 31, replace=False), 4095))
+    ref = x[rows] @ w.T + (r[rows] if residual else 0.0)
+    assert_close(f64_from_bf16(ys[0])[rows], ref, "narrow last wave, sampled rows")
+
+
 @pytest.mark.parametrize("t,n_in,n_out", [(300, 4096, 4096), (129, 4032, 4000 // 64 * 64)])
 def test_backward_weight_many_tiles(t, n_in, n_out):
     rng = np.random.default_rng(22)
