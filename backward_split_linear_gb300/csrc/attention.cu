@@ -7,14 +7,16 @@
 // ("Zero-Bubble Pipeline Parallelism Guide for LLMs", "Core Innovation 1");
 // the core has no weights, so all of its backward belongs to B.
 //
-// Three kernels on 128-row tiles (the forward and dK/dV one CTA per tile, dQ
-// persistent with one CTA per SM):
+// Three kernels on 128-row tiles (the forward one CTA per tile, or per two
+// tiles of one kv group; dK/dV one CTA per tile; dQ persistent with one CTA
+// per SM):
 //   warp 0     one thread issues TMA loads
 //   warp 1     allocates tensor memory; the whole warp runs the MMA issue loop
 //              and its elected lane carries each tcgen05.mma and commit
 //   warps 2-5  one row each: softmax / gradient arithmetic, epilogue
 //   warps 6-9  (backward kernels) a second group of row warps, on the other
-//              64 columns of every 128-wide step
+//              64 columns of every 128-wide step; (two-tile forward) the
+//              softmax warps of the second tile
 //   warp 10    (dK/dV) the statistics warp: lse and D of each step's queries
 //              into the B operand of the score products' extra K step;
 //              (dQ) a second MMA warp, for the dQ products
@@ -310,22 +312,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             const int k0 = (kb0 + j) * kRows;
             const int lim = min(q - k0, s1 - 1 - k0);  // last visible key column of this row
-            float mx = -INFINITY;
+            // eight running maxima and sums, not one chain of 128 dependent operations
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
             if (__all_sync(0xffffffffu, lim >= 127)) {  // below the diagonal: no mask
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     s[c] *= p.scale_log2;
-                    mx = fmaxf(mx, s[c]);
+                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
                 }
             } else {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     // -inf where masked, by bit operations (no branch per element)
-                    const uint32_t m = 0u - static_cast<uint32_t>(c <= lim);
-                    s[c] = __uint_as_float((__float_as_uint(s[c] * p.scale_log2) & m) | (0xff800000u & ~m));
-                    mx = fmaxf(mx, s[c]);
+                    const uint32_t mk = 0u - static_cast<uint32_t>(c <= lim);
+                    s[c] = __uint_as_float((__float_as_uint(s[c] * p.scale_log2) & mk) | (0xff800000u & ~mk));
+                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
                 }
             }
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             if (j > 0 && !warp_wait(p_free, (j - 1) & 1, p.status)) {
                 ok = false;
                 break;
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 m = m_new;
             }
-            float sum = 0.f;
+            float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t w[16];
@@ -360,12 +367,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int e = 0; e < 16; ++e) {
                     const float a = ex2(s[32 * c + 2 * e] - m);
                     const float b = ex2(s[32 * c + 2 * e + 1] - m);
-                    sum += a + b;
+                    sum8[e & 7] += a + b;
                     w[e] = pack_bf16x2(a, b);
                 }
                 tmem_store_16(tmem_base + t_row + sb * 128 + 16 * c, w);
             }
-            l += sum;
+            l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             tmem_wait_store();
             tc_fence_before();
             warp_arrive(p_full, lane);
@@ -409,6 +416,271 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // a 128-column buffer into its first 32: group kk / 4 at 64 (kk / 4), then 8
 // columns per K step.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3)); }
+
+// Two query heads of one kv group per CTA: the same query block and the same
+// keys, tile A head h0 and tile B head h0 + 1.  Each tile has one score buffer
+// and one O accumulator (the four 128-column regions of tensor memory) and a
+// group of four softmax warps of its own.  The MMA order per key block j is
+// PV_A[j], S_A[j+1], PV_B[j], S_B[j+1]: one group's softmax over block j runs
+// while the other tile's products run.  (With one tile per CTA the four
+// softmax warps held the kernel: the tensor pipe was 46 % active.)  S_X[j+1]
+// reuses the columns P_X[j] was packed into, after PV_X[j] in issue order, and
+// when S_X[j] completes PV_X[j-1] has too, so the softmax rescales O_X without
+// a further wait.  Used when the group has an even number of heads.
+template <int D>
+struct FwdPairSmem {
+    static constexpr int kStages = 2;
+    static constexpr uint32_t kTile = D * 256;
+    static constexpr uint32_t kQ = 0;           // Q of tile A, then Q of tile B
+    static constexpr uint32_t kKV = 2 * kTile;  // stage s: K at kKV + 2 s kTile, V after it
+    static constexpr uint32_t kBars = kKV + 2 * kStages * kTile;
+    static constexpr size_t kUsed = 1024 + kBars + 16 * 8;
+    static constexpr size_t kBytes = kUsed > kMinSmem ? kUsed : kMinSmem;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnBwdThreads, 1)
+    attn_causal_fwd_pair_kernel(const __grid_constant__ CUtensorMap map_qkv, const AttnParams p) {
+    using L = FwdPairSmem<D>;
+    constexpr int NS = L::kStages;
+    constexpr uint32_t kTile = L::kTile;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t s_q = base + L::kQ, s_kv = base + L::kKV;
+    const uint32_t bars = base + L::kBars;
+    const uint32_t q_full = bars;
+    auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bars + 8u * (1 + NS + s); };
+    auto s_full = [&](int x) { return bars + 8u * (1 + 2 * NS + x); };
+    auto p_full = [&](int x) { return bars + 8u * (3 + 2 * NS + x); };
+    const uint32_t done = bars + 8u * (5 + 2 * NS), drain = bars + 8u * (6 + 2 * NS);
+    const uint32_t tmem_slot = bars + 8u * (7 + 2 * NS);
+    volatile uint32_t* tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pairs = p.n_heads / 2;
+    const int qb = p.n_blocks - 1 - static_cast<int>(blockIdx.x) / pairs;  // longest rows first
+    const int h0 = 2 * (static_cast<int>(blockIdx.x) % pairs);
+    const int g = h0 / (p.n_heads / p.n_kv_heads);
+    const int q0 = qb * kRows;
+    int s0, s1;
+    seq_bounds(p, q0, s0, s1);
+    const int kb0 = s0 / kRows;
+    const int nk = qb - kb0 + 1;
+    const int kcol = (p.n_heads + g) * D, vcol = (p.n_heads + p.n_kv_heads + g) * D;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(p_full(x), 4);
+        }
+        mbar_init(done, 1);
+        mbar_init(drain, 1);
+        mbar_fence_init();
+        tma_prefetch_map(&map_qkv);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+    // columns: S_A 0-127, S_B 128-255 (P packed into the first 64 columns of its
+    // buffer once read), O_A 256.., O_B 384..
+    auto t_s = [&](int x) { return tmem_base + 128u * static_cast<uint32_t>(x); };
+    auto t_o = [&](int x) { return tmem_base + 256u + 128u * static_cast<uint32_t>(x); };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, 2 * kTile);
+            load_tile<D>(s_q, &map_qkv, q_full, h0 * D, q0);
+            load_tile<D>(s_q + kTile, &map_qkv, q_full, (h0 + 1) * D, q0);
+            uint32_t n_fills = 0;
+            for (int j = 0; j < nk; ++j) {
+                const int st = j % NS;
+                if (!mbar_wait_fast(kv_empty(st), ((j / NS) & 1) ^ 1u, p.status, kSiteAttn)) break;
+                mbar_arrive_expect_tx(kv_full(st), 2 * kTile);
+                const int k0 = (kb0 + j) * kRows;
+                load_tile<D>(s_kv + 2 * st * kTile, &map_qkv, kv_full(st), kcol, k0);
+                load_tile<D>(s_kv + (2 * st + 1) * kTile, &map_qkv, kv_full(st), vcol, k0);
+                ++n_fills;
+            }
+            mbar_wait_fast(q_full, 0, p.status, kSiteDrain);
+            for (int s = 0; s < NS; ++s) {
+                const uint32_t u = ring_uses(n_fills, NS, s);
+                if (u > 0) mbar_wait_fast(kv_full(s), (u - 1) & 1, p.status, kSiteDrain);
+            }
+        }
+    } else if (warp == 1) {
+        // the whole warp runs the issue loop; its elected lane carries each instruction
+        const uint32_t leader = elect_one_sync();
+        constexpr uint32_t idesc_s = mma_idesc_bf16(128, 128, false, false);
+        constexpr uint32_t idesc_o = mma_idesc_bf16(128, D, false, true);
+        auto issue_s = [&](int x, int j) {
+            const int st = j % NS;
+            const uint64_t a_desc = kdesc_base(s_q + static_cast<uint32_t>(x) * kTile),
+                           b_desc = kdesc_base(s_kv + 2 * st * kTile);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                umma_bf16_elected(leader, t_s(x), kdesc_at(a_desc, kk), kdesc_at(b_desc, kk), idesc_s, kk > 0);
+            umma_commit_elected(leader, s_full(x));
+        };
+        auto issue_pv = [&](int x, int j) {
+            if (!warp_wait(p_full(x), j & 1, p.status)) return false;
+            tc_fence_after();
+            const uint64_t v_desc = mndesc_base(s_kv + (2 * (j % NS) + 1) * kTile);
+#pragma unroll
+            for (int kk = 0; kk < kRows / 16; ++kk)
+                umma_bf16_ts_elected(leader, t_o(x), t_s(x) + 8 * kk, mndesc_at(v_desc, kk), idesc_o,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+            return true;
+        };
+        auto kv_ready = [&](int j) {
+            if (!warp_wait(kv_full(j % NS), (j / NS) & 1, p.status)) return false;
+            tc_fence_after();
+            return true;
+        };
+        bool ok = warp_wait(q_full, 0, p.status) && kv_ready(0);
+        if (ok) {
+            issue_s(0, 0);
+            issue_s(1, 0);
+        }
+        for (int j = 0; ok && j < nk; ++j) {
+            const bool more = j + 1 < nk;
+            if (!issue_pv(0, j) || (more && !kv_ready(j + 1))) break;
+            if (more) issue_s(0, j + 1);
+            if (!issue_pv(1, j)) break;
+            umma_commit_elected(leader, kv_empty(j % NS));
+            if (more) issue_s(1, j + 1);
+        }
+        umma_commit_elected(leader, done);
+        umma_commit_elected(leader, drain);
+        mbar_wait_fast(drain, 0, p.status, kSiteDrain);
+    } else {
+        // ---------------- softmax rows: warps 2-5 tile A, warps 6-9 tile B
+        const int x = (warp - 2) >> 2;
+        const int h = h0 + x;
+        const int qw = warp & 3;
+        const int row = qw * 32 + lane;
+        const int q = q0 + row;
+        const uint32_t t_row = static_cast<uint32_t>(qw * 32) << 16;
+        const uint32_t ts = t_s(x), to = t_o(x);
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nk && ok; ++j) {
+            if (!warp_wait(s_full(x), j & 1, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[128];
+            {
+                uint32_t r[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_load_32(ts + t_row + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
+                tmem_wait_load();
+#pragma unroll
+                for (int e = 0; e < 128; ++e) s[e] = __uint_as_float(r[e]);
+            }
+            const int k0 = (kb0 + j) * kRows;
+            const int lim = min(q - k0, s1 - 1 - k0);  // last visible key column of this row
+            // eight running maxima and sums, not one chain of 128 dependent operations
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+            if (__all_sync(0xffffffffu, lim >= 127)) {  // below the diagonal: no mask
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    s[c] *= p.scale_log2;
+                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    // -inf where masked, by bit operations (no branch per element)
+                    const uint32_t mk = 0u - static_cast<uint32_t>(c <= lim);
+                    s[c] = __uint_as_float((__float_as_uint(s[c] * p.scale_log2) & mk) | (0xff800000u & ~mk));
+                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                }
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            if (j == 0) {
+                m = mx;
+            } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
+                // A row's maximum rose far above its reference: the warp rescales
+                // O and l of all its rows to their new maxima (warp-wide
+                // tensor-memory loads and stores; rescaling to any larger
+                // reference is exact).  PV_X[j-1] completed before S_X[j].
+                const float m_new = fmaxf(m, mx);
+                const float alpha = ex2(m - m_new);
+                l *= alpha;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_load_32(to + t_row + 32 * c, r);
+                    tmem_wait_load();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    tmem_store_32(to + t_row + 32 * c, r);
+                }
+                m = m_new;
+            }
+            float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float a = ex2(s[32 * c + 2 * e] - m);
+                    const float b = ex2(s[32 * c + 2 * e + 1] - m);
+                    sum8[e & 7] += a + b;
+                    w[e] = pack_bf16x2(a, b);
+                }
+                tmem_store_16(ts + t_row + 16 * c, w);
+            }
+            l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+            tmem_wait_store();
+            tc_fence_before();
+            warp_arrive(p_full(x), lane);
+        }
+        if (ok && warp_wait(done, 0, p.status)) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            const bool valid = q < s1;
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<int64_t>(q) * p.ld_out + h * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_load_32(to + t_row + 32 * c, r);
+                tmem_wait_load();
+                if (valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        d4[k] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
+                                           pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
+                                           pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
+                                           pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
+                }
+            }
+            if (valid) p.lse[static_cast<int64_t>(h) * p.ld_stat + q] = m + lg2(l);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
 
 // ------------------------------------------------------------------------ backward: dq
 
@@ -1306,7 +1578,10 @@ template <int D>
 cudaError_t fwd_launch(const AttnShape& s, const void* qkv, void* a, float* lse, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] { err = set_smem(attn_causal_fwd_kernel<D>, FwdSmem<D>::kBytes); });
+    std::call_once(once, [] {
+        err = set_smem(attn_causal_fwd_kernel<D>, FwdSmem<D>::kBytes);
+        if (err == cudaSuccess) err = set_smem(attn_causal_fwd_pair_kernel<D>, FwdPairSmem<D>::kBytes);
+    });
     if (err != cudaSuccess) return err;
     const int qkv_w = (s.n_heads + 2 * s.n_kv_heads) * D;
     CUtensorMap m;
@@ -1316,7 +1591,11 @@ cudaError_t fwd_launch(const AttnShape& s, const void* qkv, void* a, float* lse,
     p.out = a;
     p.ld_out = static_cast<int64_t>(s.n_heads) * D;
     p.lse = lse;
-    attn_causal_fwd_kernel<D><<<p.n_blocks * s.n_heads, kAttnThreads, FwdSmem<D>::kBytes, stream>>>(m, p);
+    if ((s.n_heads / s.n_kv_heads) % 2 == 0)  // two heads of a group per CTA
+        attn_causal_fwd_pair_kernel<D><<<p.n_blocks * (s.n_heads / 2), kAttnBwdThreads, FwdPairSmem<D>::kBytes,
+                                          stream>>>(m, p);
+    else
+        attn_causal_fwd_kernel<D><<<p.n_blocks * s.n_heads, kAttnThreads, FwdSmem<D>::kBytes, stream>>>(m, p);
     return cudaGetLastError();
 }
 
