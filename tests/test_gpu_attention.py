@@ -78,23 +78,25 @@ def test_forward_and_backward(t, nh, nkv, d, seq_len):
     assert_close(got[:, w + kw:], ref[:, w + kw:], "dv")
 
 
+@pytest.mark.parametrize("nh", [1, 2])
 @pytest.mark.parametrize("d", [64, 128])
-def test_rescale_when_row_maxima_rise(d):
+def test_rescale_when_row_maxima_rise(d, nh):
     """Scores that grow with the key index make a row's maximum rise by far more than the
     forward's rescale threshold from one key block to the next, for every other query row
     (the rows in between see falling scores): the rescale runs in some rows of a warp and
     not in others.  Checked: a and the row statistic (what the rescale touches) and dv.
     dq and dk are left out on this input: its softmax rows are nearly one-hot, so dS =
     P (dP - D) cancels almost exactly, and D = rowsum(dO * O) from the bf16 output alone
-    moves dq by about 5e-2 relative (a float64 replay of that rounding gives the same)."""
-    t, nh, nkv = 1024, 2, 1
+    moves dq by about 5e-2 relative (a float64 replay of that rounding gives the same).
+    One head runs the one-tile forward, two heads of one kv head the two-tile forward."""
+    t, nkv = 1024, 1
     rng = np.random.default_rng(31 + d)
     u = np.ones(d)
     sign = np.where(np.arange(t) % 2 == 0, 1.0, -1.0)
     q = sign[:, None] * u[None, :] + 0.05 * rng.standard_normal((t, d))
     k = (5.0 * np.arange(t) / t)[:, None] * u[None, :] + 0.05 * rng.standard_normal((t, d))
     v = rng.standard_normal((t, d))
-    qkv64 = np.concatenate([q, q, k, v], axis=1)
+    qkv64 = np.concatenate([q] * nh + [k, v], axis=1)
     qkvb = synth.bf16_bits(qkv64.astype(np.float32))
     qkv64 = synth.bf16_to_f64(qkvb)
     dab, da64 = draw_bf16(rng, (t, nh * d))
