@@ -165,20 +165,20 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_bwd_kernel(
 // chunk of 8 columns) streams tokens t0 + g, t0 + g + 8, ... of that range,
 // four tokens of loads in flight; the 8 row groups are then added in order
 // g = 0..7 in shared memory and the block writes part[cy][256 columns].
-// `parts` depends only on T and H (about 320 blocks in all), never on the
+// `parts` depends only on T and H (about 512 blocks in all), never on the
 // device, so the partition and hence the float32 sums are reproducible.
 // Pass 2: dgamma[j] += part[0][j] + part[1][j] + ... in order.
 constexpr int kGammaCols = 256;                           // columns per block
 constexpr int kGammaChunks = kGammaCols / 8;              // 32 threads across the columns
 constexpr int kGammaGroups = kRowThreads / kGammaChunks;  // 8 row groups
-constexpr int kGammaTargetBlocks = 320;
+constexpr int kGammaTargetBlocks = 512;
 constexpr int kGammaUnroll = 4;
 
-// parts = min(ceil(320 / column blocks), ceil(T / 8), 2^17 / H), at least 1.
+// parts = min(ceil(512 / column blocks), ceil(T / 8), 2^17 / H), at least 1.
 // The last bound keeps the partial sums (parts * H floats) within 2^17 floats
 // for every H <= 2^17, whatever T: a fixed 512 KiB buffer then serves every
-// token count of those widths.  At H <= 16384 it never binds (the first bound
-// is smaller), so the partition of the stage's widths is unaffected.
+// token count of those widths.  Up to H = 16384 it is never below the first
+// bound, so it does not change the partition of the stage's widths.
 int gamma_parts(int tokens, int hidden) {
     const int col_blocks = (hidden + kGammaCols - 1) / kGammaCols;
     const int want = (kGammaTargetBlocks + col_blocks - 1) / col_blocks;
