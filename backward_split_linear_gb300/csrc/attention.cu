@@ -697,10 +697,10 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
 // V through two, on one barrier per step.
 //
 // Two warps issue the MMAs: warp 1 the S and dP products, warp 10 the dQ
-// products.  With one issuing warp, every wait and commit between two batches
-// of 128 x 128 products left the tensor pipe idle (its queue holds little more
-// than one such product), about a quarter of each step; with two, one warp's
-// waits run while the other's products execute.  The warps order their
+// products.  With one issuing warp, the waits and commits between batches of
+// 128 x 128 products left the tensor pipe idle for about a quarter of each
+// step (a timed copy that observed every batch's completion); with two, one
+// warp's waits run while the other's products execute.  The warps order their
 // products through two barriers: S[j+2] reuses the buffer that dQ[j] reads,
 // so warp 1 issues it after warp 10 has issued dQ[j]; and warp 10 issues
 // dQ[j] after warp 1 has issued dP[j+1], which the row warps wait for.
