@@ -1119,7 +1119,9 @@ struct DkvSmem {
     static constexpr uint32_t kAug = kOnes + 2 * kAugTile;      // stage s: the B operand of step s
     static constexpr uint32_t kStat = kAug + kAugStages * kAugTile;  // stage s: lse (512 bytes) then D (512 bytes)
     static constexpr uint32_t kBars = kStat + 1024 * kStatStages;
-    static constexpr int kNumBars = 1 + 2 * (kQStages + kStatStages) + kDoStages + kAugStages + 8;
+    // kv full; Q (with dO and statistics) full / empty; statistics full / empty;
+    // statistics operand empty; S^T, dP^T, P^T and dS^T chunks, done, drain
+    static constexpr int kNumBars = 1 + 2 * (kQStages + kStatStages) + kAugStages + 8;
     static constexpr size_t kBytes = kBars + 8 * kNumBars + 16;
 };
 constexpr int kAttnDkvThreads = kAttnBwdThreads + 32;  // + the statistics warp
@@ -1166,12 +1168,13 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
     const uint32_t bars = base + L::kBars;
     const uint32_t kv_full = bars;
     auto q_full = [&](int s) { return bars + 8u * (1 + s); };
+    // q_empty(s) releases Q, dO (same ring position, ND == NQ) and nothing else
     auto q_empty = [&](int s) { return bars + 8u * (1 + NQ + s); };
-    auto do_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + s); };
-    auto st_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + s); };
-    auto st_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + NT + s); };
-    auto aug_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + ND + 2 * NT + s); };
-    constexpr int kB = 1 + 2 * (NQ + NT) + ND + NA;
+    auto st_full = [&](int s) { return bars + 8u * (1 + 2 * NQ + s); };
+    auto st_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + NT + s); };
+    auto aug_empty = [&](int s) { return bars + 8u * (1 + 2 * NQ + 2 * NT + s); };
+    constexpr int kB = 1 + 2 * (NQ + NT) + NA;
+    static_assert(NQ == ND, "Q and dO share their ring position and release");
     // p_full(c) / ds_full(c): chunk c (32 query columns of each group) of P^T / dS^T is packed
     auto p_full = [&](int c) { return bars + 8u * (kB + 2 + c); };
     auto ds_full = [&](int c) { return bars + 8u * (kB + 4 + c); };
@@ -1211,7 +1214,6 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
             mbar_init(q_full(s), 2);  // the Q and dO tiles' TMA and the statistics warp's B operand
             mbar_init(q_empty(s), 1);
         }
-        for (int s = 0; s < ND; ++s) mbar_init(do_empty(s), 1);
         for (int s = 0; s < NT; ++s) {
             mbar_init(st_full(s), 1);
             mbar_init(st_empty(s), 1);
@@ -1256,8 +1258,8 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
                 ++nt;
                 // Q[i] and dO[i] land on one barrier (with the statistics operand):
                 // one wait per step for the MMA warp
+                // one release covers the Q and dO stages (dK[i - 2], after dV[i - 2], read the last of them)
                 if (!mbar_wait_fast(q_empty(i % NQ), ((i / NQ) & 1) ^ 1u, p.status, kSiteAttn)) break;
-                if (!mbar_wait_fast(do_empty(i % ND), ((i / ND) & 1) ^ 1u, p.status, kSiteAttn)) break;
                 mbar_arrive_expect_tx(q_full(i % NQ), 2 * kTile);
                 load_tile<D>(s_q + (i % NQ) * kTile, &map_qkv, q_full(i % NQ), h * D, r0);
                 load_tile<D>(s_do + (i % ND) * kTile, &map_do, q_full(i % NQ), h * D, r0);
@@ -1325,7 +1327,6 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
                 }
             }
             if (!ok) break;
-            umma_commit_elected(leader, do_empty(i % ND));
             // S^T[i+1] overwrites the S^T buffer after dV[i] has read P^T[i] from it
             if (i + 1 < n_steps && !issue_s(i + 1)) break;
             const uint64_t q_mn = mndesc_base(s_q + (i % NQ) * kTile);
@@ -1344,6 +1345,7 @@ __global__ void __launch_bounds__(kAttnDkvThreads, 1)
                 }
             }
             if (!ok) break;
+            // Q[i] and dO[i]: dK[i] is the last product that reads either
             umma_commit_elected(leader, q_empty(i % NQ));
             if (i + 1 < n_steps && !issue_dp(i + 1)) break;
         }
