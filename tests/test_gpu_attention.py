@@ -3,7 +3,8 @@
 Per-step ops on seeded bf16 inputs: the forward (a and the row statistics it
 keeps) and the backward (dq, dk, dv).  Shapes cover one and several 128-row
 blocks, ragged token counts, sequences shorter than the microbatch, grouped
-K/V heads and both head sizes.  The backward reads the GPU forward's a and
+K/V heads (groups of 1, 2, 3, 4 and 8 query heads: odd groups run the
+one-tile forward, even ones the two-tile forward) and both head sizes.  The backward reads the GPU forward's a and
 row statistics, as the stage does.  Bar per step: relative Frobenius <= 5e-3,
 max-abs <= 2e-2 max|ref| (tests/parity.py).
 """
@@ -46,7 +47,7 @@ def run_backward(qkv, a, lse, dab, t, nh, nkv, d, seq_len):
 
 
 SHAPES = [(300, 4, 2, 64, 0), (512, 4, 1, 128, 256), (77, 2, 1, 128, 0), (640, 8, 2, 64, 128),
-          (1, 2, 2, 64, 0), (384, 2, 2, 128, 128)]
+          (1, 2, 2, 64, 0), (384, 2, 2, 128, 128), (384, 16, 2, 128, 0), (200, 6, 2, 64, 0)]
 
 
 @pytest.mark.parametrize("t,nh,nkv,d,seq_len", SHAPES)
