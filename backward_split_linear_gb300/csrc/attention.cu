@@ -316,23 +316,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             float mx8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+            // the maximum of the raw scores (the scale is positive), the scale
+            // folded into the exponent's FMA below
             if (__all_sync(0xffffffffu, lim >= 127)) {  // below the diagonal: no mask
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    s[c] *= p.scale_log2;
-                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                }
+                for (int c = 0; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
             } else {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     // -inf where masked, by bit operations (no branch per element)
                     const uint32_t mk = 0u - static_cast<uint32_t>(c <= lim);
-                    s[c] = __uint_as_float((__float_as_uint(s[c] * p.scale_log2) & mk) | (0xff800000u & ~mk));
+                    s[c] = __uint_as_float((__float_as_uint(s[c]) & mk) | (0xff800000u & ~mk));
                     mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
                 }
             }
             const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
             if (j > 0 && !warp_wait(p_free, (j - 1) & 1, p.status)) {
                 ok = false;
                 break;
@@ -365,8 +364,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float a = ex2(s[32 * c + 2 * e] - m);
-                    const float b = ex2(s[32 * c + 2 * e + 1] - m);
+                    const float a = ex2(fmaf(s[32 * c + 2 * e], p.scale_log2, -m));
+                    const float b = ex2(fmaf(s[32 * c + 2 * e + 1], p.scale_log2, -m));
                     sum8[e & 7] += a + b;
                     w[e] = pack_bf16x2(a, b);
                 }
@@ -594,23 +593,22 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
             float mx8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+            // the maximum of the raw scores (the scale is positive), the scale
+            // folded into the exponent's FMA below
             if (__all_sync(0xffffffffu, lim >= 127)) {  // below the diagonal: no mask
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    s[c] *= p.scale_log2;
-                    mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                }
+                for (int c = 0; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
             } else {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     // -inf where masked, by bit operations (no branch per element)
                     const uint32_t mk = 0u - static_cast<uint32_t>(c <= lim);
-                    s[c] = __uint_as_float((__float_as_uint(s[c] * p.scale_log2) & mk) | (0xff800000u & ~mk));
+                    s[c] = __uint_as_float((__float_as_uint(s[c]) & mk) | (0xff800000u & ~mk));
                     mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
                 }
             }
             const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
             if (j == 0) {
                 m = mx;
             } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
@@ -638,8 +636,8 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float a = ex2(s[32 * c + 2 * e] - m);
-                    const float b = ex2(s[32 * c + 2 * e + 1] - m);
+                    const float a = ex2(fmaf(s[32 * c + 2 * e], p.scale_log2, -m));
+                    const float b = ex2(fmaf(s[32 * c + 2 * e + 1], p.scale_log2, -m));
                     sum8[e & 7] += a + b;
                     w[e] = pack_bf16x2(a, b);
                 }
