@@ -29,13 +29,14 @@ def _case(rng, t, hidden):
 @pytest.mark.gpu
 def test_noalloc_matches_scratch_entry_point_twice(cuda_device):
     rng = np.random.default_rng(123)
-    # Calls in a row with different sizes.  The first fills 20 x 4096 partial
+    # Calls in a row with different sizes.  The first fills 32 x 4096 partial
     # sums of the shared array, the second only 8 x 4096: partials the first
     # call left beyond the second's range would show up if the second read
     # them.  The third is the widest row whose partition still took two parts
     # per column before the partition was capped to the array (hidden 65600).
     cases = ((4096, 4096), (64, 4096), (200, 65600))
-    assert zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(64, 4096) < zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(4096, 4096)
+    assert zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(4096, 4096) == 32 * 4096 * 4
+    assert zb.zb_op_rmsnorm_backward_gamma_scratch_bytes(64, 4096) == 8 * 4096 * 4
     for t, hidden in cases:
         dn, x, rstd = _case(rng, t, hidden)
         init = torch.from_numpy(rng.standard_normal(hidden).astype(np.float32)).cuda()
