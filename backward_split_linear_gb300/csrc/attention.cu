@@ -24,6 +24,9 @@
 //   attn_causal_fwd_kernel   (head h, query block):  S = Q K^T -> online softmax ->
 //                     O += P V over the key blocks up to the diagonal; writes
 //                     a and the row log-sum-exp (base 2) for the backward.
+//   attn_causal_fwd_pair_kernel  the same for two heads of one kv group and
+//                     one query block, when the group has an even number of
+//                     heads: the two tiles share every K / V load.
 //   attn_causal_dkdv_kernel  (kv head j, key block): for every query head of group j
 //                     and every query block from the diagonal on:
 //                     S^T = K Q^T, dP^T = V dO^T, P^T = exp2(S^T c - lse),
