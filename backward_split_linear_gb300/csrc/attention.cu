@@ -45,6 +45,11 @@
 // descriptor, as an MN-major one (contraction over its 128 rows).  P and dS
 // stay in tensor memory: each row thread packs them to bf16 over the score
 // columns it has read, and the next product takes them as its A operand.
+// A later score product then overwrites those columns with no wait for the
+// reading product to complete. That relies on the tensor cores executing a
+// CTA's MMAs in the order they were issued. The PTX ISA promises this only
+// for MMAs of the same accumulator and shape, so it is an assumption about
+// the hardware. The full-size parity tests cover every such reuse.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
