@@ -129,6 +129,26 @@ def test_backward_bitwise_reproducible():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
+def test_full_size_bitwise_reproducible():
+    """The 8B-shaped layer (4096 tokens, 32 heads on 8 kv heads, d = 128) run again and again:
+    every launch gives the same bits.  The kernels reuse tensor-memory columns that an
+    earlier product reads without waiting for it to complete; an MMA that ran out of issue
+    order would change results from one launch to the next."""
+    t, nh, nkv, d = 4096, 32, 8, 128
+    rng = np.random.default_rng(21)
+    qkvb, _ = draw_bf16(rng, (t, (nh + 2 * nkv) * d))
+    dab, _ = draw_bf16(rng, (t, nh * d))
+    qkv, a, lse = run_forward(qkvb, t, nh, nkv, d, 0)
+    for _ in range(4):
+        _, a2, lse2 = run_forward(qkvb, t, nh, nkv, d, 0)
+        assert torch.equal(a.view(torch.int16), a2.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    first = run_backward(qkv, a, lse, dab, t, nh, nkv, d, 0).view(torch.int16)
+    for _ in range(9):
+        assert torch.equal(first, run_backward(qkv, a, lse, dab, t, nh, nkv, d, 0).view(torch.int16))
+    assert torch.isfinite(a.float()).all() and torch.isfinite(first.view(torch.bfloat16).float()).all()
+
+
 def test_full_size_one_group():
     """The 8B-shaped layer's attention at 4096 tokens (32 heads on 8 kv heads, d = 128), in
     the launch configuration the stage uses.  Groups are independent, so the oracle follows
