@@ -47,7 +47,9 @@ def run_backward(qkv, a, lse, dab, t, nh, nkv, d, seq_len):
 
 
 SHAPES = [(300, 4, 2, 64, 0), (512, 4, 1, 128, 256), (77, 2, 1, 128, 0), (640, 8, 2, 64, 128),
-          (1, 2, 2, 64, 0), (384, 2, 2, 128, 128), (384, 16, 2, 128, 0), (200, 6, 2, 64, 0)]
+          (1, 2, 2, 64, 0), (384, 2, 2, 128, 128), (384, 16, 2, 128, 0), (200, 6, 2, 64, 0),
+          # the last sequence shorter than seq_len and the token count off the 128-row grid
+          (700, 8, 2, 128, 256), (450, 6, 3, 64, 128)]
 
 
 @pytest.mark.parametrize("t,nh,nkv,d,seq_len", SHAPES)
