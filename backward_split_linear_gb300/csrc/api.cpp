@@ -138,6 +138,32 @@ zb_status run_backward_input(const void* dy, const void* w, void* dx, int t, int
     return cuda_status(zbk::launch_gemm(g, s));
 }
 
+// dx = dy w, and per row and head the attention backward's D = rowsum(dx * a)
+// from the stored bf16 dx (CTA-pair GEMMs only: gemm_takes_pair(t, in)).
+zb_status run_backward_input_rowdot(const void* dy, const void* w, void* dx, const void* a, float* dvec,
+                                    int64_t ld_stat, int head_dim, int t, int in, int out, cudaStream_t s,
+                                    const SplitWs* ws) {
+    GemmArgs g{};
+    g.kind = GemmKind::BackwardInput;
+    g.epi = Epilogue::StoreBf16RowDot;
+    g.a = dy;
+    g.lda = out;
+    g.b = w;
+    g.ldb = in;
+    g.m = t;
+    g.n = in;
+    g.k = out;
+    g.out = dx;
+    g.ldo = in;
+    g.aux = a;
+    g.ld_aux = in;
+    g.dot = dvec;
+    g.ld_dot = ld_stat;
+    g.dot_cols = head_dim;
+    set_split(g, ws);
+    return cuda_status(zbk::launch_gemm(g, s));
+}
+
 zb_status run_backward_input_swiglu(const void* dy, const void* w_down, const void* gu, void* dgu,
                                     int t, int hidden, int ffn, cudaStream_t s, const SplitWs* ws = nullptr) {
     GemmArgs g{};
@@ -833,17 +859,26 @@ zb_status stage_backward_input_body(zb_stage* st, int slot, const void* dy, void
             const double kv = static_cast<double>(c.n_kv_heads) * c.head_dim;
             if (c.attention == ZB_ATTN_CAUSAL) {
                 // a3: output projection B into a temporary, then the attention backward
-                // (rowsum, dK/dV, dQ) writes every column of dqkv
+                // (dK/dV, dQ) writes every column of dqkv.  D = rowsum(da * a) per
+                // head comes from the GEMM's epilogue when the CTA-pair kernel
+                // takes it, else from a row kernel before dK/dV and dQ.
                 void* da = st->ws + st->lay.da_tmp;
-                ZB_TRY(traced(st, ZB_KCLASS_GEMM_BACKWARD_INPUT, 1, gemm_flops(T, H, H), dgrad_bytes(T, H, H), s,
-                              [&] { return run_backward_input(dh, p.w_o, da, t, H, H, H, s, &ws); }));
+                float* dvec = reinterpret_cast<float*>(st->ws + st->lay.dvec);
+                const bool d_in_gemm = zbk::gemm_takes_pair(t, H);
+                ZB_TRY(traced(st, ZB_KCLASS_GEMM_BACKWARD_INPUT, 1, gemm_flops(T, H, H),
+                              dgrad_bytes(T, H, H) + (d_in_gemm ? 2.0 * T * H + 4.0 * T * c.n_heads : 0.0), s, [&] {
+                                  return d_in_gemm ? run_backward_input_rowdot(dh, p.w_o, da, st->at(slot, L.a), dvec,
+                                                                               st->lay.ld_stat, c.head_dim, t, H, H,
+                                                                               s, &ws)
+                                                   : run_backward_input(dh, p.w_o, da, t, H, H, H, s, &ws);
+                              }));
                 const double pairs = causal_pairs(t, c.seq_len) * c.n_heads;
-                ZB_TRY(traced(st, ZB_KCLASS_ATTN_BACKWARD, 3, 10.0 * c.head_dim * pairs,
-                              2.0 * T * (2.0 * Q + 2.0 * H) + 8.0 * T * c.n_heads, s, [&] {
+                ZB_TRY(traced(st, ZB_KCLASS_ATTN_BACKWARD, d_in_gemm ? 2 : 3, 10.0 * c.head_dim * pairs,
+                              2.0 * T * (2.0 * Q + (d_in_gemm ? 1.0 : 2.0) * H) + 8.0 * T * c.n_heads, s, [&] {
                                   return cuda_status(zbk::launch_attention_causal_backward(
                                       attn_shape(t, c.n_heads, c.n_kv_heads, c.head_dim, c.seq_len, st->lay.ld_stat),
-                                      st->at(slot, L.qkv), st->at(slot, L.a), da, st->at<float>(slot, L.lse),
-                                      reinterpret_cast<float*>(st->ws + st->lay.dvec), dqkv, s));
+                                      st->at(slot, L.qkv), st->at(slot, L.a), da, st->at<float>(slot, L.lse), dvec,
+                                      dqkv, s, d_in_gemm));
                               }));
             } else {
                 // a3: output projection B (into the q columns of dqkv) and the stand-in backward

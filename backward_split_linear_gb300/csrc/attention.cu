@@ -36,8 +36,10 @@
 //                     the key blocks up to the diagonal.
 // dQ has its own kernel (it recomputes S and dP) so that no two CTAs add into
 // the same output: results are the same bits on every run.  D = rowsum(dO * O)
-// comes from a small row kernel first; then dK/dV (on the caller's stream) and
-// dQ (on a side stream forked from it and joined back) run side by side.
+// comes from a small row kernel first, or, inside a stage, from the epilogue of
+// the output projection's dgrad that writes dO; then dK/dV (on the caller's
+// stream) and dQ (on a side stream forked from it and joined back) run side by
+// side.
 //
 // Tiles are 128 rows x d columns of bf16 in 128-byte-swizzled layout: d / 64
 // blocks of 128 rows x 128 bytes (16 KiB each), as TMA writes them.  A tile
@@ -1661,7 +1663,7 @@ SideStream* side_stream() {
 
 template <int D>
 cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const void* da, const float* lse,
-                       float* dvec, void* dqkv, cudaStream_t stream) {
+                       float* dvec, void* dqkv, cudaStream_t stream, bool dvec_ready) {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
@@ -1680,11 +1682,13 @@ cudaError_t bwd_launch(const AttnShape& s, const void* qkv, const void* a, const
     p.ld_out = qkv_w;
     p.lse = const_cast<float*>(lse);
     p.dvec = dvec;
-    const int64_t warps = (static_cast<int64_t>(s.tokens) * s.n_heads + 7) / 8;  // 8 rows per warp
-    attn_causal_rowsum_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(da), static_cast<const uint16_t*>(a), dvec, s.tokens, s.n_heads, s.ld_stat);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (!dvec_ready) {
+        const int64_t warps = (static_cast<int64_t>(s.tokens) * s.n_heads + 7) / 8;  // 8 rows per warp
+        attn_causal_rowsum_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(da), static_cast<const uint16_t*>(a), dvec, s.tokens, s.n_heads, s.ld_stat);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     SideStream* side = side_stream();
     if (!side) return cudaErrorInitializationError;
     std::lock_guard<std::mutex> lock(side->mu);
@@ -1719,10 +1723,11 @@ cudaError_t launch_attention_causal_forward(const AttnShape& s, const void* qkv,
 cudaError_t attention_prepare() { return side_stream() ? cudaSuccess : cudaErrorInitializationError; }
 
 cudaError_t launch_attention_causal_backward(const AttnShape& s, const void* qkv, const void* a, const void* da,
-                                             const float* lse, float* dvec, void* dqkv, cudaStream_t stream) {
+                                             const float* lse, float* dvec, void* dqkv, cudaStream_t stream,
+                                             bool dvec_ready) {
     if (s.tokens <= 0) return cudaSuccess;
-    if (s.head_dim == 128) return bwd_launch<128>(s, qkv, a, da, lse, dvec, dqkv, stream);
-    if (s.head_dim == 64) return bwd_launch<64>(s, qkv, a, da, lse, dvec, dqkv, stream);
+    if (s.head_dim == 128) return bwd_launch<128>(s, qkv, a, da, lse, dvec, dqkv, stream, dvec_ready);
+    if (s.head_dim == 64) return bwd_launch<64>(s, qkv, a, da, lse, dvec, dqkv, stream, dvec_ready);
     return cudaErrorInvalidValue;
 }
 

@@ -96,6 +96,9 @@ struct KParams {
     uint32_t* flags;   // one word per 32 rows of a split tile: 2 epoch (claimed), 2 epoch + 1 (partial written)
     float* partial;    // one float32 256 x 256 tile per split tile
     uint32_t epoch;
+    float* dot;        // row-dot epilogue: [n / dot_cols][ld_dot] float32 sums
+    int64_t ld_dot;
+    int dot_cols;
 };
 
 struct Unit {
@@ -221,6 +224,23 @@ __device__ __forceinline__ void epilogue_pack(const uint32_t (&r)[32], const uin
                                pack_bf16x2(v[6], v[7]));
         }
     }
+}
+
+// Row-dot epilogue: the sum over one 32-column chunk of a row of the stored
+// (bf16-rounded) results times aux, in four interleaved float32 chains.
+__device__ __forceinline__ float row_dot_bf16(const uint32_t (&r)[32], const uint4 (&x0)[4]) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t xw[4] = {x0[j].x, x0[j].y, x0[j].z, x0[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t v = pack_bf16x2(__uint_as_float(r[8 * j + 2 * e]), __uint_as_float(r[8 * j + 2 * e + 1]));
+            acc[e] = fmaf(bf16_lo(v), bf16_lo(xw[e]), acc[e]);
+            acc[e] = fmaf(bf16_hi(v), bf16_hi(xw[e]), acc[e]);
+        }
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 // Epilogue of one 32-column chunk of row m, written straight to global memory.
@@ -936,12 +956,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
+                float row_dot = 0.f;  // row-dot epilogue: this row's sum over the current column group
     #pragma unroll 1
                 for (int c = 0; c < unit_chunks; ++c) {
                     const int n = n_base + c * 32;
                     const bool ok = run_epi && n < p.n;
                     uint4 x0[4];
-                    if constexpr (EPI == static_cast<int>(Epilogue::AddResidual)) {
+                    if constexpr (EPI == static_cast<int>(Epilogue::AddResidual) ||
+                                  EPI == static_cast<int>(Epilogue::StoreBf16RowDot)) {
                         if (ok) {
                             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.aux) +
                                                                               static_cast<int64_t>(m) * p.ld_aux + n);
@@ -984,6 +1006,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
                                 r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
                                 r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                            }
+                        }
+                        if constexpr (EPI == static_cast<int>(Epilogue::StoreBf16RowDot)) {
+                            // a column group never crosses a unit (128 divides
+                            // n_base and is a multiple of dot_cols), so its
+                            // chunks are all this thread's, in order
+                            if (ok) row_dot += row_dot_bf16(r, x0);
+                            if ((n + 32) % p.dot_cols == 0) {
+                                if (ok) p.dot[static_cast<int64_t>(n / p.dot_cols) * p.ld_dot + m] = row_dot;
+                                row_dot = 0.f;
                             }
                         }
                         // The box is stored when any of the warp's rows lies inside
@@ -1265,6 +1297,7 @@ cudaError_t dispatch_pair(const GemmArgs& g, const PairGroup& G, cudaStream_t st
     constexpr int kSwiglu = static_cast<int>(Epilogue::SwigluBwd);
     constexpr int kAccum = static_cast<int>(Epilogue::AccumF32);
     constexpr int kSwigluFwd = static_cast<int>(Epilogue::SwigluFwd);
+    constexpr int kRowDot = static_cast<int>(Epilogue::StoreBf16RowDot);
     switch (g.kind) {
         case GemmKind::Forward:
             if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, false, kStore>(G, stream);
@@ -1274,6 +1307,7 @@ cudaError_t dispatch_pair(const GemmArgs& g, const PairGroup& G, cudaStream_t st
         case GemmKind::BackwardInput:
             if (g.epi == Epilogue::StoreBf16) return launch_pair_variant<false, true, kStore>(G, stream);
             if (g.epi == Epilogue::SwigluBwd) return launch_pair_variant<false, true, kSwiglu>(G, stream);
+            if (g.epi == Epilogue::StoreBf16RowDot) return launch_pair_variant<false, true, kRowDot>(G, stream);
             break;
         case GemmKind::BackwardWeight:
             if (g.epi == Epilogue::AccumF32) return launch_pair_variant<true, true, kAccum>(G, stream);
@@ -1326,7 +1360,7 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
                     CUtensorMap* mx, KParams& p, bool& pair) {
     const int sms = sm_count();
     // A CTA pair takes 256 x 256 tiles; small outputs keep the one-CTA kernel.
-    pair = g.m >= kPairM && g.n >= kPairN;
+    pair = gemm_takes_pair(g.m, g.n);
     const int tile_m = pair ? kPairM : BM;
     const int tile_n = pair ? kPairN : kBN;
     const uint32_t b_rows = pair ? kHalf : kBN;  // rows of a K-major B box
@@ -1343,8 +1377,17 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
             break;
     }
     // Output of the CTA-pair kernel's TMA stores (bf16) and reduce-adds (float32).
-    if (ok && pair && (g.epi == Epilogue::StoreBf16 || g.epi == Epilogue::AddResidual))
+    if (ok && pair &&
+        (g.epi == Epilogue::StoreBf16 || g.epi == Epilogue::AddResidual || g.epi == Epilogue::StoreBf16RowDot))
         ok = encode_map(&mo, g.out, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    // Row dots: every column group lies inside one 128-column half of a tile
+    // (so inside one work unit, wide or narrow), and the per-row reads of aux
+    // are 16-byte loads.
+    if (g.epi == Epilogue::StoreBf16RowDot &&
+        (!pair || g.kind != GemmKind::BackwardInput || !g.aux || !g.dot || g.ld_dot < g.m ||
+         (g.dot_cols != 32 && g.dot_cols != 64 && g.dot_cols != 128) || g.n % g.dot_cols != 0 || g.ld_aux < g.n ||
+         g.ld_aux % 8 != 0 || reinterpret_cast<uintptr_t>(g.aux) % 16 != 0))
+        return cudaErrorInvalidValue;
     if (ok && pair && g.epi == Epilogue::AccumF32)
         ok = encode_map(&mo, g.out, g.m, g.n, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
@@ -1418,7 +1461,8 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
     // QKV projection 141.0 -> 134.4 us, F of the O projection with its
     // residual 105.1 -> 96.6 us.
     if (allow_split && pair && p.split == 1 &&
-        (g.epi == Epilogue::StoreBf16 || g.epi == Epilogue::AddResidual || g.epi == Epilogue::AccumF32)) {
+        (g.epi == Epilogue::StoreBf16 || g.epi == Epilogue::AddResidual || g.epi == Epilogue::AccumF32 ||
+         g.epi == Epilogue::StoreBf16RowDot)) {
         const int pairs = pair_max_clusters();
         const int rem = pairs > 0 ? p.num_tiles % pairs : 0;
         if (rem > 0 && 2 * rem <= pairs) {
@@ -1435,6 +1479,9 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
     p.aux = g.aux;
     p.ld_aux = g.ld_aux;
     p.ffn = g.ffn;
+    p.dot = g.dot;
+    p.ld_dot = g.ld_dot;
+    p.dot_cols = g.dot_cols;
     p.status = status_word();
     p.mn_lbo = kMnBlockBytes;
     p.mn_sbo = 1024;
@@ -1443,6 +1490,8 @@ cudaError_t prepare(const GemmArgs& g, bool allow_split, CUtensorMap& ma, CUtens
 }
 
 }  // namespace
+
+bool gemm_takes_pair(int m, int n) { return m >= kPairM && n >= kPairN; }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     if (g.m <= 0 || g.n <= 0 || g.k <= 0) return cudaSuccess;

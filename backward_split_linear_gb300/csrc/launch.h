@@ -22,6 +22,10 @@ enum class Epilogue : int {
     AccumF32 = 3,      // out f32 += acc
     SwigluFwd = 4,     // b = [W_gate; W_up] (2 ffn rows): out = [g | u] (bf16, row stride ldo) and
                        // out2 = silu(g) u from the bf16 g and u (row stride ldo2); n = 2 ffn
+    StoreBf16RowDot = 5,  // out bf16 = acc, and for every row m and every group j of dot_cols output
+                          // columns dot[j ld_dot + m] = sum over the group of bf16(acc) aux (bf16, row
+                          // stride ld_aux): the attention backward's D = rowsum(dO * O) per head when
+                          // out is dO and aux is O.  CTA-pair kernel, BackwardInput only
 };
 
 struct GemmArgs {
@@ -52,6 +56,11 @@ struct GemmArgs {
     uint32_t* split_flags;
     float* split_partial;
     int split_tiles;
+    // StoreBf16RowDot: float32 sums, one row of m per column group (dot_cols is
+    // 32, 64 or 128 and divides n; aux 16-byte aligned, ld_aux a multiple of 8).
+    float* dot;
+    int64_t ld_dot;
+    int dot_cols;
 };
 
 constexpr size_t kSplitTileFlagBytes = 8 * 4;            // one word per 32 rows of a 256 x 256 tile
@@ -61,6 +70,9 @@ constexpr size_t kSplitTilePartialBytes = 256 * 256 * 4;  // one float32 tile
 constexpr int kSplitMaxTiles = 64;
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
+// Whether an m x n output takes the CTA-pair kernel (the one that has the
+// StoreBf16RowDot epilogue).
+bool gemm_takes_pair(int m, int n);
 
 // Up to kMaxGroup independent GEMMs in one launch when they all take the
 // CTA-pair kernel with the same layouts and epilogue (else one launch each).
@@ -115,9 +127,12 @@ cudaError_t launch_attention_causal_forward(const AttnShape& s, const void* qkv,
                                             cudaStream_t stream);
 // Writes all of dqkv (dq, dk, dv); dvec is scratch of the lse's shape.  Runs the
 // dK/dV kernel on `stream` and the dQ kernel on a per-device side stream forked
-// from it and joined back.
+// from it and joined back.  With dvec_ready, dvec already holds D = rowsum(da * a)
+// per head (from the epilogue of the GEMM that wrote da) and the row kernel that
+// forms it is skipped.
 cudaError_t launch_attention_causal_backward(const AttnShape& s, const void* qkv, const void* a, const void* da,
-                                             const float* lse, float* dvec, void* dqkv, cudaStream_t stream);
+                                             const float* lse, float* dvec, void* dqkv, cudaStream_t stream,
+                                             bool dvec_ready = false);
 // Creates the current device's side stream, events and dQ tile counter ahead
 // of the first backward (a stage calls it at its first forward, so that nothing
 // is created or allocated while the caller's stream may be capturing a graph).
