@@ -469,13 +469,15 @@ zb_status zb_stage_stash_view(zb_stage_t st, int32_t mb, int32_t layer, int32_t 
  * ---------------------------------------------------------------------- */
 typedef enum {
     ZB_KCLASS_GEMM_FORWARD = 0,      /* F GEMMs */
-    ZB_KCLASS_GEMM_BACKWARD_INPUT,   /* B GEMMs, incl. the fused SwiGLU backward */
+    ZB_KCLASS_GEMM_BACKWARD_INPUT,   /* B GEMMs, incl. the fused SwiGLU backward and the causal
+                                        attention's D in the output projection's dgrad */
     ZB_KCLASS_GEMM_BACKWARD_WEIGHT,  /* W GEMMs (float32 accumulation) */
     ZB_KCLASS_ROW_BACKWARD_INPUT,    /* B row kernels: RMSNorm backward, stand-in backward */
     ZB_KCLASS_ROW_BACKWARD_WEIGHT,   /* W row kernels: gamma-gradient reduction */
     ZB_KCLASS_ROW_FORWARD,           /* F row kernels */
     ZB_KCLASS_ATTN_FORWARD,          /* F causal attention */
-    ZB_KCLASS_ATTN_BACKWARD,         /* B causal attention (rowsum, dK/dV, dQ kernels) */
+    ZB_KCLASS_ATTN_BACKWARD,         /* B causal attention (dK/dV and dQ kernels, and the rowsum kernel
+                                        when the output projection's dgrad does not form D) */
     ZB_KCLASS_STASH_COPY,            /* the stash copies of the caller's x (F) and dy (B):
                                         device-to-device cudaMemcpyAsync, not a kernel of the
                                         library (time and bytes count, launches do not) */
