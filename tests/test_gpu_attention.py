@@ -201,7 +201,10 @@ CAUSAL_TF = dict(kind="transformer", n_layers=2, hidden=256, ffn=512, n_heads=4,
 @pytest.mark.parametrize("seq_len,tokens", [(0, [300, 128]), (128, [384, 200])])
 def test_causal_stage_against_oracle(seq_len, tokens):
     """A two-layer stage with the causal attention core: F -> B -> W per microbatch,
-    dx and every weight gradient against the oracle at the causal two-layer stage tolerance."""
+    dx and every weight gradient against the oracle at the causal two-layer stage tolerance.
+    Both ways of forming D = rowsum(dO * O) run: a microbatch of 256 tokens or more takes the
+    CTA-pair GEMM for the output projection's dgrad, whose epilogue forms D (300, 384); a
+    smaller one takes the one-CTA GEMM and the row kernel (128, 200)."""
     c = CAUSAL_TF
     inp = synth.stage_inputs(c["kind"], 2, 256, 512, 4, 2, 64, n_mb=len(tokens), seed=21, tokens_per_mb=tokens)
     st = Stage.from_synth(c["kind"], 2, 256, 512, 4, 2, 64, 1e-5, max(tokens), len(tokens), inp["params"],
